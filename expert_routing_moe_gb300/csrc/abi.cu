@@ -1,0 +1,163 @@
+// abi.cu -- the extern "C" entry points of moe_gb300.h: host-side argument
+// checks, then asynchronous launches on the caller's stream.  Nothing here
+// allocates, frees or synchronises.
+#include <cuda_runtime.h>
+
+#include "../../include/moe_gb300.h"
+#include "launch.h"
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+inline moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool sere_ok(const moe_sere_params* p, int N, int k) {
+    return p->sim != nullptr && p->k_primary >= 1 && p->k_primary <= k && !(p->rho != p->rho) && N <= MOE_MAX_EXPERTS;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_route(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int R, int k,
+                       uint32_t flags, float* logits, int32_t* ids, float* gates, const moe_sere_params* sere,
+                       moe_dev_status* st, void* stream) {
+    if (T < 0 || N < 1 || N > MOE_MAX_EXPERTS || R < 1 || R > MOE_MAX_RANKS || R > N || k < 1 || k > R)
+        return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_ROUTE_FROM_LOGITS | MOE_ROUTE_RENORM_TOPK)) return MOE_ERR_INVALID_ARG;
+    if (sere != nullptr && (R != k || !sere_ok(sere, N, k))) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;  // nothing to rank; per-token pointers may be NULL
+    if (logits == nullptr || ids == nullptr || gates == nullptr) return MOE_ERR_INVALID_ARG;
+    const bool from_logits = (flags & MOE_ROUTE_FROM_LOGITS) != 0;
+    if (!from_logits) {
+        if (x == nullptr || w_router == nullptr || H < 1) return MOE_ERR_INVALID_ARG;
+        if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+        if (x_dtype == MOE_DTYPE_BF16 && (H % 8 != 0)) return MOE_ERR_UNSUPPORTED;
+        if (x_dtype == MOE_DTYPE_F32 && (H % 4 != 0)) return MOE_ERR_UNSUPPORTED;
+        if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+    }
+    if (sere != nullptr) {
+        if (R != k || !sere_ok(sere, N, k)) return MOE_ERR_INVALID_ARG;
+        if (T > moe::kSereMaxT) return MOE_ERR_UNSUPPORTED;
+    }
+    cudaStream_t s = as_stream(stream);
+    if (!from_logits) {
+        cudaError_t e = moe::launch_router(x, x_dtype, w_router, T, H, N, logits, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    const bool renorm = (flags & MOE_ROUTE_RENORM_TOPK) != 0;
+    if (sere != nullptr) return from_cuda(moe::launch_rank_sere(logits, T, N, k, renorm, ids, gates, *sere, st, s));
+    return from_cuda(moe::launch_rank(logits, T, N, R, k, renorm, ids, gates, st, s));
+}
+
+moe_status_t moe_reroute_sere(int32_t* ids, float* gates, int ld, int T, int N, int k, const moe_sere_params* sere,
+                              moe_dev_status* st, void* stream) {
+    if (ids == nullptr || gates == nullptr || sere == nullptr) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || N < 1 || N > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_RANKS || k > N || ld < k)
+        return MOE_ERR_INVALID_ARG;
+    if (!sere_ok(sere, N, k)) return MOE_ERR_INVALID_ARG;
+    if (T > moe::kSereMaxT) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    return from_cuda(moe::launch_sere(ids, gates, ld, T, N, k, *sere, st, as_stream(stream)));
+}
+
+size_t moe_workspace_size(int op, int T, int H, int I, int N, int k, int R, int capped, int dtype) {
+    if (T < 0 || N < 1 || N > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_RANKS) return 0;
+    if (op == MOE_OP_DISPATCH) return moe::dispatch_workspace(T, N, k, R, capped != 0);
+    if (op == MOE_OP_FFN) {
+        if (H < 1 || I < 1) return 0;
+        return moe::ffn_workspace(T, H, I, N, k, dtype);
+    }
+    return 0;
+}
+
+moe_status_t moe_dispatch_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, int k, int R,
+                                   const float* token_w, float capacity_factor, int32_t* counts, int32_t* offsets,
+                                   int32_t* row_token, float* row_gate, int32_t* active, int32_t* out_ids,
+                                   float* out_gates, int32_t* slot_row, uint8_t* slot_status, int64_t* load_q,
+                                   int64_t* cap_q, void* workspace, size_t ws_bytes, moe_dev_status* st,
+                                   void* stream) {
+    if (T < 0 || N < 1 || N > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_RANKS || k > N) return MOE_ERR_INVALID_ARG;
+    if (counts == nullptr || offsets == nullptr || active == nullptr ||
+        ((ids == nullptr || gates == nullptr || row_token == nullptr || row_gate == nullptr) && T > 0))
+        return MOE_ERR_INVALID_ARG;
+    if (capacity_factor != capacity_factor) return MOE_ERR_INVALID_ARG;
+    const bool capped = capacity_factor > 0.f;
+    if (capped) {
+        if (R < k || R > MOE_MAX_RANKS || R > N || ld < R) return MOE_ERR_INVALID_ARG;
+        if (T > moe::kCapacityMaxT) return MOE_ERR_UNSUPPORTED;
+    } else if (ld < k) {
+        return MOE_ERR_INVALID_ARG;
+    }
+    const size_t need = moe::dispatch_workspace(T, N, k, R, capped);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_dispatch(ids, gates, ld, T, N, k, R, token_w, capacity_factor, counts, offsets,
+                                          row_token, row_gate, active, out_ids, out_gates, slot_row, slot_status,
+                                          load_q, cap_q, workspace, st, as_stream(stream)));
+}
+
+moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const void* w_up, const void* w_down,
+                             int T, int H, int I, int N, int k, const int32_t* offsets, const int32_t* row_token,
+                             const float* row_gate, const int32_t* active, uint32_t flags, float* out,
+                             void* workspace, size_t ws_bytes, moe_dev_status* st, void* stream) {
+    if (T < 0 || H < 1 || I < 1 || N < 1 || N > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_RANKS || k > N)
+        return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_FFN_FUSE_COMBINE | MOE_FFN_ZERO_Y)) return MOE_ERR_INVALID_ARG;
+    if (dtype != MOE_DTYPE_F32 && dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;  // no rows, nothing to write
+    if (x == nullptr || w_gate == nullptr || w_up == nullptr || w_down == nullptr || offsets == nullptr ||
+        row_token == nullptr || row_gate == nullptr || active == nullptr || out == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    if (dtype == MOE_DTYPE_F32) {
+        return from_cuda(moe::launch_ffn_f32(static_cast<const float*>(x), static_cast<const float*>(w_gate),
+                                             static_cast<const float*>(w_up), static_cast<const float*>(w_down), T,
+                                             H, I, N, k, offsets, row_token, row_gate, active, flags, out, st, s));
+    }
+    if (dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+    if (H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(out))
+        return MOE_ERR_INVALID_ARG;
+    // tensor-map extents are 32-bit row counts
+    if (static_cast<long long>(N) * I > 0x7fffffffLL || static_cast<long long>(N) * H > 0x7fffffffLL ||
+        static_cast<long long>(T) * k > 0x7fffffffLL)
+        return MOE_ERR_UNSUPPORTED;
+    const size_t need = moe::ffn_workspace(T, H, I, N, k, dtype);
+    if (workspace == nullptr || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_ffn_bf16(x, w_gate, w_up, w_down, T, H, I, N, k, offsets, row_token, row_gate,
+                                          active, flags, out, workspace, st, s));
+}
+
+moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const float* slot_gate, int T, int H, int k,
+                         float* y, void* stream) {
+    if (T < 0 || H < 1 || k < 1 || k > MOE_MAX_RANKS) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (rows_out == nullptr || slot_row == nullptr || slot_gate == nullptr || y == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine(rows_out, slot_row, slot_gate, T, H, k, y, as_stream(stream)));
+}
+
+const char* moe_status_string(int code, int device) {
+    if (device) {
+        switch (code) {
+            case MOE_DEV_OK: return "ok";
+            case MOE_DEV_NONFINITE: return "non-finite router logit or token weight";
+            case MOE_DEV_TIMEOUT: return "on-chip wait timed out";
+            case MOE_DEV_BAD_INDEX: return "expert id or row index out of range";
+            default: return "unknown device status";
+        }
+    }
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported size or option";
+        case MOE_ERR_CUDA: return "CUDA launch failed";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

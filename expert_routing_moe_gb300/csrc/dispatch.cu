@@ -1,0 +1,485 @@
+// dispatch.cu -- expert-sorted permutation and the capacity-bounded dispatch.
+//
+// Token sets I_j and the straggler bound: "MACS: Modality-Aware Capacity
+// Scaling for Efficient Multimodal MoE Inference", sec. 3.1 Eqs. (2)-(3);
+// weighted load: sec. 3.2 Eq. (6); overflow handling (reroute locally, else
+// drop): Fig. 1 and the sec. 3.4 summary in the introduction.
+//
+// Permutation: rows ordered by (expert asc, token asc).  Because a token
+// holds an expert at most once, a row's position is the expert's start plus
+// the number of earlier tokens holding that expert; that count comes from a
+// per-expert presence bitmap over the tokens of a 1024-token block and
+// population counts, so the result is deterministic without any sort.
+//
+// Capacity: loads are integers in 2^-24 units (exact, order-free sums).  Each
+// expert's candidates are sorted by (gate desc, token asc) with a bitonic sort
+// in shared memory and admitted while the running load stays within C.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+constexpr int kBlk = 1024;          // tokens per permutation block (one per thread)
+constexpr int kWordsPerBlk = kBlk / 32;
+constexpr uint8_t kPending = 255;
+
+static inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct DispatchWs {
+    int32_t* blk_start;   // [nblk][N]
+    // capacity mode only
+    unsigned long long* S;
+    int32_t* cnt1;        // [N]
+    int32_t* cnt2;        // [N]
+    uint32_t* bucket1;    // [N][T]
+    uint32_t* bucket2;    // [N][T]
+    long long* load;      // [N]
+    uint8_t* status;      // [T][k]
+    int32_t* wids;        // [T][k]
+    float* wgates;        // [T][k]
+    size_t zero_bytes;    // bytes from S to the end of cnt2 (cleared per call)
+};
+
+static size_t carve(DispatchWs* w, void* base, int T, int N, int k, bool capped) {
+    const int nblk = (T + kBlk - 1) / kBlk;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    size_t o_blk = take(sizeof(int32_t) * static_cast<size_t>(nblk > 0 ? nblk : 1) * N);
+    size_t o_S = 0, o_c1 = 0, o_c2 = 0, o_b1 = 0, o_b2 = 0, o_ld = 0, o_st = 0, o_id = 0, o_g = 0;
+    if (capped) {
+        o_S = take(sizeof(unsigned long long));
+        o_c1 = take(sizeof(int32_t) * N);
+        o_c2 = take(sizeof(int32_t) * N);
+        o_b1 = take(sizeof(uint32_t) * static_cast<size_t>(N) * (T > 0 ? T : 1));
+        o_b2 = take(sizeof(uint32_t) * static_cast<size_t>(N) * (T > 0 ? T : 1));
+        o_ld = take(sizeof(long long) * N);
+        o_st = take(static_cast<size_t>(T > 0 ? T : 1) * k);
+        o_id = take(sizeof(int32_t) * static_cast<size_t>(T > 0 ? T : 1) * k);
+        o_g = take(sizeof(float) * static_cast<size_t>(T > 0 ? T : 1) * k);
+    }
+    if (w != nullptr) {
+        char* b = static_cast<char*>(base);
+        w->blk_start = reinterpret_cast<int32_t*>(b + o_blk);
+        if (capped) {
+            w->S = reinterpret_cast<unsigned long long*>(b + o_S);
+            w->cnt1 = reinterpret_cast<int32_t*>(b + o_c1);
+            w->cnt2 = reinterpret_cast<int32_t*>(b + o_c2);
+            w->bucket1 = reinterpret_cast<uint32_t*>(b + o_b1);
+            w->bucket2 = reinterpret_cast<uint32_t*>(b + o_b2);
+            w->load = reinterpret_cast<long long*>(b + o_ld);
+            w->status = reinterpret_cast<uint8_t*>(b + o_st);
+            w->wids = reinterpret_cast<int32_t*>(b + o_id);
+            w->wgates = reinterpret_cast<float*>(b + o_g);
+            w->zero_bytes = o_b1 - o_S;
+        }
+    }
+    return off;
+}
+
+size_t dispatch_workspace(int T, int N, int k, int R, bool capped) {
+    (void)R;
+    return carve(nullptr, nullptr, T, N, k, capped);
+}
+
+// ---------------------------------------------------------------------------
+// Permutation
+// ---------------------------------------------------------------------------
+// Marks, for the 1024-token block `b`, bit (t mod 1024) of expert e's bitmap
+// for every slot of token t holding e.
+__device__ void presence_bits(const int32_t* __restrict__ ids, int ld, int T, int N, int k, int b, uint32_t* bits,
+                              moe_dev_status* st) {
+    for (int i = threadIdx.x; i < N * kWordsPerBlk; i += blockDim.x) bits[i] = 0u;
+    __syncthreads();
+    const int t = b * kBlk + threadIdx.x;
+    if (t < T) {
+        for (int r = 0; r < k; ++r) {
+            const int e = ids[static_cast<size_t>(t) * ld + r];
+            if (e >= N) report(st, MOE_DEV_BAD_INDEX, e);
+            if (e >= 0 && e < N) atomicOr(&bits[e * kWordsPerBlk + (threadIdx.x >> 5)], 1u << (threadIdx.x & 31));
+        }
+    }
+    __syncthreads();
+}
+
+__device__ int block_count(const uint32_t* bits, int e) {
+    int c = 0;
+    for (int w = 0; w < kWordsPerBlk; ++w) c += __popc(bits[e * kWordsPerBlk + w]);
+    return c;
+}
+
+// Writes the rows of block b given the absolute start row of each expert in
+// this block (start[e]).
+__device__ void write_rows(const int32_t* __restrict__ ids, const float* __restrict__ gates, int ld, int T, int N,
+                           int k, int b, const uint32_t* bits, const int32_t* start, int32_t* __restrict__ row_token,
+                           float* __restrict__ row_gate, int32_t* __restrict__ out_ids,
+                           float* __restrict__ out_gates, int32_t* __restrict__ slot_row) {
+    const int t = b * kBlk + threadIdx.x;
+    if (t >= T) return;
+    const int w0 = threadIdx.x >> 5;
+    const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
+    for (int r = 0; r < k; ++r) {
+        const size_t si = static_cast<size_t>(t) * ld + r;
+        const size_t so = static_cast<size_t>(t) * k + r;
+        const int e = ids[si];
+        const float g = gates[si];
+        int row = -1;
+        if (e >= 0 && e < N) {
+            int c = 0;
+            for (int w = 0; w < w0; ++w) c += __popc(bits[e * kWordsPerBlk + w]);
+            c += __popc(bits[e * kWordsPerBlk + w0] & below);
+            row = start[e] + c;
+            row_token[row] = t;
+            row_gate[row] = g;
+        }
+        if (slot_row) slot_row[so] = row;
+        if (out_ids) out_ids[so] = (row >= 0) ? e : -1;
+        if (out_gates) out_gates[so] = (row >= 0) ? g : 0.f;
+    }
+}
+
+// Exclusive scan of counts over experts; fills offsets and the active list.
+// Runs in one CTA with blockDim >= N.
+__device__ void scan_experts(const int* cnt_total, int N, int32_t* counts, int32_t* offsets, int32_t* active,
+                             int* s_off) {
+    // N <= 256: a simple two-level scan by the first warp
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int run = 0, arun = 0;
+        for (int base = 0; base < N; base += 32) {
+            const int e = base + lane;
+            const int c = (e < N) ? cnt_total[e] : 0;
+            const int a = (c > 0) ? 1 : 0;
+            int inc = c, ainc = a;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(kFull, inc, off);
+                const int av = __shfl_up_sync(kFull, ainc, off);
+                if (lane >= off) {
+                    inc += v;
+                    ainc += av;
+                }
+            }
+            if (e < N) {
+                s_off[e] = run + inc - c;
+                counts[e] = c;
+                offsets[e] = run + inc - c;
+                if (a) active[1 + arun + ainc - 1] = e;
+            }
+            run += __shfl_sync(kFull, inc, 31);
+            arun += __shfl_sync(kFull, ainc, 31);
+        }
+        if (lane == 0) {
+            offsets[N] = run;
+            active[0] = arun;
+        }
+    }
+}
+
+// Single-block permutation (T <= 1024): presence, counts, scan and rows in one launch.
+__global__ void __launch_bounds__(kBlk) permute_single_kernel(const int32_t* __restrict__ ids,
+                                                              const float* __restrict__ gates, int ld, int T, int N,
+                                                              int k, int32_t* counts, int32_t* offsets,
+                                                              int32_t* row_token, float* row_gate, int32_t* active,
+                                                              int32_t* out_ids, float* out_gates,
+                                                              int32_t* slot_row, moe_dev_status* st) {
+    __shared__ uint32_t bits[MOE_MAX_EXPERTS * kWordsPerBlk];
+    __shared__ int cnt[MOE_MAX_EXPERTS];
+    __shared__ int start[MOE_MAX_EXPERTS];
+    presence_bits(ids, ld, T, N, k, 0, bits, st);
+    for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = block_count(bits, e);
+    __syncthreads();
+    scan_experts(cnt, N, counts, offsets, active, start);
+    __syncthreads();
+    write_rows(ids, gates, ld, T, N, k, 0, bits, start, row_token, row_gate, out_ids, out_gates, slot_row);
+}
+
+// Multi-block permutation, pass 1: per-block expert counts.
+__global__ void __launch_bounds__(kBlk) permute_count_kernel(const int32_t* __restrict__ ids, int ld, int T, int N,
+                                                             int k, int32_t* __restrict__ blk_cnt,
+                                                             moe_dev_status* st) {
+    __shared__ uint32_t bits[MOE_MAX_EXPERTS * kWordsPerBlk];
+    presence_bits(ids, ld, T, N, k, blockIdx.x, bits, st);
+    for (int e = threadIdx.x; e < N; e += blockDim.x)
+        blk_cnt[static_cast<size_t>(blockIdx.x) * N + e] = block_count(bits, e);
+}
+
+// Pass 2 (one CTA): totals, offsets, active list; blk_cnt becomes the
+// absolute start row of each (block, expert).
+__global__ void __launch_bounds__(256) permute_scan_kernel(int nblk, int N, int32_t* __restrict__ blk_cnt,
+                                                           int32_t* counts, int32_t* offsets, int32_t* active) {
+    __shared__ int tot[MOE_MAX_EXPERTS];
+    __shared__ int start[MOE_MAX_EXPERTS];
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int run = 0;
+        for (int b = 0; b < nblk; ++b) {
+            const int c = blk_cnt[static_cast<size_t>(b) * N + e];
+            blk_cnt[static_cast<size_t>(b) * N + e] = run;
+            run += c;
+        }
+        tot[e] = run;
+    }
+    __syncthreads();
+    scan_experts(tot, N, counts, offsets, active, start);
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x)
+        for (int b = 0; b < nblk; ++b) blk_cnt[static_cast<size_t>(b) * N + e] += start[e];
+}
+
+// Pass 3: rows of each block.
+__global__ void __launch_bounds__(kBlk) permute_rows_kernel(const int32_t* __restrict__ ids,
+                                                            const float* __restrict__ gates, int ld, int T, int N,
+                                                            int k, const int32_t* __restrict__ blk_start,
+                                                            int32_t* row_token, float* row_gate, int32_t* out_ids,
+                                                            float* out_gates, int32_t* slot_row,
+                                                            moe_dev_status* st) {
+    __shared__ uint32_t bits[MOE_MAX_EXPERTS * kWordsPerBlk];
+    __shared__ int start[MOE_MAX_EXPERTS];
+    for (int e = threadIdx.x; e < N; e += blockDim.x) start[e] = blk_start[static_cast<size_t>(blockIdx.x) * N + e];
+    presence_bits(ids, ld, T, N, k, blockIdx.x, bits, nullptr);
+    write_rows(ids, gates, ld, T, N, k, blockIdx.x, bits, start, row_token, row_gate, out_ids, out_gates, slot_row);
+    (void)st;
+}
+
+static cudaError_t launch_permute(const int32_t* ids, const float* gates, int ld, int T, int N, int k,
+                                  int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,
+                                  int32_t* active, int32_t* out_ids, float* out_gates, int32_t* slot_row,
+                                  int32_t* blk_start, moe_dev_status* st, cudaStream_t s) {
+    const int nblk = (T + kBlk - 1) / kBlk;
+    if (nblk <= 1) {
+        permute_single_kernel<<<1, kBlk, 0, s>>>(ids, gates, ld, T, N, k, counts, offsets, row_token, row_gate,
+                                                 active, out_ids, out_gates, slot_row, st);
+        return cudaGetLastError();
+    }
+    permute_count_kernel<<<nblk, kBlk, 0, s>>>(ids, ld, T, N, k, blk_start, st);
+    permute_scan_kernel<<<1, 256, 0, s>>>(nblk, N, blk_start, counts, offsets, active);
+    permute_rows_kernel<<<nblk, kBlk, 0, s>>>(ids, gates, ld, T, N, k, blk_start, row_token, row_gate, out_ids,
+                                             out_gates, slot_row, st);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Capacity mode
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ long long fixed_weight(float w) {
+    return static_cast<long long>(rintf(__fmul_rn(w, 16777216.0f)));
+}
+
+__device__ __forceinline__ long long capacity_value(unsigned long long S, int k, float gamma, int N) {
+    const double a = __dmul_rn(static_cast<double>(S), static_cast<double>(k));
+    const double b = __dmul_rn(a, static_cast<double>(gamma));
+    return static_cast<long long>(floor(__ddiv_rn(b, static_cast<double>(N))));
+}
+
+// Phase-1 bucketing: fixed-point weights, total S, copies of the slots, and
+// each slot appended to its expert's bucket (order fixed later by the sort).
+__global__ void cap_bucket_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gates, int ld, int T,
+                                  int N, int k, const float* __restrict__ token_w, DispatchWs w, moe_dev_status* st) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    float wt = token_w ? token_w[t] : 1.0f;
+    if (!isfinite(wt) || wt < 0.f) {
+        report(st, MOE_DEV_NONFINITE, t);
+        wt = 0.f;
+    }
+    atomicAdd(w.S, static_cast<unsigned long long>(fixed_weight(wt)));
+    for (int r = 0; r < k; ++r) {
+        const size_t si = static_cast<size_t>(t) * ld + r;
+        const size_t so = static_cast<size_t>(t) * k + r;
+        const int e = ids[si];
+        w.wids[so] = e;
+        w.wgates[so] = gates[si];
+        w.status[so] = kPending;
+        if (e < 0 || e >= N) {
+            report(st, MOE_DEV_BAD_INDEX, e);
+            w.status[so] = MOE_SLOT_DROPPED;
+            w.wids[so] = -1;
+            continue;
+        }
+        const int pos = atomicAdd(&w.cnt1[e], 1);
+        if (pos >= T) {  // only possible if a token holds the same expert twice
+            report(st, MOE_DEV_BAD_INDEX, e);
+            continue;
+        }
+        w.bucket1[static_cast<size_t>(e) * T + pos] = static_cast<uint32_t>(t) * 16u + static_cast<uint32_t>(r);
+    }
+}
+
+// One CTA per expert: sort its candidates by (gate desc, token asc), admit
+// while load + running weight <= C.  `round` < 0 is phase 1 (candidates are
+// the expert's own slots); round i >= 0 admits overflow offers as rerouted.
+__global__ void __launch_bounds__(1024) cap_admit_kernel(const float* __restrict__ gates, int ld, int T, int N,
+                                                         int k, float gamma, const float* __restrict__ token_w,
+                                                         int round, DispatchWs w) {
+    extern __shared__ unsigned long long keys[];
+    __shared__ long long part[1024];
+    __shared__ unsigned long long admitted_max;
+    const int e = blockIdx.x;
+    const int n = min((round < 0) ? w.cnt1[e] : w.cnt2[e], T);
+    const uint32_t* bucket = ((round < 0) ? w.bucket1 : w.bucket2) + static_cast<size_t>(e) * T;
+    int P2 = 1;
+    while (P2 < n) P2 <<= 1;
+    for (int i = threadIdx.x; i < P2; i += blockDim.x) {
+        unsigned long long key = ~0ull;
+        if (i < n) {
+            const uint32_t tr = bucket[i];
+            const int t = static_cast<int>(tr >> 4), r = static_cast<int>(tr & 15u);
+            const float g = gates[static_cast<size_t>(t) * ld + r];
+            key = (static_cast<unsigned long long>(~__float_as_uint(g)) << 32) | tr;
+        }
+        keys[i] = key;
+    }
+    if (threadIdx.x == 0) admitted_max = 0ull;
+    __syncthreads();
+    for (int size = 2; size <= P2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < P2 / 2; i += blockDim.x) {
+                const int lo = 2 * i - (i & (stride - 1));
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const unsigned long long a = keys[lo], b = keys[hi];
+                if ((a > b) == up) {
+                    keys[lo] = b;
+                    keys[hi] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // running weight in sorted order: each thread owns a contiguous chunk
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int i0 = threadIdx.x * per;
+    long long local = 0;
+    for (int i = i0; i < min(n, i0 + per); ++i) {
+        const int t = static_cast<int>((keys[i] & 0xffffffffull) >> 4);
+        float wt = token_w ? token_w[t] : 1.0f;
+        if (!isfinite(wt) || wt < 0.f) wt = 0.f;
+        local += fixed_weight(wt);
+    }
+    part[threadIdx.x] = local;
+    __syncthreads();
+    // inclusive Hillis-Steele scan over the 1024 chunk sums
+    for (int off = 1; off < 1024; off <<= 1) {
+        const long long v = (threadIdx.x >= off) ? part[threadIdx.x - off] : 0ll;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    const long long C = capacity_value(*w.S, k, gamma, N);
+    const long long base = (round < 0) ? 0ll : w.load[e];
+    long long cum = part[threadIdx.x] - local;
+    unsigned long long best = 0ull;
+    for (int i = i0; i < min(n, i0 + per); ++i) {
+        const uint32_t tr = static_cast<uint32_t>(keys[i] & 0xffffffffull);
+        const int t = static_cast<int>(tr >> 4), r = static_cast<int>(tr & 15u);
+        float wt = token_w ? token_w[t] : 1.0f;
+        if (!isfinite(wt) || wt < 0.f) wt = 0.f;
+        cum += fixed_weight(wt);
+        if (base + cum <= C) {
+            const size_t so = static_cast<size_t>(t) * k + r;
+            if (round < 0) {
+                w.status[so] = MOE_SLOT_KEPT;
+            } else {
+                w.status[so] = MOE_SLOT_REROUTED;
+                w.wids[so] = e;
+            }
+            best = static_cast<unsigned long long>(cum);
+        }
+    }
+    if (best > 0ull) atomicMax(&admitted_max, best);
+    __syncthreads();
+    if (threadIdx.x == 0) w.load[e] = base + static_cast<long long>(admitted_max);
+}
+
+// Overflow round i: each token offers its lowest-rank pending slot to its
+// rank-(k+i) expert.
+__global__ void cap_offer_kernel(const int32_t* __restrict__ ids, int ld, int T, int N, int k, int round,
+                                 DispatchWs w) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    for (int r = 0; r < k; ++r) {
+        if (w.status[static_cast<size_t>(t) * k + r] != kPending) continue;
+        const int c = ids[static_cast<size_t>(t) * ld + k + round];
+        if (c >= 0 && c < N) {
+            const int pos = atomicAdd(&w.cnt2[c], 1);
+            if (pos < T)
+                w.bucket2[static_cast<size_t>(c) * T + pos] = static_cast<uint32_t>(t) * 16u + static_cast<uint32_t>(r);
+        }
+        break;
+    }
+}
+
+// Pending slots are dropped; results are copied out.
+__global__ void cap_finalize_kernel(int T, int N, int k, DispatchWs w, uint8_t* slot_status, int64_t* load_q,
+                                    int64_t* cap_q, float gamma) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < T * k) {
+        if (w.status[i] == kPending) {
+            w.status[i] = MOE_SLOT_DROPPED;
+            w.wids[i] = -1;
+            w.wgates[i] = 0.f;
+        } else if (w.status[i] == MOE_SLOT_DROPPED) {
+            w.wgates[i] = 0.f;
+        }
+        if (slot_status) slot_status[i] = w.status[i];
+    }
+    if (i < N && load_q) load_q[i] = w.load[i];
+    if (i == 0 && cap_q) *cap_q = capacity_value(*w.S, k, gamma, N);
+}
+
+cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int T, int N, int k, int R,
+                            const float* token_w, float capacity_factor, int32_t* counts, int32_t* offsets,
+                            int32_t* row_token, float* row_gate, int32_t* active, int32_t* out_ids,
+                            float* out_gates, int32_t* slot_row, uint8_t* slot_status, int64_t* load_q,
+                            int64_t* cap_q, void* ws, moe_dev_status* st, cudaStream_t s) {
+    const bool capped = capacity_factor > 0.f;
+    DispatchWs w{};
+    carve(&w, ws, T, N, k, capped);
+    if (!capped) {
+        if (T == 0) {
+            cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
+            cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
+            cudaMemsetAsync(active, 0, sizeof(int32_t) * (N + 1), s);
+            return cudaGetLastError();
+        }
+        return launch_permute(ids, gates, ld, T, N, k, counts, offsets, row_token, row_gate, active, out_ids,
+                              out_gates, slot_row, w.blk_start, st, s);
+    }
+    cudaError_t err = cudaMemsetAsync(w.S, 0, w.zero_bytes, s);
+    if (err != cudaSuccess) return err;
+    const int tb = 256;
+    if (T > 0) {
+        cap_bucket_kernel<<<(T + tb - 1) / tb, tb, 0, s>>>(ids, gates, ld, T, N, k, token_w, w, st);
+        size_t P2 = 1;
+        while (P2 < static_cast<size_t>(T)) P2 <<= 1;
+        const size_t smem = P2 * sizeof(unsigned long long);
+        err = cudaFuncSetAttribute(cap_admit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        cap_admit_kernel<<<N, 1024, smem, s>>>(gates, ld, T, N, k, capacity_factor, token_w, -1, w);
+        for (int i = 0; i + k < R; ++i) {
+            cudaMemsetAsync(w.cnt2, 0, sizeof(int32_t) * N, s);
+            cap_offer_kernel<<<(T + tb - 1) / tb, tb, 0, s>>>(ids, ld, T, N, k, i, w);
+            cap_admit_kernel<<<N, 1024, smem, s>>>(gates, ld, T, N, k, capacity_factor, token_w, i, w);
+        }
+    }
+    const int nfin = (T * k > N ? T * k : N);
+    cap_finalize_kernel<<<(nfin + tb - 1) / tb, tb, 0, s>>>(T, N, k, w, slot_status, load_q, cap_q, capacity_factor);
+    if (out_ids) cudaMemcpyAsync(out_ids, w.wids, sizeof(int32_t) * T * k, cudaMemcpyDeviceToDevice, s);
+    if (out_gates) cudaMemcpyAsync(out_gates, w.wgates, sizeof(float) * T * k, cudaMemcpyDeviceToDevice, s);
+    if (T == 0) {
+        cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
+        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
+        cudaMemsetAsync(active, 0, sizeof(int32_t) * (N + 1), s);
+        return cudaGetLastError();
+    }
+    return launch_permute(w.wids, w.wgates, k, T, N, k, counts, offsets, row_token, row_gate, active, nullptr,
+                          nullptr, slot_row, w.blk_start, st, s);
+}
+
+}  // namespace moe

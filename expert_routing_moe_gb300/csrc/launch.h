@@ -1,0 +1,46 @@
+// launch.h -- internal host-side launchers shared by the C-ABI layer (abi.cu)
+// and the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+// ---- routing (router.cu) ----
+cudaError_t launch_router(const void* x, int x_dtype, const float* w_router, int T, int H, int N, float* logits,
+                          cudaStream_t s);
+cudaError_t launch_rank(const float* logits, int T, int N, int R, int k, bool renorm, int32_t* ids, float* gates,
+                        moe_dev_status* st, cudaStream_t s);
+cudaError_t launch_rank_sere(const float* logits, int T, int N, int k, bool renorm, int32_t* ids, float* gates,
+                             const moe_sere_params& p, moe_dev_status* st, cudaStream_t s);
+cudaError_t launch_sere(int32_t* ids, float* gates, int ld, int T, int N, int k, const moe_sere_params& p,
+                        moe_dev_status* st, cudaStream_t s);
+constexpr int kSereMaxT = 4096;
+
+// ---- dispatch (dispatch.cu) ----
+size_t dispatch_workspace(int T, int N, int k, int R, bool capped);
+cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int T, int N, int k, int R,
+                            const float* token_w, float capacity_factor, int32_t* counts, int32_t* offsets,
+                            int32_t* row_token, float* row_gate, int32_t* active, int32_t* out_ids,
+                            float* out_gates, int32_t* slot_row, uint8_t* slot_status, int64_t* load_q,
+                            int64_t* cap_q, void* ws, moe_dev_status* st, cudaStream_t s);
+constexpr int kCapacityMaxT = 16384;
+
+// ---- FFN (ffn_simt.cu, ffn_tc.cu) ----
+size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype);
+cudaError_t launch_ffn_f32(const float* x, const float* wg, const float* wu, const float* wd, int T, int H, int I,
+                           int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
+                           const int32_t* active, uint32_t flags, float* out, moe_dev_status* st,
+                           cudaStream_t s);
+cudaError_t launch_ffn_bf16(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
+                            int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
+                            const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
+                            cudaStream_t s);
+cudaError_t launch_combine(const float* rows_out, const int32_t* slot_row, const float* slot_gate, int T, int H,
+                           int k, float* y, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,91 @@
+"""A resident MoE layer: device weights, preallocated buffers and the C-ABI
+calls of one forward pass in order (router + rank (+ SERE) -> dispatch
+(+ capacity) -> grouped FFN with the combine fused in).  Buffers are sized
+once for a maximum batch, so a forward pass allocates nothing and can be
+captured in a CUDA graph."""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _abi as abi
+
+
+class MoELayer:
+    def __init__(self, w_router: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                 k: int, max_tokens: int, sim: Optional[torch.Tensor] = None, protect: Optional[torch.Tensor] = None,
+                 k_primary: int = 2, rho: float = 0.5, R: Optional[int] = None, capacity_factor: float = 0.0,
+                 renorm: bool = False):
+        dev = w_gate.device
+        self.w_router, self.w_gate, self.w_up, self.w_down = w_router, w_gate, w_up, w_down
+        self.N, self.I, self.H = w_gate.shape
+        self.k = k
+        self.R = R if R is not None else k
+        self.max_T = max_tokens
+        self.sim, self.protect = sim, protect
+        self.k_primary, self.rho = k_primary, rho
+        self.capacity_factor = capacity_factor
+        self.flags = abi.MOE_ROUTE_RENORM_TOPK if renorm else 0
+        T, N, R, H = max_tokens, self.N, self.R, self.H
+        i32, f32 = torch.int32, torch.float32
+        self.logits = torch.empty(T, N, dtype=f32, device=dev)
+        self.ids = torch.empty(T, R, dtype=i32, device=dev)
+        self.gates = torch.empty(T, R, dtype=f32, device=dev)
+        self.counts = torch.empty(N, dtype=i32, device=dev)
+        self.offsets = torch.empty(N + 1, dtype=i32, device=dev)
+        self.active = torch.empty(N + 1, dtype=i32, device=dev)
+        self.row_token = torch.empty(max(T * k, 1), dtype=i32, device=dev)
+        self.row_gate = torch.empty(max(T * k, 1), dtype=f32, device=dev)
+        self.out_ids = torch.empty(T, k, dtype=i32, device=dev)
+        self.out_gates = torch.empty(T, k, dtype=f32, device=dev)
+        self.slot_status = torch.empty(T, k, dtype=torch.uint8, device=dev)
+        self.load_q = torch.empty(N, dtype=torch.int64, device=dev)
+        self.cap_q = torch.empty(1, dtype=torch.int64, device=dev)
+        self.union_bitmap = torch.empty((N + 31) // 32, dtype=i32, device=dev)
+        self.stats = torch.zeros(8, dtype=i32, device=dev)
+        self.status = torch.zeros(2, dtype=i32, device=dev)
+        dt = abi.MOE_DTYPE_BF16 if w_gate.dtype == torch.bfloat16 else abi.MOE_DTYPE_F32
+        capped = capacity_factor > 0
+        wsd = abi.workspace_size(abi.MOE_OP_DISPATCH, T, H, self.I, N, k, self.R, capped, dt)
+        wsf = abi.workspace_size(abi.MOE_OP_FFN, T, H, self.I, N, k, self.R, capped, dt)
+        self.ws_dispatch = torch.empty(max(wsd, 256), dtype=torch.uint8, device=dev)
+        self.ws_ffn = torch.empty(max(wsf, 256), dtype=torch.uint8, device=dev)
+        self.y = torch.empty(T, H, dtype=f32, device=dev)
+
+    def sere_params(self) -> abi.SereParams:
+        return abi.SereParams(self.k_primary, self.rho, self.sim, self.protect, self.union_bitmap, self.stats)
+
+    def route(self, x: torch.Tensor, sere: bool, stream=None):
+        T = x.shape[0]
+        sp = self.sere_params() if sere else None
+        abi.moe_route(x, self.w_router, self.logits[:T], self.ids[:T], self.gates[:T], self.k, self.flags, sp,
+                      self.status, stream)
+
+    def dispatch(self, T: int, token_w: Optional[torch.Tensor] = None, stream=None):
+        abi.moe_dispatch_capacity(self.ids[:T], self.gates[:T], self.N, self.k, self.R, self.counts, self.offsets,
+                                  self.row_token, self.row_gate, self.active, self.ws_dispatch, token_w,
+                                  self.capacity_factor, self.out_ids[:T], self.out_gates[:T], None,
+                                  self.slot_status[:T] if self.capacity_factor > 0 else None,
+                                  self.load_q if self.capacity_factor > 0 else None,
+                                  self.cap_q if self.capacity_factor > 0 else None, self.status, stream)
+
+    def ffn(self, x: torch.Tensor, stream=None):
+        T = x.shape[0]
+        abi.moe_ffn_grouped(x, self.w_gate, self.w_up, self.w_down, self.k, self.offsets, self.row_token,
+                            self.row_gate, self.active, self.y[:T], self.ws_ffn,
+                            abi.MOE_FFN_FUSE_COMBINE | abi.MOE_FFN_ZERO_Y, self.status, stream)
+
+    def forward(self, x: torch.Tensor, sere: bool = False, token_w: Optional[torch.Tensor] = None, stream=None):
+        """y[T][H] fp32 (a view of the layer's output buffer)."""
+        T = x.shape[0]
+        if T > self.max_T:
+            raise abi.MoeError("batch %d exceeds the layer's max_tokens %d" % (T, self.max_T))
+        self.route(x, sere and self.sim is not None, stream)
+        self.dispatch(T, token_w, stream)
+        self.ffn(x, stream)
+        return self.y[:T]
+
+    def device_status(self):
+        code, detail = (int(v) for v in self.status.tolist())
+        return code, detail

@@ -1,0 +1,231 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) MoE routing-layer library.
+ *
+ * One mixture-of-experts layer under batch-level routing control:
+ *
+ *   y(x) = sum_{j in Top-k(G(x))} G(x)_j * E_j(x)
+ *       ("MACS: Modality-Aware Capacity Scaling for Efficient Multimodal MoE
+ *        Inference", sec. 3.1, Eq. (1))
+ *
+ * computed as   moe_route        router GEMM + fp32 softmax + top-R ranking,
+ *                                optionally fused with the SERE batch reroute
+ *               moe_reroute_sere the SERE reroute on its own
+ *               moe_dispatch_capacity
+ *                                expert-sorted permutation, optionally under a
+ *                                weighted capacity with overflow reroute / drop
+ *               moe_ffn_grouped  grouped SwiGLU expert FFN, combine fused in
+ *               moe_combine      weighted combine of per-row expert outputs
+ *
+ * Conventions for every entry point
+ *  - Pointers named "host" are host memory; every other pointer is device
+ *    memory (cudaMalloc / PyTorch CUDA tensors).  The caller owns all memory;
+ *    the library allocates nothing, frees nothing and never synchronises.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on that stream; launch configurations
+ *    depend only on the scalar arguments, so a sequence of calls can be
+ *    captured into a CUDA graph.
+ *  - Arguments are checked on the host before anything is launched.  A bad
+ *    argument returns a negative moe_status_t and launches nothing.
+ *  - Errors that depend on the data (non-finite logits, an out-of-range id,
+ *    an internal wait that timed out) are written asynchronously into the
+ *    optional device-side status word `st` (first error wins; clear it to
+ *    zero before use).  Outputs of a call that set an error are unspecified.
+ *  - Matrices are row-major and densely packed unless a leading dimension
+ *    (`ld`) is given.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int moe_status_t;
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)   /* a pointer, size, alignment or option is invalid */
+#define MOE_ERR_UNSUPPORTED (-2)   /* valid but outside what the kernels support (see limits) */
+#define MOE_ERR_CUDA (-3)          /* a CUDA launch or driver call failed */
+#define MOE_ERR_WORKSPACE (-4)     /* workspace missing or smaller than moe_workspace_size() */
+
+/* Device-side status word, written by kernels. */
+typedef struct moe_dev_status {
+    int32_t code;    /* MOE_DEV_* */
+    int32_t detail;  /* code-specific: token index, expert id, or wait site */
+} moe_dev_status;
+#define MOE_DEV_OK 0
+#define MOE_DEV_NONFINITE 1        /* a router logit was NaN or infinite (detail = token) */
+#define MOE_DEV_TIMEOUT 2          /* a bounded on-chip wait gave up (detail = wait site) */
+#define MOE_DEV_BAD_INDEX 3        /* an expert id or row index was out of range (detail = value) */
+
+#define MOE_DTYPE_F32 0
+#define MOE_DTYPE_BF16 1
+
+/* Limits of this build. */
+#define MOE_MAX_EXPERTS 256        /* N */
+#define MOE_MAX_RANKS 16           /* R (and k <= R) */
+
+/* ---------------------------------------------------------------- */
+/* moe_route                                                          */
+/* ---------------------------------------------------------------- */
+#define MOE_ROUTE_FROM_LOGITS 1u   /* `logits` is an input; x and w_router are not read */
+#define MOE_ROUTE_RENORM_TOPK 2u   /* divide the first k gates by their fp32 sum */
+
+/* SERE parameters ("SERE" expert rerouting, Xiaohongshu multi-image QA
+ * inference article, sec. 4.1-4.2). */
+typedef struct moe_sere_params {
+    int k_primary;            /* K': ranks [0, K') are primaries, 1 <= K' <= k */
+    float rho;                /* a secondary moves only if sim > rho (strict) */
+    const float* sim;         /* [N][N] fp32 expert similarity, row = source expert */
+    const uint8_t* protect;   /* [N] 0/1, nonzero = this source never moves; NULL = none */
+    uint32_t* union_bitmap;   /* out [ceil(N/32)]: bit p set iff expert p is in the
+                                 primary union P; may be NULL */
+    int32_t* stats;           /* out [8]: union before, |P|, union after, moved, merged,
+                                 kept-protected, kept-dissimilar, 0; may be NULL */
+} moe_sere_params;
+
+/*
+ * Router scores, softmax gate and ranking.  "MACS" sec. 3.1, Eq. (1): the
+ * router G(x) scores all N experts; the layer keeps the top-k and weights
+ * each by its gate.
+ *
+ *   x          [T][H]  token activations, x_dtype BF16 or F32 (16-byte aligned)
+ *   w_router   [N][H]  fp32 router weight
+ *   logits     [T][N]  fp32; written (router GEMM, fp32 accumulation), or read
+ *                      with MOE_ROUTE_FROM_LOGITS
+ *   ids        [T][R]  int32 out: expert ids by logit descending, ties to the lower id
+ *   gates      [T][R]  fp32 out: softmax gate of each ranked expert (over all N),
+ *                      computed in a fixed fp32 order so that results are
+ *                      reproducible bit for bit
+ *   k                  the number of experts a token uses (k <= R); used by
+ *                      MOE_ROUTE_RENORM_TOPK and by SERE
+ *   sere               NULL, or SERE parameters: then R must equal k and the
+ *                      reroute runs inside the same kernel as the ranking
+ *                      (one CTA, T <= 4096), rewriting ids/gates in place:
+ *                      moved slots take the target id, merged slots become
+ *                      (-1, 0.0f) with the gate added to the slot that holds
+ *                      the target.
+ * Limits: 1 <= N <= 256, 1 <= k <= R <= min(16, N), T >= 0, H >= 1
+ * (H % 8 == 0 for BF16 x, H % 4 == 0 for F32 x).
+ */
+moe_status_t moe_route(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int R,
+                       int k, uint32_t flags, float* logits, int32_t* ids, float* gates,
+                       const moe_sere_params* sere, moe_dev_status* st, void* stream);
+
+/*
+ * SERE batch reroute on given routing ("SERE" article, sec. 4.1: the union P
+ * of every token's top-K' primary experts is the shared candidate set; every
+ * secondary outside P whose source is not protected (sec. 4.2) moves to its
+ * most similar member of P when that similarity exceeds rho; ties to the
+ * lower id; a token that already holds the target gets the gate added).
+ *
+ *   ids, gates [T][ld] in/out (the first k columns are used); same rewrite
+ *   rules as moe_route with `sere`.  One CTA; T <= 4096.
+ */
+moe_status_t moe_reroute_sere(int32_t* ids, float* gates, int ld, int T, int N, int k,
+                              const moe_sere_params* sere, moe_dev_status* st, void* stream);
+
+/* ---------------------------------------------------------------- */
+/* moe_dispatch_capacity                                              */
+/* ---------------------------------------------------------------- */
+#define MOE_SLOT_KEPT 0
+#define MOE_SLOT_REROUTED 1
+#define MOE_SLOT_DROPPED 2
+
+/*
+ * Expert-sorted permutation, optionally under a weighted capacity.
+ *
+ * Uncapped (capacity_factor <= 0): every slot with id >= 0 among the first k
+ * columns of ids becomes one row.  Capped ("MACS" sec. 3.1 Eq. (3) and
+ * sec. 3.2 Eq. (6)): token weights w are taken in fixed point
+ * w_q = rint(w * 2^24); S = sum w_q; C = floor(((double)S * k) *
+ * capacity_factor / N).  Each expert admits its (token, slot) pairs in
+ * (gate desc, token asc) order while the cumulative w_q stays <= C.  Then, in
+ * rounds i = 0 .. R-k-1, every token with an overflowed slot offers its
+ * lowest-rank overflowed slot (with that slot's gate) to its rank-(k+i)
+ * expert, which admits offers in the same order while load + cumulative
+ * w_q <= C.  Slots left over are dropped (the "MACS" Fig. 1 overflow path:
+ * reroute locally, else drop).
+ *
+ *   ids, gates   [T][ld]  ranked routing (ld >= R when capped, >= k otherwise)
+ *   token_w      [T] fp32 >= 0, or NULL (all 1); capped mode only
+ *   counts       [N]      out: rows per expert
+ *   offsets      [N+1]    out: exclusive prefix of counts
+ *   row_token    [T*k]    out: token of each row, rows ordered by (expert, token)
+ *   row_gate     [T*k]    out: gate of each row
+ *   active       [N+1]    out: active[0] = experts with rows, active[1..] their ids ascending
+ *   out_ids, out_gates [T][k] out (may be NULL): final expert and gate per slot,
+ *                      (-1, 0.0f) for empty or dropped slots
+ *   slot_row     [T][k]   out (may be NULL): row index of each slot, -1 if none
+ *   slot_status  [T][k]   out (may be NULL): MOE_SLOT_*; capped mode only
+ *   load_q       [N]      out (may be NULL): final weighted load in 2^-24 units
+ *   cap_q        [1]      out (may be NULL): C in 2^-24 units
+ *   workspace    device scratch of moe_workspace_size(MOE_OP_DISPATCH, ...) bytes
+ * Limits: N <= 256, k <= R <= min(16, N); capped mode T <= 16384.
+ */
+moe_status_t moe_dispatch_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, int k,
+                                   int R, const float* token_w, float capacity_factor, int32_t* counts,
+                                   int32_t* offsets, int32_t* row_token, float* row_gate, int32_t* active,
+                                   int32_t* out_ids, float* out_gates, int32_t* slot_row,
+                                   uint8_t* slot_status, int64_t* load_q, int64_t* cap_q, void* workspace,
+                                   size_t ws_bytes, moe_dev_status* st, void* stream);
+
+/* ---------------------------------------------------------------- */
+/* moe_ffn_grouped                                                    */
+/* ---------------------------------------------------------------- */
+#define MOE_FFN_FUSE_COMBINE 1u    /* out is y[T][H] fp32: y[t] += gate * E_e(x_t) per row */
+#define MOE_FFN_ZERO_Y 2u          /* with FUSE_COMBINE: zero y first */
+
+/*
+ * Grouped SwiGLU expert FFN ("MACS" sec. 3.1 Eq. (1), E_j(x) =
+ * W_down_j (silu(W_gate_j x) * (W_up_j x))) over the rows of
+ * moe_dispatch_capacity, only for active experts.
+ *
+ *   x       [T][H]     activations, dtype BF16 or F32 (same dtype as the weights)
+ *   w_gate  [N][I][H], w_up [N][I][H], w_down [N][H][I]  expert weights
+ *   offsets [N+1], row_token [T*k], row_gate [T*k], active [N+1]  from dispatch
+ *   out     FUSE_COMBINE: y [T][H] fp32 (accumulated into); otherwise
+ *           rows_out [T*k][H] fp32, row r = E_e(x_token(r)) without the gate
+ *   workspace  device scratch of moe_workspace_size(MOE_OP_FFN, ...) bytes
+ * BF16 runs on the tensor cores (tcgen05, TMA-fed) with fp32 accumulation;
+ * the SwiGLU activation is rounded to bf16 before the down projection.
+ * F32 runs a CUDA-core kernel in fp32.
+ * Limits BF16: H % 128 == 0, I % 128 == 0, all pointers 16-byte aligned;
+ * rows_out mode needs FUSE_COMBINE off and is accumulated, so zero it first.
+ */
+moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const void* w_up,
+                             const void* w_down, int T, int H, int I, int N, int k, const int32_t* offsets,
+                             const int32_t* row_token, const float* row_gate, const int32_t* active,
+                             uint32_t flags, float* out, void* workspace, size_t ws_bytes,
+                             moe_dev_status* st, void* stream);
+
+/*
+ * Weighted combine ("MACS" Eq. (1)): y[t] = sum_r gate[t][r] * rows_out[slot_row[t][r]]
+ * over the slots r < k with slot_row >= 0, in slot order (deterministic).
+ *   rows_out [M][H] fp32, slot_row [T][k], slot_gate [T][k], y [T][H] fp32 out.
+ */
+moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const float* slot_gate, int T,
+                         int H, int k, float* y, void* stream);
+
+/* ---------------------------------------------------------------- */
+/* Workspace sizes and status strings                                 */
+/* ---------------------------------------------------------------- */
+#define MOE_OP_DISPATCH 1
+#define MOE_OP_FFN 2
+
+/* Bytes of device workspace that `op` needs for these sizes (0 if none).
+ * capped != 0 asks for the capacity-mode size of MOE_OP_DISPATCH; dtype
+ * selects the FFN kernel.  Returns 0 for invalid arguments. */
+size_t moe_workspace_size(int op, int T, int H, int I, int N, int k, int R, int capped, int dtype);
+
+/* Static string for a status code (host or device MOE_DEV_* codes are
+ * told apart by the `device` flag). */
+const char* moe_status_string(int code, int device);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,127 @@
+"""The C-ABI library loads without a GPU, exports every declared entry point,
+and rejects bad arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__ as entry
+from expert_routing_moe_gb300 import _abi as abi
+
+HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(HDR):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HDR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    entry.build()
+    return abi.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_symbols()
+    assert {"moe_route", "moe_reroute_sere", "moe_dispatch_capacity", "moe_ffn_grouped", "moe_combine",
+            "moe_workspace_size", "moe_status_string"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert abi.status_string(0, False) == "ok"
+    assert "invalid" in abi.status_string(-1, False)
+    assert "timed out" in abi.status_string(abi.MOE_DEV_TIMEOUT, True)
+
+
+def test_workspace_sizes(lib):
+    assert abi.workspace_size(abi.MOE_OP_FFN, 32, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16) >= 256 * 2048 * 2
+    assert abi.workspace_size(abi.MOE_OP_FFN, 32, 64, 128, 8, 2, 2, False, abi.MOE_DTYPE_F32) == 0
+    capped = abi.workspace_size(abi.MOE_OP_DISPATCH, 8192, 2048, 768, 128, 8, 10, True, abi.MOE_DTYPE_BF16)
+    assert capped >= 2 * 128 * 8192 * 4
+    assert abi.workspace_size(abi.MOE_OP_DISPATCH, 8, 64, 64, 0, 2, 2, False, 0) == 0   # N = 0 is invalid
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its host-side checks
+
+
+@pytest.mark.parametrize("args", [
+    # T, H, N, R, k
+    (4, 64, 0, 2, 2),      # no experts
+    (4, 64, 300, 2, 2),    # N above the limit
+    (4, 64, 8, 17, 2),     # R above the limit
+    (4, 64, 8, 2, 3),      # k > R
+    (4, 64, 8, 9, 2),      # R > N
+    (-1, 64, 8, 2, 2),     # negative T
+])
+def test_route_rejects_bad_sizes(lib, args):
+    T, H, N, R, k = args
+    rc = lib.moe_route(FAKE, 0, FAKE, T, H, N, R, k, 0, FAKE, FAKE, FAKE, None, None, None)
+    assert rc == -1
+
+
+def test_route_rejects_misaligned_and_unsupported(lib):
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.moe_route(odd, 1, FAKE, 4, 64, 8, 2, 2, 0, FAKE, FAKE, FAKE, None, None, None) == -1
+    assert lib.moe_route(FAKE, 1, FAKE, 4, 60, 8, 2, 2, 0, FAKE, FAKE, FAKE, None, None, None) == -2  # H % 8
+    assert lib.moe_route(FAKE, 0, FAKE, 4, 64, 8, 2, 2, 1 << 7, FAKE, FAKE, FAKE, None, None, None) == -1  # flag
+    assert lib.moe_route(None, 0, None, 4, 64, 8, 2, 2, 0, FAKE, FAKE, FAKE, None, None, None) == -1  # no x
+
+
+def test_sere_rejects_bad_params(lib):
+    sp = abi._SereParams(0, 0.5, FAKE, None, None, None)          # K' = 0
+    assert lib.moe_reroute_sere(FAKE, FAKE, 4, 4, 8, 4, ctypes.byref(sp), None, None) == -1
+    sp = abi._SereParams(5, 0.5, FAKE, None, None, None)          # K' > k
+    assert lib.moe_reroute_sere(FAKE, FAKE, 4, 4, 8, 4, ctypes.byref(sp), None, None) == -1
+    sp = abi._SereParams(1, 0.5, None, None, None, None)          # no similarity matrix
+    assert lib.moe_reroute_sere(FAKE, FAKE, 4, 4, 8, 4, ctypes.byref(sp), None, None) == -1
+    sp = abi._SereParams(1, 0.5, FAKE, None, None, None)
+    assert lib.moe_reroute_sere(FAKE, FAKE, 4, 5000, 8, 4, ctypes.byref(sp), None, None) == -2  # T too large
+    # fused with ranking: R must equal k
+    assert lib.moe_route(FAKE, 0, FAKE, 4, 64, 8, 4, 2, 0, FAKE, FAKE, FAKE, ctypes.byref(sp), None, None) == -1
+
+
+def test_dispatch_rejects(lib):
+    d = lib.moe_dispatch_capacity
+    # capped mode needs ld >= R and R >= k
+    assert d(FAKE, FAKE, 2, 4, 8, 2, 4, None, 1.25, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
+             None, FAKE, 1 << 30, None, None) == -1
+    # capped mode with T above the limit
+    assert d(FAKE, FAKE, 4, 20000, 8, 2, 4, None, 1.25, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
+             None, FAKE, 1 << 30, None, None) == -2
+    # workspace too small
+    assert d(FAKE, FAKE, 4, 64, 8, 2, 4, None, 1.25, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
+             None, FAKE, 16, None, None) == -4
+    # NaN capacity factor
+    assert d(FAKE, FAKE, 4, 64, 8, 2, 4, None, float("nan"), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None,
+             None, None, FAKE, 1 << 30, None, None) == -1
+
+
+def test_ffn_rejects(lib):
+    f = lib.moe_ffn_grouped
+    # bf16 needs H % 128 == 0 and I % 128 == 0
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 96, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, 1 << 30, None,
+             None) == -2
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 128, 96, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, 1 << 30, None,
+             None) == -2
+    # missing workspace
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 128, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, None, 0, None,
+             None) == -4
+    # unknown dtype and unknown flag
+    assert f(FAKE, 7, FAKE, FAKE, FAKE, 4, 128, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, 1 << 30, None,
+             None) == -1
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 128, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1 << 5, FAKE, FAKE, 1 << 30,
+             None, None) == -1
+
+
+def test_combine_rejects(lib):
+    assert lib.moe_combine(FAKE, FAKE, FAKE, 4, 64, 0, FAKE, None) == -1
+    assert lib.moe_combine(FAKE, None, FAKE, 4, 64, 2, FAKE, None) == -1
