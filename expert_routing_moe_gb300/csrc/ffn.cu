@@ -435,10 +435,16 @@ static bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
 }
 
 static int sm_count() {
-    int dev = 0, n = 0;
+    static int cached[64] = {};
+    int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 1;
+    if (dev < 0 || dev >= 64) return 1;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
 }
 
 template <int NT>
@@ -467,8 +473,16 @@ static cudaError_t run_tc(const void* x, const void* wg, const void* wu, const v
         !make_tmap(&tm_wd, wd, I, static_cast<uint64_t>(N) * H, 64, 128) ||
         !make_tmap(&tm_x, xperm, H, xrows, 64, NT))
         return cudaErrorInvalidValue;
-    cudaError_t ae = cudaFuncSetAttribute(ffn_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (ae != cudaSuccess) return ae;
+    // the attribute is set once per device, on the first (uncaptured) call
+    static bool attr_set[64] = {};
+    int devi = 0;
+    cudaGetDevice(&devi);
+    if (devi < 0 || devi >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[devi]) {
+        cudaError_t ae = cudaFuncSetAttribute(ffn_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (ae != cudaSuccess) return ae;
+        attr_set[devi] = true;
+    }
     const long long max_items = (N < Mmax ? N : Mmax) + (Mmax + NT - 1) / NT;
     long long max_units = max_items * (I / C::BI);
     int grid = sm_count();
