@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["abi.cu", "router.cu", "dispatch.cu", "ffn.cu"]
+SOURCES = ["abi.cu", "router.cu", "dispatch.cu", "dispatch_static.cu", "ffn.cu"]
 HEADERS = ["common.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

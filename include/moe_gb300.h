@@ -172,6 +172,42 @@ moe_status_t moe_dispatch_capacity(const int32_t* ids, const float* gates, int l
                                    uint8_t* slot_status, int64_t* load_q, int64_t* cap_q, void* workspace,
                                    size_t ws_bytes, moe_dev_status* st, void* stream);
 
+/*
+ * moe_dispatch_capacity_static -- the same dispatch as moe_dispatch_capacity,
+ * for callers that cannot allocate device memory.  The paper has no
+ * counterpart; this is an interface of this library only.
+ *
+ * Who needs it: code that is not allowed to call cudaMalloc or to hold a
+ * workspace of its own, for example a plugin inside a serving engine that
+ * hands out all device memory from its own pool, or code running while a
+ * stream is captured into a CUDA graph under a capture mode that forbids
+ * allocation calls.  Such a caller still passes its inputs and outputs; only
+ * the scratch memory moves into the library.
+ *
+ * Scratch: one file-scope device array of MOE_STATIC_DISPATCH_SCRATCH_BYTES
+ * (4.5 MiB), present on every GPU that loads the library until the process
+ * exits.  It is enough for every size with T <= MOE_STATIC_DISPATCH_MAX_T
+ * (2048 tokens) and the limits of moe_dispatch_capacity; larger T returns
+ * MOE_ERR_UNSUPPORTED and launches nothing.  No call allocates or frees.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array: calls whose work
+ * overlaps on the GPU (two streams, or two host threads) race and give wrong
+ * results, so serialise them.  Each call clears the parts of the array that
+ * must start at zero, so leftovers of the previous call do no harm.
+ *
+ * Arguments, outputs and errors are those of moe_dispatch_capacity without
+ * `workspace` and `ws_bytes`.
+ */
+#define MOE_STATIC_DISPATCH_MAX_T 2048
+#define MOE_STATIC_DISPATCH_SCRATCH_BYTES (4608u * 1024u)
+moe_status_t moe_dispatch_capacity_static(const int32_t* ids, const float* gates, int ld, int T, int N, int k,
+                                          int R, const float* token_w, float capacity_factor, int32_t* counts,
+                                          int32_t* offsets, int32_t* row_token, float* row_gate,
+                                          int32_t* active, int32_t* out_ids, float* out_gates,
+                                          int32_t* slot_row, uint8_t* slot_status, int64_t* load_q,
+                                          int64_t* cap_q, moe_dev_status* st, void* stream);
+
 /* ---------------------------------------------------------------- */
 /* moe_ffn_grouped                                                    */
 /* ---------------------------------------------------------------- */
