@@ -289,7 +289,7 @@ def run_ours(args):
     us_top8 = active_counts(False)
     g_sere = capture(True)
     g_top8 = capture(False)
-    launches_per_step = 5  # router, rank+SERE, permute, FFN prep (gather), FFN tensor-core kernel
+    launches_per_step = 4  # router, rank+SERE, permute, FFN tensor-core kernel (plus a memset node for y)
 
     clk = ClockSampler(local if ws > 1 else 0)
     clk.start()
@@ -352,7 +352,7 @@ def run_ours(args):
         "config": workload_config({"parallelism": "replicas" if ws > 1 else "single GPU",
                                    "cuda_graphs": "per step: routing+dispatch graph, FFN graph"}),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "moe_ffn_grouped (gather + tcgen05 FFN)",
+                     "traffic": None, "kernel": "moe_ffn_grouped (y clear + tcgen05 FFN kernel)",
                      "peak_source": peak_src,
                      "bytes_per_launch_mean": float(np.mean(ffn_bytes)),
                      "ms_per_launch_mean": float(np.mean(ffn_ms))},

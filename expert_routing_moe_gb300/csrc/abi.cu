@@ -125,8 +125,8 @@ moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const
         static_cast<long long>(T) * k > 0x7fffffffLL)
         return MOE_ERR_UNSUPPORTED;
     const size_t need = moe::ffn_workspace(T, H, I, N, k, dtype);
-    if (workspace == nullptr || ws_bytes < need) return MOE_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_ffn_bf16(x, w_gate, w_up, w_down, T, H, I, N, k, offsets, row_token, row_gate,
                                           active, flags, out, workspace, st, s));
 }

@@ -92,35 +92,37 @@ size_t dispatch_workspace(int T, int N, int k, int R, bool capped) {
 // ---------------------------------------------------------------------------
 // Marks, for the 1024-token block `b`, bit (t mod 1024) of expert e's bitmap
 // for every slot of token t holding e.
-__device__ void presence_bits(const int32_t* __restrict__ ids, int ld, int T, int N, int k, int b, uint32_t* bits,
-                              moe_dev_status* st) {
-    for (int i = threadIdx.x; i < N * kWordsPerBlk; i += blockDim.x) bits[i] = 0u;
+// nw = 32-bit words per expert (tokens of the block / 32, rounded up).
+__device__ void presence_bits(const int32_t* __restrict__ ids, int ld, int T, int N, int k, int b, int nw,
+                              uint32_t* bits, moe_dev_status* st) {
+    for (int i = threadIdx.x; i < N * nw; i += blockDim.x) bits[i] = 0u;
     __syncthreads();
     const int t = b * kBlk + threadIdx.x;
-    if (t < T) {
+    if (t < T && threadIdx.x < nw * 32) {
         for (int r = 0; r < k; ++r) {
             const int e = ids[static_cast<size_t>(t) * ld + r];
             if (e >= N) report(st, MOE_DEV_BAD_INDEX, e);
-            if (e >= 0 && e < N) atomicOr(&bits[e * kWordsPerBlk + (threadIdx.x >> 5)], 1u << (threadIdx.x & 31));
+            if (e >= 0 && e < N) atomicOr(&bits[e * nw + (threadIdx.x >> 5)], 1u << (threadIdx.x & 31));
         }
     }
     __syncthreads();
 }
 
-__device__ int block_count(const uint32_t* bits, int e) {
+__device__ int block_count(const uint32_t* bits, int e, int nw) {
     int c = 0;
-    for (int w = 0; w < kWordsPerBlk; ++w) c += __popc(bits[e * kWordsPerBlk + w]);
+    for (int w = 0; w < nw; ++w) c += __popc(bits[e * nw + w]);
     return c;
 }
 
 // Writes the rows of block b given the absolute start row of each expert in
 // this block (start[e]).
 __device__ void write_rows(const int32_t* __restrict__ ids, const float* __restrict__ gates, int ld, int T, int N,
-                           int k, int b, const uint32_t* bits, const int32_t* start, int32_t* __restrict__ row_token,
+                           int k, int b, int nw, const uint32_t* bits, const int32_t* start,
+                           int32_t* __restrict__ row_token,
                            float* __restrict__ row_gate, int32_t* __restrict__ out_ids,
                            float* __restrict__ out_gates, int32_t* __restrict__ slot_row) {
     const int t = b * kBlk + threadIdx.x;
-    if (t >= T) return;
+    if (t >= T || threadIdx.x >= nw * 32) return;
     const int w0 = threadIdx.x >> 5;
     const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
     for (int r = 0; r < k; ++r) {
@@ -131,8 +133,8 @@ __device__ void write_rows(const int32_t* __restrict__ ids, const float* __restr
         int row = -1;
         if (e >= 0 && e < N) {
             int c = 0;
-            for (int w = 0; w < w0; ++w) c += __popc(bits[e * kWordsPerBlk + w]);
-            c += __popc(bits[e * kWordsPerBlk + w0] & below);
+            for (int w = 0; w < w0; ++w) c += __popc(bits[e * nw + w]);
+            c += __popc(bits[e * nw + w0] & below);
             row = start[e] + c;
             row_token[row] = t;
             row_gate[row] = g;
@@ -188,31 +190,38 @@ __global__ void __launch_bounds__(kBlk) permute_single_kernel(const int32_t* __r
                                                               int32_t* row_token, float* row_gate, int32_t* active,
                                                               int32_t* out_ids, float* out_gates,
                                                               int32_t* slot_row, moe_dev_status* st) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ uint32_t bits[MOE_MAX_EXPERTS * kWordsPerBlk];
     __shared__ int cnt[MOE_MAX_EXPERTS];
     __shared__ int start[MOE_MAX_EXPERTS];
-    presence_bits(ids, ld, T, N, k, 0, bits, st);
-    for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = block_count(bits, e);
+    const int nw = (T + 31) / 32;
+    presence_bits(ids, ld, T, N, k, 0, nw, bits, st);
+    for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = block_count(bits, e, nw);
     __syncthreads();
     scan_experts(cnt, N, counts, offsets, active, start);
     __syncthreads();
-    write_rows(ids, gates, ld, T, N, k, 0, bits, start, row_token, row_gate, out_ids, out_gates, slot_row);
+    write_rows(ids, gates, ld, T, N, k, 0, nw, bits, start, row_token, row_gate, out_ids, out_gates, slot_row);
 }
 
 // Multi-block permutation, pass 1: per-block expert counts.
 __global__ void __launch_bounds__(kBlk) permute_count_kernel(const int32_t* __restrict__ ids, int ld, int T, int N,
                                                              int k, int32_t* __restrict__ blk_cnt,
                                                              moe_dev_status* st) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ uint32_t bits[MOE_MAX_EXPERTS * kWordsPerBlk];
-    presence_bits(ids, ld, T, N, k, blockIdx.x, bits, st);
+    presence_bits(ids, ld, T, N, k, blockIdx.x, kWordsPerBlk, bits, st);
     for (int e = threadIdx.x; e < N; e += blockDim.x)
-        blk_cnt[static_cast<size_t>(blockIdx.x) * N + e] = block_count(bits, e);
+        blk_cnt[static_cast<size_t>(blockIdx.x) * N + e] = block_count(bits, e, kWordsPerBlk);
 }
 
 // Pass 2 (one CTA): totals, offsets, active list; blk_cnt becomes the
 // absolute start row of each (block, expert).
 __global__ void __launch_bounds__(256) permute_scan_kernel(int nblk, int N, int32_t* __restrict__ blk_cnt,
                                                            int32_t* counts, int32_t* offsets, int32_t* active) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int tot[MOE_MAX_EXPERTS];
     __shared__ int start[MOE_MAX_EXPERTS];
     for (int e = threadIdx.x; e < N; e += blockDim.x) {
@@ -238,11 +247,14 @@ __global__ void __launch_bounds__(kBlk) permute_rows_kernel(const int32_t* __res
                                                             int32_t* row_token, float* row_gate, int32_t* out_ids,
                                                             float* out_gates, int32_t* slot_row,
                                                             moe_dev_status* st) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ uint32_t bits[MOE_MAX_EXPERTS * kWordsPerBlk];
     __shared__ int start[MOE_MAX_EXPERTS];
     for (int e = threadIdx.x; e < N; e += blockDim.x) start[e] = blk_start[static_cast<size_t>(blockIdx.x) * N + e];
-    presence_bits(ids, ld, T, N, k, blockIdx.x, bits, nullptr);
-    write_rows(ids, gates, ld, T, N, k, blockIdx.x, bits, start, row_token, row_gate, out_ids, out_gates, slot_row);
+    presence_bits(ids, ld, T, N, k, blockIdx.x, kWordsPerBlk, bits, nullptr);
+    write_rows(ids, gates, ld, T, N, k, blockIdx.x, kWordsPerBlk, bits, start, row_token, row_gate, out_ids,
+               out_gates, slot_row);
     (void)st;
 }
 
@@ -252,15 +264,16 @@ static cudaError_t launch_permute(const int32_t* ids, const float* gates, int ld
                                   int32_t* blk_start, moe_dev_status* st, cudaStream_t s) {
     const int nblk = (T + kBlk - 1) / kBlk;
     if (nblk <= 1) {
-        permute_single_kernel<<<1, kBlk, 0, s>>>(ids, gates, ld, T, N, k, counts, offsets, row_token, row_gate,
-                                                 active, out_ids, out_gates, slot_row, st);
-        return cudaGetLastError();
+        const int threads = T <= 128 ? 128 : (T + 31) / 32 * 32;
+        return launch_pdl(permute_single_kernel, dim3(1), dim3(threads), 0, s, ids, gates, ld, T, N, k, counts,
+                          offsets, row_token, row_gate, active, out_ids, out_gates, slot_row, st);
     }
-    permute_count_kernel<<<nblk, kBlk, 0, s>>>(ids, ld, T, N, k, blk_start, st);
-    permute_scan_kernel<<<1, 256, 0, s>>>(nblk, N, blk_start, counts, offsets, active);
-    permute_rows_kernel<<<nblk, kBlk, 0, s>>>(ids, gates, ld, T, N, k, blk_start, row_token, row_gate, out_ids,
-                                             out_gates, slot_row, st);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(permute_count_kernel, dim3(nblk), dim3(kBlk), 0, s, ids, ld, T, N, k, blk_start, st);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(256), 0, s, nblk, N, blk_start, counts, offsets, active);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(permute_rows_kernel, dim3(nblk), dim3(kBlk), 0, s, ids, gates, ld, T, N, k,
+                      static_cast<const int32_t*>(blk_start), row_token, row_gate, out_ids, out_gates, slot_row, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -280,6 +293,8 @@ __device__ __forceinline__ long long capacity_value(unsigned long long S, int k,
 // each slot appended to its expert's bucket (order fixed later by the sort).
 __global__ void cap_bucket_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gates, int ld, int T,
                                   int N, int k, const float* __restrict__ token_w, DispatchWs w, moe_dev_status* st) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     float wt = token_w ? token_w[t] : 1.0f;
@@ -316,6 +331,8 @@ __global__ void cap_bucket_kernel(const int32_t* __restrict__ ids, const float* 
 __global__ void __launch_bounds__(1024) cap_admit_kernel(const float* __restrict__ gates, int ld, int T, int N,
                                                          int k, float gamma, const float* __restrict__ token_w,
                                                          int round, DispatchWs w) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ unsigned long long keys[];
     __shared__ long long part[1024];
     __shared__ unsigned long long admitted_max;
@@ -400,6 +417,8 @@ __global__ void __launch_bounds__(1024) cap_admit_kernel(const float* __restrict
 // rank-(k+i) expert.
 __global__ void cap_offer_kernel(const int32_t* __restrict__ ids, int ld, int T, int N, int k, int round,
                                  DispatchWs w) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     for (int r = 0; r < k; ++r) {
@@ -417,6 +436,8 @@ __global__ void cap_offer_kernel(const int32_t* __restrict__ ids, int ld, int T,
 // Pending slots are dropped; results are copied out.
 __global__ void cap_finalize_kernel(int T, int N, int k, DispatchWs w, uint8_t* slot_status, int64_t* load_q,
                                     int64_t* cap_q, float gamma) {
+    pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < T * k) {
         if (w.status[i] == kPending) {
@@ -454,22 +475,31 @@ cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int 
     if (err != cudaSuccess) return err;
     const int tb = 256;
     if (T > 0) {
-        cap_bucket_kernel<<<(T + tb - 1) / tb, tb, 0, s>>>(ids, gates, ld, T, N, k, token_w, w, st);
+        err = launch_pdl(cap_bucket_kernel, dim3((T + tb - 1) / tb), dim3(tb), 0, s, ids, gates, ld, T, N, k, token_w,
+                         w, st);
+        if (err != cudaSuccess) return err;
         size_t P2 = 1;
         while (P2 < static_cast<size_t>(T)) P2 <<= 1;
         const size_t smem = P2 * sizeof(unsigned long long);
         err = cudaFuncSetAttribute(cap_admit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem));
         if (err != cudaSuccess) return err;
-        cap_admit_kernel<<<N, 1024, smem, s>>>(gates, ld, T, N, k, capacity_factor, token_w, -1, w);
+        err = launch_pdl(cap_admit_kernel, dim3(N), dim3(1024), smem, s, gates, ld, T, N, k, capacity_factor,
+                         token_w, -1, w);
+        if (err != cudaSuccess) return err;
         for (int i = 0; i + k < R; ++i) {
             cudaMemsetAsync(w.cnt2, 0, sizeof(int32_t) * N, s);
-            cap_offer_kernel<<<(T + tb - 1) / tb, tb, 0, s>>>(ids, ld, T, N, k, i, w);
-            cap_admit_kernel<<<N, 1024, smem, s>>>(gates, ld, T, N, k, capacity_factor, token_w, i, w);
+            err = launch_pdl(cap_offer_kernel, dim3((T + tb - 1) / tb), dim3(tb), 0, s, ids, ld, T, N, k, i, w);
+            if (err != cudaSuccess) return err;
+            err = launch_pdl(cap_admit_kernel, dim3(N), dim3(1024), smem, s, gates, ld, T, N, k, capacity_factor,
+                             token_w, i, w);
+            if (err != cudaSuccess) return err;
         }
     }
     const int nfin = (T * k > N ? T * k : N);
-    cap_finalize_kernel<<<(nfin + tb - 1) / tb, tb, 0, s>>>(T, N, k, w, slot_status, load_q, cap_q, capacity_factor);
+    err = launch_pdl(cap_finalize_kernel, dim3((nfin + tb - 1) / tb), dim3(tb), 0, s, T, N, k, w, slot_status,
+                     load_q, cap_q, capacity_factor);
+    if (err != cudaSuccess) return err;
     if (out_ids) cudaMemcpyAsync(out_ids, w.wids, sizeof(int32_t) * T * k, cudaMemcpyDeviceToDevice, s);
     if (out_gates) cudaMemcpyAsync(out_gates, w.wgates, sizeof(float) * T * k, cudaMemcpyDeviceToDevice, s);
     if (T == 0) {

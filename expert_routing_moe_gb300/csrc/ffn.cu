@@ -27,7 +27,6 @@
 
 namespace moe {
 
-static inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ---------------------------------------------------------------------------
 // Tile configuration of the tensor-core kernel.
@@ -39,97 +38,55 @@ struct TcCfg {
     static constexpr int BH = 128;                 // H tile of GEMM2 (GEMM2 M)
     static constexpr int W_BOX = 128 * 64 * 2;     // one 128x64 bf16 box = 16 KiB
     static constexpr int W_BYTES = 2 * W_BOX;      // two boxes per stage
-    static constexpr int X_BYTES = NT * 64 * 2;    // token tile per stage
+    static constexpr int X_BYTES = NT * 64 * 2;    // token tile per stage (NT gathered rows)
     static constexpr int STAGE = W_BYTES + X_BYTES;
-    static constexpr int NSTAGE = (NT >= 64) ? 5 : 6;
+    static constexpr int NSTAGE = (NT <= 16) ? 6 : 5;
     static constexpr int ACT_BYTES = NT * BI * 2;  // two 64-column swizzle atoms of NT rows
-    static constexpr int NBAR = 2 * NSTAGE + 9;
-    static constexpr int SMEM = 1024 + NSTAGE * STAGE + ACT_BYTES + NBAR * 8 + 64;
+    static constexpr int NACC2 = (NT <= 32) ? 4 : 2;
+    static constexpr int EPI_WARPS = 8;            // two warps per TMEM lane quadrant
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+    static constexpr int CW = NT / 2;              // token columns per epilogue warp
+    static constexpr int NBAR = 2 * NSTAGE + 5 + 2 * NACC2;
+    static constexpr int TABLE_INTS = 4 * MOE_MAX_EXPERTS + 4;
+    static constexpr int SMEM =
+        1024 + NSTAGE * STAGE + ACT_BYTES + NBAR * 8 + 16 + 64 * 4 + TABLE_INTS * 4 + EPI_WARPS * 32 * 8;
     static constexpr uint32_t TMEM_COLS = 256;
     static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
-    static_assert(4 * NT <= (int)TMEM_COLS, "TMEM columns");
+    static_assert((2 + NACC2) * NT <= (int)TMEM_COLS, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(CW == 8 || CW == 16 || CW == 32, "epilogue column split");
 };
-
-struct TcItems {
-    int4* items;    // (expert, first row, rows, 0)
-    int* n_items;
-};
-
-static size_t tc_x_rows(int T, int k) { return static_cast<size_t>(T) * k > 64 ? static_cast<size_t>(T) * k : 64; }
 
 size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype) {
-    (void)I;
-    if (dtype != MOE_DTYPE_BF16) return 0;
-    size_t off = 0;
-    off = align_up(off + tc_x_rows(T, k) * H * 2, 256);                                      // X_perm
-    off = align_up(off + sizeof(int4) * (static_cast<size_t>(N) + tc_x_rows(T, k) / 16 + 2), 256);  // items
-    off = align_up(off + sizeof(int) * 4, 256);                                              // n_items
-    return off;
+    (void)T; (void)H; (void)I; (void)N; (void)k; (void)dtype;
+    return 0;  // the tensor-core path reads token rows straight from x
 }
 
-static void carve_ffn(void* ws, int T, int H, int N, int k, void** xperm, TcItems* it) {
-    char* b = static_cast<char*>(ws);
-    size_t off = 0;
-    *xperm = b + off;
-    off = align_up(off + tc_x_rows(T, k) * H * 2, 256);
-    it->items = reinterpret_cast<int4*>(b + off);
-    off = align_up(off + sizeof(int4) * (static_cast<size_t>(N) + tc_x_rows(T, k) / 16 + 2), 256);
-    it->n_items = reinterpret_cast<int*>(b + off);
-}
+// Work units: for every active expert a, ceil(rows/NT) token chunks, each
+// split into I/128 slices.  The table (built once per CTA in shared memory)
+// holds, per active expert, its id, first row, row count and first chunk.
+struct UnitTable {
+    int* e;      // [na]
+    int* row;    // [na]
+    int* cnt;    // [na]
+    int* pre;    // [na + 1]: exclusive prefix of chunk counts
+    int na;
+};
 
-// ---------------------------------------------------------------------------
-// Preparation: gather x rows into expert-sorted order (16-byte vector copies),
-// build the work-item list (one item per <= NT-row chunk of each active
-// expert) and optionally clear y.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) ffn_prep_kernel(const uint4* __restrict__ x, int H, int Mmax,
-                                                       const int32_t* __restrict__ offsets,
-                                                       const int32_t* __restrict__ row_token,
-                                                       const int32_t* __restrict__ active, int N, int NT,
-                                                       uint4* __restrict__ xperm, TcItems it, float* y, int T,
-                                                       int zero_y) {
-    const int M = offsets[N];
-    const int vec_per_row = H / 8;  // 8 bf16 per 16 bytes
-    const long long total = static_cast<long long>(min(M, Mmax)) * vec_per_row;
-    for (long long v = blockIdx.x * 256ll + threadIdx.x; v < total; v += 256ll * gridDim.x) {
-        const int row = static_cast<int>(v / vec_per_row), c = static_cast<int>(v % vec_per_row);
-        const int tok = row_token[row];
-        xperm[v] = x[static_cast<long long>(tok) * vec_per_row + c];
+__device__ __forceinline__ void unit_info(const UnitTable& tb, int u, int S, int NT, int& e, int& s, int& row0,
+                                          int& nrows) {
+    const int item = u / S;
+    s = u - item * S;
+    int lo = 0, hi = tb.na - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tb.pre[mid] <= item) lo = mid; else hi = mid - 1;
     }
-    if (zero_y) {
-        const long long ny = static_cast<long long>(T) * H / 4;
-        float4* y4 = reinterpret_cast<float4*>(y);
-        for (long long v = blockIdx.x * 256ll + threadIdx.x; v < ny; v += 256ll * gridDim.x)
-            y4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (blockIdx.x == 0 && threadIdx.x < 32) {
-        // one warp: prefix over active experts of their chunk counts
-        const int lane = threadIdx.x;
-        const int na = active[0];
-        int run = 0;
-        for (int base = 0; base < na; base += 32) {
-            const int a = base + lane;
-            int e = -1, r0 = 0, cnt = 0, ch = 0;
-            if (a < na) {
-                e = active[1 + a];
-                r0 = offsets[e];
-                cnt = offsets[e + 1] - r0;
-                ch = (cnt + NT - 1) / NT;
-            }
-            int inc = ch;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(kFull, inc, off);
-                if (lane >= off) inc += o;
-            }
-            int pos = run + inc - ch;
-            for (int c = 0; c < ch; ++c)
-                it.items[pos + c] = make_int4(e, r0 + c * NT, min(NT, cnt - c * NT), 0);
-            run += __shfl_sync(kFull, inc, 31);
-        }
-        if (lane == 0) *it.n_items = run;
-    }
+    const int c = item - tb.pre[lo];
+    e = tb.e[lo];
+    row0 = tb.row[lo] + c * NT;
+    nrows = min(NT, tb.cnt[lo] - c * NT);
 }
 
 // ---------------------------------------------------------------------------
@@ -145,30 +102,48 @@ __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[CW]) {
+    if constexpr (CW == 8) {
+        tmem_ld8(taddr, v);
+    } else {
+#pragma unroll
+        for (int c = 0; c < CW / 16; ++c) {
+            uint32_t w[16];
+            tmem_ld16(taddr + c * 16, w);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[c * 16 + j] = w[j];
+        }
+    }
+}
+
 template <int NT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                   const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
-                  const int4* __restrict__ items, const int* __restrict__ n_items_ptr,
+                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ active,
                   const int32_t* __restrict__ row_token, const float* __restrict__ row_gate,
-                  float* __restrict__ out, int H, int I, int fuse_combine, moe_dev_status* st) {
+                  float* __restrict__ out, int H, int I, int N, int fuse_combine, moe_dev_status* st) {
     using C = TcCfg<NT>;
+    constexpr int CW = C::CW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int S = I / C::BI;
-    const int n_units = (*n_items_ptr) * S;
-    if (static_cast<int>(blockIdx.x) >= n_units) return;
-
     uint8_t* ring = smem;
     uint8_t* act = smem + C::NSTAGE * C::STAGE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(act + C::ACT_BYTES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_units = reinterpret_cast<int*>(tmem_slot + 2);
+    int* ptok = reinterpret_cast<int*>(tmem_slot + 4);           // [64] token rows of the producer's unit
+    int* table = ptok + 64;
+    int* etok_all = table + C::TABLE_INTS;                           // [EPI_WARPS][32] tokens of each epilogue warp
+    float* egt_all = reinterpret_cast<float*>(etok_all + C::EPI_WARPS * 32);  // [EPI_WARPS][32] their gates
+    UnitTable tb{table, table + MOE_MAX_EXPERTS, table + 2 * MOE_MAX_EXPERTS, table + 3 * MOE_MAX_EXPERTS, 0};
 
     const uint32_t ring_a = smem_u32(ring), act_a = smem_u32(act);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
     const int B_FULL = 0, B_EMPTY = C::NSTAGE, B_G1 = 2 * C::NSTAGE, B_ACTRDY = B_G1 + 1, B_TMEMFREE = B_G1 + 2,
-              B_ACTFREE = B_G1 + 3, B_ACC2F = B_G1 + 4, B_ACC2E = B_G1 + 6, B_DRAIN = B_G1 + 8;
+              B_ACTFREE = B_G1 + 3, B_DRAIN = B_G1 + 4, B_ACC2F = B_G1 + 5, B_ACC2E = B_ACC2F + C::NACC2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -177,14 +152,14 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(bar(B_EMPTY + i), 1);
         }
         mbar_init(bar(B_G1), 1);
-        mbar_init(bar(B_ACTRDY), 128);
-        mbar_init(bar(B_TMEMFREE), 128);
+        mbar_init(bar(B_ACTRDY), C::EPI_THREADS);
+        mbar_init(bar(B_TMEMFREE), C::EPI_THREADS);
         mbar_init(bar(B_ACTFREE), 1);
-        mbar_init(bar(B_ACC2F), 1);
-        mbar_init(bar(B_ACC2F + 1), 1);
-        mbar_init(bar(B_ACC2E), 128);
-        mbar_init(bar(B_ACC2E + 1), 128);
         mbar_init(bar(B_DRAIN), 1);
+        for (int b = 0; b < C::NACC2; ++b) {
+            mbar_init(bar(B_ACC2F + b), 1);
+            mbar_init(bar(B_ACC2E + b), C::EPI_THREADS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -194,6 +169,47 @@ __global__ void __launch_bounds__(192, 1)
         tma_prefetch_desc(&tm_wd);
         tma_prefetch_desc(&tm_x);
     }
+    // everything above is private to this CTA; the dispatch outputs and y are read below
+    pdl_wait();
+    pdl_trigger();
+    if (warp == 2) {
+        // work-unit table: prefix over active experts of their chunk counts
+        const int na = min(active[0], N);
+        int run = 0;
+        for (int base = 0; base < na; base += 32) {
+            const int a = base + lane;
+            int e = 0, r0 = 0, cnt = 0, ch = 0;
+            if (a < na) {
+                e = active[1 + a];
+                r0 = offsets[e];
+                cnt = offsets[e + 1] - r0;
+                ch = (cnt + NT - 1) / NT;
+            }
+            int inc = ch;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(kFull, inc, off);
+                if (lane >= off) inc += o;
+            }
+            if (a < na) {
+                tb.e[a] = e;
+                tb.row[a] = r0;
+                tb.cnt[a] = cnt;
+                tb.pre[a] = run + inc - ch;
+            }
+            run += __shfl_sync(kFull, inc, 31);
+        }
+        if (lane == 0) {
+            tb.pre[na] = run;
+            s_units[0] = na;
+            s_units[1] = run * (I / C::BI);
+        }
+    }
+    __syncthreads();
+    tb.na = s_units[0];
+    const int n_units = s_units[1];
+    const int S = I / C::BI;
+    if (static_cast<int>(blockIdx.x) >= n_units) return;
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
@@ -205,15 +221,18 @@ __global__ void __launch_bounds__(192, 1)
     const int KT = H / C::BK, MT = H / C::BH;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer ----------------
-            const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
-            int stage = 0;
-            uint32_t phase = 0, pend = 0, pend_par = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const int4 it = items[u / S];
-                const int s = u % S, e = it.x, row0 = it.y;
+        // ---------------- TMA producer (lane 0 issues; the warp loads token lists) ----------------
+        const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0, pend = 0, pend_par = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            int e, s, row0, nrows;
+            unit_info(tb, u, S, NT, e, s, row0, nrows);
+            // rows past the chunk repeat its first token; their columns are never used
+            for (int t = lane; t < NT; t += 32) ptok[t] = row_token[row0 + (t < nrows ? t : 0)];
+            __syncwarp();
+            if (lane == 0) {
                 const int wrow = e * I + s * C::BI;
                 for (int kt = 0; kt < KT + MT; ++kt) {
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
@@ -226,7 +245,10 @@ __global__ void __launch_bounds__(192, 1)
                         mbar_arrive_expect_tx(fb, C::STAGE);
                         tma_load_2d(dst, &tm_wg, kt * C::BK, wrow, fb, pol_w);
                         tma_load_2d(dst + C::W_BOX, &tm_wu, kt * C::BK, wrow, fb, pol_w);
-                        tma_load_2d(dst + C::W_BYTES, &tm_x, kt * C::BK, row0, fb, pol_x);
+#pragma unroll
+                        for (int g = 0; g < NT / 4; ++g)
+                            tma_gather4(dst + C::W_BYTES + g * 512, &tm_x, kt * C::BK, ptok[4 * g], ptok[4 * g + 1],
+                                        ptok[4 * g + 2], ptok[4 * g + 3], fb, pol_x);
                     } else {
                         const int m = kt - KT;
                         mbar_arrive_expect_tx(fb, C::W_BYTES);
@@ -241,11 +263,13 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
-            if (!ok) {
-                // let every copy still in flight land before the CTA exits
-                for (int i = 0; i < C::NSTAGE; ++i)
-                    if (pend >> i & 1u) mbar_drain(bar(B_FULL + i), pend_par >> i & 1u);
-            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+        }
+        if (!ok && lane == 0) {
+            // let every copy still in flight land before the CTA exits
+            for (int i = 0; i < C::NSTAGE; ++i)
+                if (pend >> i & 1u) mbar_drain(bar(B_FULL + i), pend_par >> i & 1u);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -289,7 +313,7 @@ __global__ void __launch_bounds__(192, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t b = n2 & 1u, use = n2 >> 1;
+                    const uint32_t b = n2 % C::NACC2, use = n2 / C::NACC2;
                     if (!mbar_wait(bar(B_ACC2E + b), (use & 1u) ^ 1u, abort_flag, st, kSiteMmaAcc2Empty)) {
                         ok = false;
                         break;
@@ -318,81 +342,89 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue: warps 2..5 ----------------
-        const int q = warp & 3;               // TMEM lane quadrant of this warp
-        const int row = q * 32 + lane;        // row within the 128-row tile
+        // ---------------- epilogue: warps 2..9, two per TMEM lane quadrant ----------------
+        const int q = warp & 3;                        // TMEM lane quadrant of this warp
+        const int half = (warp - 2) >> 2;              // which half of the token columns
+        const int row = q * 32 + lane;                 // row within the 128-row tile
+        const int c_lo = half * CW;                    // first token column of this warp
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const int c = row >> 6, ci = row & 63;
         int j = 0;
         uint32_t n2 = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
-            const int4 it = items[u / S];
-            const int s = u % S, row0 = it.y, nrows = it.z;
+            int e, s, row0, nrows;
+            unit_info(tb, u, S, NT, e, s, row0, nrows);
             // every lane polls; the warp proceeds only if all lanes saw the phase complete
             bool okw = mbar_wait(bar(B_G1), j & 1, abort_flag, st, kSiteEpiG1Done);
             if (!__all_sync(kFull, okw)) break;
             okw = mbar_wait(bar(B_ACTFREE), (j & 1) ^ 1, abort_flag, st, kSiteEpiActFree);
             if (!__all_sync(kFull, okw)) break;
             tc_fence_after();
-            // SwiGLU of this thread's I row for every token of the chunk -> bf16 B operand of GEMM2
-            const int c = row >> 6, ci = row & 63;
-            const uint32_t col_base = act_a + c * (NT * 128);
+            {
+                // SwiGLU of this thread's I row for its token columns -> bf16 B operand of GEMM2,
+                // eight columns at a time
+                const uint32_t col_base = act_a + c * (NT * 128);
 #pragma unroll
-            for (int c0 = 0; c0 < NT / 16; ++c0) {
-                uint32_t g[16], v[16];
-                tmem_ld16(t_gate + lane_off + c0 * 16, g);
-                tmem_ld16(t_up + lane_off + c0 * 16, v);
-                tmem_ld_wait();
+                for (int c8 = 0; c8 < CW / 8; ++c8) {
+                    uint32_t g[8], v[8];
+                    tmem_ld8(t_gate + lane_off + c_lo + c8 * 8, g);
+                    tmem_ld8(t_up + lane_off + c_lo + c8 * 8, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int t = c0 * 16 + jj;
-                    const float a = (t < nrows) ? silu_mul(__uint_as_float(g[jj]), __uint_as_float(v[jj])) : 0.f;
-                    const __nv_bfloat16 hb = __float2bfloat16_rn(a);
-                    const uint32_t addr =
-                        col_base + t * 128 + ((((ci >> 3) ^ (t & 7)) << 4) | ((ci & 7) << 1));
-                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const uint16_t*>(&hb))
-                                 : "memory");
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int t = c_lo + c8 * 8 + jj;
+                        const float a =
+                            (t < nrows) ? silu_mul(__uint_as_float(g[jj]), __uint_as_float(v[jj])) : 0.f;
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(a);
+                        const uint32_t addr = col_base + t * 128 + ((((ci >> 3) ^ (t & 7)) << 4) | ((ci & 7) << 1));
+                        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
+                                     "h"(*reinterpret_cast<const uint16_t*>(&hb))
+                                     : "memory");
+                    }
                 }
             }
             tc_fence_before();
             mbar_arrive(bar(B_TMEMFREE));
             fence_proxy_async_smem();
             mbar_arrive(bar(B_ACTRDY));
-            // down projection tiles: add gate * E_e(x) into y
+            // token and gate of each of this warp's columns, for the reductions below
+            int* etok = etok_all + (warp - 2) * 32;
+            float* egt = egt_all + (warp - 2) * 32;
+            if (lane < CW) {
+                const int t = c_lo + lane;
+                etok[lane] = (t < nrows) ? row_token[row0 + t] : 0;
+                egt[lane] = (t < nrows) ? row_gate[row0 + t] : 0.f;
+            }
+            __syncwarp();
+            // down-projection tiles: add gate * E_e(x) into y
             bool ok = true;
             for (int m = 0; m < H / C::BH; ++m, ++n2) {
-                const uint32_t b = n2 & 1u, use = n2 >> 1;
+                const uint32_t b = n2 % C::NACC2, use = n2 / C::NACC2;
                 const bool okw2 = mbar_wait(bar(B_ACC2F + b), use & 1u, abort_flag, st, kSiteEpiAcc2Full);
                 if (!__all_sync(kFull, okw2)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                uint32_t v[CW];
+                tmem_ld_cols<CW>(t_acc2 + b * NT + lane_off + c_lo, v);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(bar(B_ACC2E + b));   // the accumulator is free again; reductions follow
                 const int h = m * C::BH + row;
 #pragma unroll
-                for (int c0 = 0; c0 < NT / 16; ++c0) {
-                    uint32_t v[16];
-                    tmem_ld16(t_acc2 + b * NT + lane_off + c0 * 16, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int t = c0 * 16 + jj;
-                        if (t < nrows) {
-                            const float val = __uint_as_float(v[jj]);
-                            if (fuse_combine) {
-                                const int tok = row_token[row0 + t];
-                                const float gt = row_gate[row0 + t];
-                                atomicAdd(out + static_cast<size_t>(tok) * H + h, gt * val);
-                            } else {
-                                atomicAdd(out + static_cast<size_t>(row0 + t) * H + h, val);
-                            }
-                        }
+                for (int jj = 0; jj < CW; ++jj) {
+                    const int t = c_lo + jj;
+                    if (t < nrows) {
+                        if (fuse_combine)
+                            atomicAdd(out + static_cast<size_t>(etok[jj]) * H + h, egt[jj] * __uint_as_float(v[jj]));
+                        else
+                            atomicAdd(out + static_cast<size_t>(row0 + t) * H + h, __uint_as_float(v[jj]));
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(bar(B_ACC2E + b));
             }
+            __syncwarp();
             if (!ok) break;
-            (void)s;
         }
     }
     __syncthreads();
@@ -447,31 +479,29 @@ static int sm_count() {
     return cached[dev];
 }
 
+__global__ void zero_kernel(float* p, long long n);
+
+static cudaError_t launch_zero(float* p, long long n, cudaStream_t s) {
+    int grid = static_cast<int>((n / 4 + 255) / 256);
+    grid = grid < 1 ? 1 : (grid > 1024 ? 1024 : grid);
+    return launch_pdl(zero_kernel, dim3(grid), dim3(256), 0, s, p, n);
+}
+
 template <int NT>
 static cudaError_t run_tc(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I, int N,
                           int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
-                          const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
-                          cudaStream_t s) {
+                          const int32_t* active, uint32_t flags, float* out, moe_dev_status* st, cudaStream_t s) {
     using C = TcCfg<NT>;
-    void* xperm = nullptr;
-    TcItems it{};
-    carve_ffn(ws, T, H, N, k, &xperm, &it);
-    const size_t xrows = tc_x_rows(T, k);
-    const int Mmax = T * k;
     const bool fuse = (flags & MOE_FFN_FUSE_COMBINE) != 0;
-    const int zero_y = (fuse && (flags & MOE_FFN_ZERO_Y)) ? 1 : 0;
-    {
-        const long long work = static_cast<long long>(Mmax) * (H / 8);
-        int grid = static_cast<int>((work + 255) / 256);
-        grid = grid < 1 ? 1 : (grid > 1024 ? 1024 : grid);
-        ffn_prep_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(x), H, Mmax, offsets, row_token, active, N,
-                                             NT, static_cast<uint4*>(xperm), it, out, T, zero_y);
+    if (fuse && (flags & MOE_FFN_ZERO_Y)) {
+        cudaError_t e = launch_zero(out, static_cast<long long>(T) * H, s);
+        if (e != cudaSuccess) return e;
     }
     CUtensorMap tm_wg, tm_wu, tm_wd, tm_x;
     if (!make_tmap(&tm_wg, wg, H, static_cast<uint64_t>(N) * I, 64, 128) ||
         !make_tmap(&tm_wu, wu, H, static_cast<uint64_t>(N) * I, 64, 128) ||
         !make_tmap(&tm_wd, wd, I, static_cast<uint64_t>(N) * H, 64, 128) ||
-        !make_tmap(&tm_x, xperm, H, xrows, 64, NT))
+        !make_tmap(&tm_x, x, H, static_cast<uint64_t>(T), 64, 1))
         return cudaErrorInvalidValue;
     // the attribute is set once per device, on the first (uncaptured) call
     static bool attr_set[64] = {};
@@ -483,22 +513,23 @@ static cudaError_t run_tc(const void* x, const void* wg, const void* wu, const v
         if (ae != cudaSuccess) return ae;
         attr_set[devi] = true;
     }
+    const int Mmax = T * k;
     const long long max_items = (N < Mmax ? N : Mmax) + (Mmax + NT - 1) / NT;
-    long long max_units = max_items * (I / C::BI);
+    const long long max_units = max_items * (I / C::BI);
     int grid = sm_count();
     if (max_units < grid) grid = static_cast<int>(max_units > 0 ? max_units : 1);
-    ffn_tc_kernel<NT><<<grid, 192, C::SMEM, s>>>(tm_wg, tm_wu, tm_wd, tm_x, it.items, it.n_items, row_token,
-                                                 row_gate, out, H, I, fuse ? 1 : 0, st);
-    return cudaGetLastError();
+    return launch_pdl(ffn_tc_kernel<NT>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wd, tm_x, offsets,
+                      active, row_token, row_gate, out, H, I, N, fuse ? 1 : 0, st);
 }
 
 cudaError_t launch_ffn_bf16(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
                             int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                             const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
                             cudaStream_t s) {
-    if (T <= 16) return run_tc<16>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws, st, s);
-    if (T <= 32) return run_tc<32>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws, st, s);
-    return run_tc<64>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws, st, s);
+    (void)ws;
+    if (T <= 16) return run_tc<16>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, st, s);
+    if (T <= 32) return run_tc<32>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, st, s);
+    return run_tc<64>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, st, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -513,6 +544,8 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float* __restrict__ 
     extern __shared__ float sh[];
     float* xs = sh;       // [H]
     float* as = sh + H;   // [I]
+    pdl_wait();
+    pdl_trigger();
     const int row = blockIdx.x;
     if (row >= offsets[N]) return;
     // expert of this row: offsets is ascending; binary search
@@ -547,7 +580,13 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float* __restrict__ 
 }
 
 __global__ void zero_kernel(float* p, long long n) {
-    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n; i += 256ll * gridDim.x) p[i] = 0.f;
+    pdl_wait();
+    pdl_trigger();
+    const long long n4 = n / 4;
+    float4* p4 = reinterpret_cast<float4*>(p);
+    for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n4; i += 256ll * gridDim.x)
+        p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long i = n4 * 4 + blockIdx.x * 256ll + threadIdx.x; i < n; i += 256ll * gridDim.x) p[i] = 0.f;
 }
 
 cudaError_t launch_ffn_f32(const float* x, const float* wg, const float* wu, const float* wd, int T, int H, int I,
@@ -557,10 +596,8 @@ cudaError_t launch_ffn_f32(const float* x, const float* wg, const float* wu, con
     (void)st;
     const bool fuse = (flags & MOE_FFN_FUSE_COMBINE) != 0;
     if (fuse && (flags & MOE_FFN_ZERO_Y)) {
-        const long long n = static_cast<long long>(T) * H;
-        int grid = static_cast<int>((n + 255) / 256);
-        grid = grid < 1 ? 1 : (grid > 1024 ? 1024 : grid);
-        zero_kernel<<<grid, 256, 0, s>>>(out, n);
+        cudaError_t e = launch_zero(out, static_cast<long long>(T) * H, s);
+        if (e != cudaSuccess) return e;
     }
     const int Mmax = T * k;
     if (Mmax == 0) return cudaGetLastError();
@@ -570,8 +607,8 @@ cudaError_t launch_ffn_f32(const float* x, const float* wg, const float* wu, con
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    ffn_f32_kernel<<<Mmax, 256, smem, s>>>(x, wg, wu, wd, H, I, N, offsets, row_token, row_gate, fuse ? 1 : 0, out);
-    return cudaGetLastError();
+    return launch_pdl(ffn_f32_kernel, dim3(Mmax), dim3(256), smem, s, x, wg, wu, wd, H, I, N, offsets, row_token,
+                      row_gate, fuse ? 1 : 0, out);
 }
 
 // ---------------------------------------------------------------------------
@@ -581,6 +618,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ slot_row,
                                                       const float* __restrict__ slot_gate, int T, int H, int k,
                                                       float* __restrict__ y) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.y;
     const int h = blockIdx.x * 256 + threadIdx.x;
     if (t >= T || h >= H) return;
@@ -596,8 +635,7 @@ cudaError_t launch_combine(const float* rows_out, const int32_t* slot_row, const
                            int k, float* y, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     dim3 grid((H + 255) / 256, T);
-    combine_kernel<<<grid, 256, 0, s>>>(rows_out, slot_row, slot_gate, T, H, k, y);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(256), 0, s, rows_out, slot_row, slot_gate, T, H, k, y);
 }
 
 }  // namespace moe

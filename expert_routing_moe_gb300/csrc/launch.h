@@ -10,6 +10,25 @@
 
 namespace moe {
 
+// Launches `kernel` on `s` with programmatic stream serialization, so that it
+// may begin while its predecessor finishes; the kernel itself waits
+// (griddepcontrol.wait) before touching memory the predecessor writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- routing (router.cu) ----
 cudaError_t launch_router(const void* x, int x_dtype, const float* w_router, int T, int H, int N, float* logits,
                           cudaStream_t s);

@@ -6,6 +6,7 @@
 // SERE: Xiaohongshu multi-image QA inference article, sec. 4.1 (primary
 // union as the shared candidate set, most-similar primary above rho) and
 // sec. 4.2 (one fused operator, protection of source experts only).
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -33,34 +34,57 @@ __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
 template <typename XT>
 __global__ void __launch_bounds__(256) router_warp_kernel(const XT* __restrict__ x, const float* __restrict__ w,
                                                           int T, int H, int N, float* __restrict__ logits) {
+    constexpr int U = 4;  // 128-element strips per batch of loads (all issued before any FMA)
+    __shared__ float part[8][4];
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int j = blockIdx.x * 8 + warp;
+    const int j = blockIdx.x * 4 + (warp >> 1);   // two warps per expert, one per half of H
     const int t0 = blockIdx.y * 4;
-    if (j >= N) return;
+    const int hmid = ((H >> 1) + 127) / 128 * 128;
+    const int hbeg = (warp & 1) ? hmid : 0, hend = (warp & 1) ? H : min(hmid, H);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* wr = w + static_cast<size_t>(j) * H;
-    for (int h = lane * 4; h < H; h += 128) {
-        float wv[4];
-        load4(wr + h, wv);
+    if (j < N) {
+        const float* wr = w + static_cast<size_t>(j) * H;
+        for (int hb = hbeg + lane * 4; hb < hend; hb += 128 * U) {
+            float wv[U][4];
+            float xv[U][4][4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int h = hb + 128 * u;
+                if (h < hend) {
+                    load4(wr + h, wv[u]);
+                } else {
+                    wv[u][0] = wv[u][1] = wv[u][2] = wv[u][3] = 0.f;
+                }
+#pragma unroll
+                for (int tt = 0; tt < 4; ++tt) {
+                    if (h < hend && t0 + tt < T) {
+                        load4(x + static_cast<size_t>(t0 + tt) * H + h, xv[u][tt]);
+                    } else {
+                        xv[u][tt][0] = xv[u][tt][1] = xv[u][tt][2] = xv[u][tt][3] = 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int tt = 0; tt < 4; ++tt)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[tt] = fmaf(xv[u][tt][q], wv[u][q], acc[tt]);
+        }
 #pragma unroll
         for (int tt = 0; tt < 4; ++tt) {
-            if (t0 + tt < T) {
-                float xv[4];
-                load4(x + static_cast<size_t>(t0 + tt) * H + h, xv);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) acc[tt] = fmaf(xv[q], wv[q], acc[tt]);
-            }
+            for (int off = 16; off >= 1; off >>= 1) acc[tt] += __shfl_xor_sync(kFull, acc[tt], off);
         }
     }
-#pragma unroll
-    for (int tt = 0; tt < 4; ++tt) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) acc[tt] += __shfl_xor_sync(kFull, acc[tt], off);
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt)
-            if (t0 + tt < T) logits[static_cast<size_t>(t0 + tt) * N + j] = acc[tt];
+    if (lane < 4) part[warp][lane] = (lane == 0) ? acc[0] : (lane == 1) ? acc[1] : (lane == 2) ? acc[2] : acc[3];
+    __syncthreads();
+    if (threadIdx.x < 16) {
+        const int jl = threadIdx.x >> 2, tt = threadIdx.x & 3;
+        const int jj = blockIdx.x * 4 + jl;
+        if (jj < N && t0 + tt < T) logits[static_cast<size_t>(t0 + tt) * N + jj] = part[2 * jl][tt] + part[2 * jl + 1][tt];
     }
 }
 
@@ -74,6 +98,8 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const XT* __restrict_
     constexpr int TM = 64, TN = 64, TK = 32;
     __shared__ float xs[TK][TM + 4];
     __shared__ float ws[TK][TN + 4];
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;
     const int tb = blockIdx.y * TM, jb = blockIdx.x * TN;
@@ -126,53 +152,66 @@ cudaError_t launch_router(const void* x, int x_dtype, const float* w_router, int
                           cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (T <= 256) {
-        dim3 grid((N + 7) / 8, (T + 3) / 4);
+        dim3 grid((N + 3) / 4, (T + 3) / 4);
         if (x_dtype == MOE_DTYPE_BF16)
-            router_warp_kernel<__nv_bfloat16>
-                <<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), w_router, T, H, N, logits);
-        else
-            router_warp_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), w_router, T, H, N, logits);
+            return launch_pdl(router_warp_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
+                              static_cast<const __nv_bfloat16*>(x), w_router, T, H, N, logits);
+        return launch_pdl(router_warp_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(x), w_router, T,
+                          H, N, logits);
     } else {
         dim3 grid((N + 63) / 64, (T + 63) / 64);
         if (x_dtype == MOE_DTYPE_BF16)
-            router_tiled_kernel<__nv_bfloat16>
-                <<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), w_router, T, H, N, logits);
-        else
-            router_tiled_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), w_router, T, H, N, logits);
+            return launch_pdl(router_tiled_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
+                              static_cast<const __nv_bfloat16*>(x), w_router, T, H, N, logits);
+        return launch_pdl(router_tiled_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(x), w_router,
+                          T, H, N, logits);
     }
     return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// Ranking of one token by one warp.  Lane l holds experts j = l + 32 i.
+// Ranking of one token by one warp.  Lane l holds experts j = l + 32 i for
+// i < PL (PL = ceil(N/32), a compile-time bound).
 // Gate: m = max; e_j = exp_gate(l_j - m); Z = per-lane sums in increasing j,
 // then xor butterfly 16, 8, 4, 2, 1; g_j = e_j / Z (IEEE division).
-// Ranking: R rounds of warp arg-best under (logit desc, id asc).
-// On return lane r < R holds (id, gate) of rank r.
+// Ranking: R rounds of a warp arg-best under (logit desc, id asc), each one
+// unsigned max of order-preserving keys (redux.sync) and a min over the ids
+// holding that key.  On return lane r < R holds (id, gate) of rank r.
 // ---------------------------------------------------------------------------
 constexpr int kMaxPerLane = MOE_MAX_EXPERTS / 32;
+constexpr int kSereStageN = 128;  // sim staged in shared memory up to N = 128 (64 KiB + N bytes)
 
+// Unsigned key with the order of the float (all zeros rank as +0; NaN excluded).
+__device__ __forceinline__ uint32_t order_key(float v) {
+    uint32_t u = __float_as_uint(v);
+    if ((u << 1) == 0u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+template <int PL>
 __device__ __forceinline__ bool rank_token(const float* __restrict__ lrow, int N, int R, int k, bool renorm,
                                            int& my_id, float& my_gate) {
     const int lane = threadIdx.x & 31;
-    float lv[kMaxPerLane], ev[kMaxPerLane];
+    float lv[PL], ev[PL];
+    uint32_t kv[PL];
     bool finite = true;
+    uint32_t lmax = 0u;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
         const int j = lane + 32 * i;
         lv[i] = (j < N) ? lrow[j] : 0.f;
         if (j < N && !isfinite(lv[i])) finite = false;
+        kv[i] = (j < N) ? order_key(lv[i]) : 0u;   // every finite logit has a key > 0
+        lmax = max(lmax, kv[i]);
     }
     const bool all_finite = __all_sync(kFull, finite);
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i)
-        if (lane + 32 * i < N) m = fmaxf(m, lv[i]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+    const float m = key_value(__reduce_max_sync(kFull, lmax));
     float part = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
         const int j = lane + 32 * i;
         ev[i] = (j < N) ? exp_gate(__fsub_rn(lv[i], m)) : 0.f;
         if (j < N) part = __fadd_rn(part, ev[i]);
@@ -182,35 +221,35 @@ __device__ __forceinline__ bool rank_token(const float* __restrict__ lrow, int N
     const float Z = part;
     unsigned taken = 0u;
     my_id = -1;
-    my_gate = 0.f;
     for (int r = 0; r < R; ++r) {
-        float bv = 0.f;
-        int bi = -1;
+        uint32_t bk = 0u;
+        int bj = 0;
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
-            const int j = lane + 32 * i;
-            if (j < N && !(taken >> i & 1u) && (bi < 0 || ranks_before(lv[i], j, bv, bi))) {
-                bv = lv[i];
-                bi = j;
+        for (int i = 0; i < PL; ++i) {
+            if (!(taken >> i & 1u) && kv[i] > bk) {   // strict: the lower id wins within the lane
+                bk = kv[i];
+                bj = lane + 32 * i;
             }
         }
-        warp_best(bv, bi);
-        float g = 0.f;
-        if ((bi & 31) == lane) {
-            const int i = bi >> 5;
+        const uint32_t mk = __reduce_max_sync(kFull, bk);
+        const uint32_t cand = (bk == mk && bk != 0u) ? static_cast<uint32_t>(bj) : 0xffffffffu;
+        const int jsel = static_cast<int>(__reduce_min_sync(kFull, cand));
+        if ((jsel & 31) == lane) {
 #pragma unroll
-            for (int q = 0; q < kMaxPerLane; ++q)
-                if (q == i) {
-                    taken |= 1u << q;
-                    g = __fdiv_rn(ev[q], Z);
-                }
+            for (int q = 0; q < PL; ++q)
+                if (q == (jsel >> 5)) taken |= 1u << q;
         }
-        g = __shfl_sync(kFull, g, bi & 31);
-        if (lane == r) {
-            my_id = bi;
-            my_gate = g;
-        }
+        if (lane == r) my_id = jsel;
     }
+    // each lane r < R fetches e of its expert from the owning lane, then divides
+    const int mine = my_id >= 0 ? my_id : 0;
+    float e_mine = 0.f;
+#pragma unroll
+    for (int q = 0; q < PL; ++q) {
+        const float v = __shfl_sync(kFull, ev[q], mine & 31);
+        if (q == (mine >> 5)) e_mine = v;
+    }
+    my_gate = (lane < R) ? __fdiv_rn(e_mine, Z) : 0.f;
     if (renorm) {
         float s = 0.f;
         for (int r = 0; r < k; ++r) s = __fadd_rn(s, __shfl_sync(kFull, my_gate, r));
@@ -219,15 +258,18 @@ __device__ __forceinline__ bool rank_token(const float* __restrict__ lrow, int N
     return all_finite;
 }
 
+template <int PL>
 __global__ void __launch_bounds__(256) rank_kernel(const float* __restrict__ logits, int T, int N, int R, int k,
                                                    int renorm, int32_t* __restrict__ ids,
                                                    float* __restrict__ gates, moe_dev_status* st) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
     int id;
     float g;
-    const bool ok = rank_token(logits + static_cast<size_t>(t) * N, N, R, k, renorm != 0, id, g);
+    const bool ok = rank_token<PL>(logits + static_cast<size_t>(t) * N, N, R, k, renorm != 0, id, g);
     if (!ok && lane == 0) report(st, MOE_DEV_NONFINITE, t);
     if (lane < R) {
         ids[static_cast<size_t>(t) * R + lane] = id;
@@ -235,11 +277,20 @@ __global__ void __launch_bounds__(256) rank_kernel(const float* __restrict__ log
     }
 }
 
+template <int PL>
+static cudaError_t rank_launch(const float* logits, int T, int N, int R, int k, bool renorm, int32_t* ids,
+                               float* gates, moe_dev_status* st, cudaStream_t s) {
+    return launch_pdl(rank_kernel<PL>, dim3((T + 7) / 8), dim3(256), 0, s, logits, T, N, R, k, renorm ? 1 : 0, ids,
+                      gates, st);
+}
+
 cudaError_t launch_rank(const float* logits, int T, int N, int R, int k, bool renorm, int32_t* ids, float* gates,
                         moe_dev_status* st, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    rank_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, N, R, k, renorm ? 1 : 0, ids, gates, st);
-    return cudaGetLastError();
+    if (N <= 32) return rank_launch<1>(logits, T, N, R, k, renorm, ids, gates, st, s);
+    if (N <= 64) return rank_launch<2>(logits, T, N, R, k, renorm, ids, gates, st, s);
+    if (N <= 128) return rank_launch<4>(logits, T, N, R, k, renorm, ids, gates, st, s);
+    return rank_launch<8>(logits, T, N, R, k, renorm, ids, gates, st, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -247,6 +298,7 @@ cudaError_t launch_rank(const float* logits, int T, int N, int R, int k, bool re
 // slot r as (id, gate).  P is the primary-union bitmap in shared memory.
 // stats: [3] moved, [4] merged, [5] kept-protected, [6] kept-dissimilar.
 // ---------------------------------------------------------------------------
+template <int PL>
 __device__ __forceinline__ void sere_token(int N, int k, int kp, float rho, const float* __restrict__ sim,
                                            const uint8_t* __restrict__ protect, const uint32_t* Pbits,
                                            int& my_id, float& my_gate, int* sstats) {
@@ -261,22 +313,24 @@ __device__ __forceinline__ void sere_token(int N, int k, int kp, float rho, cons
             continue;
         }
         const float* srow = sim + static_cast<size_t>(s) * N;
-        float bv = 0.f;
-        int bi = -1;
+        uint32_t bk = 0u;
+        int bp = 0;
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
+        for (int i = 0; i < PL; ++i) {
             const int p = lane + 32 * i;
             if (p < N && (Pbits[p >> 5] >> (p & 31) & 1u)) {
-                const float v = srow[p];
-                if (bi < 0 || ranks_before(v, p, bv, bi)) {
-                    bv = v;
-                    bi = p;
+                const uint32_t key = order_key(srow[p]);
+                if (key > bk) {
+                    bk = key;
+                    bp = p;
                 }
             }
         }
-        warp_best(bv, bi);
-        if (bi >= 0 && bv > rho) {
-            const unsigned holder = __ballot_sync(kFull, lane < k && my_id == bi);
+        const uint32_t mk = __reduce_max_sync(kFull, bk);
+        const uint32_t cand = (bk == mk && bk != 0u) ? static_cast<uint32_t>(bp) : 0xffffffffu;
+        const int pbest = static_cast<int>(__reduce_min_sync(kFull, cand));
+        if (mk != 0u && key_value(mk) > rho) {
+            const unsigned holder = __ballot_sync(kFull, lane < k && my_id == pbest);
             const float gr = __shfl_sync(kFull, my_gate, r);
             if (holder != 0u) {
                 const int q = __ffs(holder) - 1;
@@ -287,7 +341,7 @@ __device__ __forceinline__ void sere_token(int N, int k, int kp, float rho, cons
                 }
                 if (lane == 0) atomicAdd(&sstats[4], 1);
             } else {
-                if (lane == r) my_id = bi;
+                if (lane == r) my_id = pbest;
                 if (lane == 0) atomicAdd(&sstats[3], 1);
             }
         } else if (lane == 0) {
@@ -296,92 +350,214 @@ __device__ __forceinline__ void sere_token(int N, int k, int kp, float rho, cons
     }
 }
 
-// One CTA of 1024 threads handles the whole batch: (optionally) rank every
-// token, build the primary union P and the before-union, reroute, build the
-// after-union, publish stats.  No host synchronisation, no extra sort.
-__global__ void __launch_bounds__(1024) rank_sere_kernel(const float* __restrict__ logits, int do_rank, int T,
-                                                         int N, int k, int renorm, int32_t* __restrict__ ids,
-                                                         float* __restrict__ gates, int ld, int kp, float rho,
-                                                         const float* __restrict__ sim,
-                                                         const uint8_t* __restrict__ protect,
-                                                         uint32_t* __restrict__ union_bitmap,
-                                                         int32_t* __restrict__ stats, moe_dev_status* st) {
-    __shared__ uint32_t Pbits[kMaxPerLane], Ubefore[kMaxPerLane], Uafter[kMaxPerLane];
+// ---------------------------------------------------------------------------
+// The fused routing kernel: one thread-block cluster of CL CTAs (8 warps each)
+// handles the whole batch.  Each CTA ranks its share of the tokens, the
+// primary union P is OR-ed across the cluster through distributed shared
+// memory, each CTA reroutes its own tokens against P, and CTA 0 gathers the
+// after-union and the statistics.  Cluster barriers are hardware barriers; no
+// host synchronisation and no sort.  Each CTA streams the similarity matrix
+// into its shared memory with one bulk copy issued at the start, which lands
+// while the tokens are being ranked.
+// ---------------------------------------------------------------------------
+namespace cg = cooperative_groups;
+constexpr int kSereWarps = 8;
+
+template <int PL>
+__global__ void __launch_bounds__(256, 1) rank_sere_kernel(const float* __restrict__ logits, int do_rank, int T,
+                                                           int N, int k, int renorm, int32_t* __restrict__ ids,
+                                                           float* __restrict__ gates, int ld, int kp, float rho,
+                                                           const float* __restrict__ sim,
+                                                           const uint8_t* __restrict__ protect,
+                                                           uint32_t* __restrict__ union_bitmap,
+                                                           int32_t* __restrict__ stats, moe_dev_status* st,
+                                                           int stage_sim) {
+    __shared__ uint32_t Ploc[kMaxPerLane], Pall[kMaxPerLane], Ubefore[kMaxPerLane], Uafter[kMaxPerLane];
     __shared__ int sstats[8];
+    __shared__ __align__(8) uint64_t sim_bar;
+    __shared__ int abort_flag;
+    extern __shared__ float4 s_sim4[];  // [N][N] fp32 similarity then [N] protect bytes, when staged
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = static_cast<int>(cluster.block_rank());
+    const int csize = static_cast<int>(cluster.num_blocks());
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gwarp = crank * kSereWarps + warp, nwarps = csize * kSereWarps;
+    const int n4 = (N * N) / 4;
+    bool staged = stage_sim != 0;
     if (threadIdx.x < kMaxPerLane) {
-        Pbits[threadIdx.x] = 0u;
+        Ploc[threadIdx.x] = 0u;
         Ubefore[threadIdx.x] = 0u;
         Uafter[threadIdx.x] = 0u;
     }
     if (threadIdx.x < 8) sstats[threadIdx.x] = 0;
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        if (staged) {
+            mbar_init(smem_u32(&sim_bar), 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(smem_u32(&sim_bar), static_cast<uint32_t>(n4) * 16u);
+            bulk_copy_g2s(smem_u32(s_sim4), sim, static_cast<uint32_t>(n4) * 16u, smem_u32(&sim_bar));
+        }
+    }
+    uint8_t* sprot = reinterpret_cast<uint8_t*>(s_sim4 + n4);
+    if (staged && protect != nullptr)
+        for (int i = threadIdx.x; i < N; i += blockDim.x) sprot[i] = protect[i];
     __syncthreads();
-    for (int t = warp; t < T; t += 32) {
-        int id = -1;
-        float g = 0.f;
+    // with at most one token per warp the routing stays in registers between the phases
+    const bool in_regs = T <= nwarps;
+    int id = -1;
+    float g = 0.f;
+    for (int t = gwarp; t < T; t += nwarps) {
+        id = -1;
+        g = 0.f;
         if (do_rank) {
-            const bool ok = rank_token(logits + static_cast<size_t>(t) * N, N, k, k, renorm != 0, id, g);
+            const bool ok = rank_token<PL>(logits + static_cast<size_t>(t) * N, N, k, k, renorm != 0, id, g);
             if (!ok && lane == 0) report(st, MOE_DEV_NONFINITE, t);
-            if (lane < k) {
+            if (!in_regs && lane < k) {
                 ids[static_cast<size_t>(t) * ld + lane] = id;
                 gates[static_cast<size_t>(t) * ld + lane] = g;
             }
         } else if (lane < k) {
             id = ids[static_cast<size_t>(t) * ld + lane];
+            g = gates[static_cast<size_t>(t) * ld + lane];
         }
-        if (lane < k && id >= N) report(st, MOE_DEV_BAD_INDEX, id);
-        if (lane < k && id >= 0 && id < N) {
+        if (lane < k && id >= N) {
+            report(st, MOE_DEV_BAD_INDEX, id);
+            id = -1;
+        }
+        if (lane < k && id >= 0) {
             atomicOr(&Ubefore[id >> 5], 1u << (id & 31));
-            if (lane < kp) atomicOr(&Pbits[id >> 5], 1u << (id & 31));
+            if (lane < kp) atomicOr(&Ploc[id >> 5], 1u << (id & 31));
         }
     }
-    __syncthreads();
-    for (int t = warp; t < T; t += 32) {
-        int id = -1;
-        float g = 0.f;
-        if (lane < k) {
-            id = ids[static_cast<size_t>(t) * ld + lane];
-            g = gates[static_cast<size_t>(t) * ld + lane];
-            if (id >= N) id = -1;
+    cluster.sync();  // every CTA's local primaries are in its shared memory
+    if (threadIdx.x < kMaxPerLane) {
+        uint32_t v = 0u;
+        for (int r = 0; r < csize; ++r) v |= cluster.map_shared_rank(Ploc, r)[threadIdx.x];
+        Pall[threadIdx.x] = v;
+    }
+    if (staged) {
+        // every thread observes the copy's completion (bounded); on a time-out
+        // the kernel records it and reads the similarity from global memory
+        if (!mbar_wait(smem_u32(&sim_bar), 0, &abort_flag, st, kSiteDrain)) staged = false;
+    }
+    staged = __syncthreads_and(staged ? 1 : 0) != 0;
+    const float* simp = staged ? reinterpret_cast<const float*>(s_sim4) : sim;
+    const uint8_t* protp = (staged && protect != nullptr) ? sprot : protect;
+    for (int t = gwarp; t < T; t += nwarps) {
+        if (!in_regs) {
+            id = -1;
+            g = 0.f;
+            if (lane < k) {
+                id = ids[static_cast<size_t>(t) * ld + lane];
+                g = gates[static_cast<size_t>(t) * ld + lane];
+                if (id >= N) id = -1;
+            }
         }
-        sere_token(N, k, kp, rho, sim, protect, Pbits, id, g, sstats);
+        sere_token<PL>(N, k, kp, rho, simp, protp, Pall, id, g, sstats);
         if (lane < k) {
             ids[static_cast<size_t>(t) * ld + lane] = id;
             gates[static_cast<size_t>(t) * ld + lane] = g;
             if (id >= 0) atomicOr(&Uafter[id >> 5], 1u << (id & 31));
         }
     }
+    cluster.sync();  // every CTA's after-union and counters are final
+    if (crank == 0) {
+        if (threadIdx.x < kMaxPerLane) {
+            uint32_t ub = 0u, ua = 0u;
+            for (int r = 0; r < csize; ++r) {
+                ub |= cluster.map_shared_rank(Ubefore, r)[threadIdx.x];
+                ua |= cluster.map_shared_rank(Uafter, r)[threadIdx.x];
+            }
+            Ubefore[threadIdx.x] = ub;   // safe: the other CTAs read only Ploc from this CTA
+            Uafter[threadIdx.x] = ua;
+            if (union_bitmap != nullptr && threadIdx.x < (N + 31) / 32) union_bitmap[threadIdx.x] = Pall[threadIdx.x];
+        } else if (threadIdx.x >= 32 && threadIdx.x < 40) {
+            const int i = threadIdx.x - 32;
+            int v = 0;
+            for (int r = 0; r < csize; ++r) v += cluster.map_shared_rank(sstats, r)[i];
+            sstats[i] = v;   // only CTA 0's own copy is rewritten, after every remote read of it
+        }
+    }
+    if (stage_sim != 0 && !staged && threadIdx.x == 0) {
+        // the copy did not complete in time: let it land before this CTA's shared memory is released
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(smem_u32(&sim_bar), 0) && global_ns() - t0 < kWaitLimitNs) {
+        }
+    }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (crank == 0 && threadIdx.x == 0 && stats != nullptr) {
         int ub = 0, np = 0, ua = 0;
         for (int w = 0; w < kMaxPerLane; ++w) {
             ub += __popc(Ubefore[w]);
-            np += __popc(Pbits[w]);
+            np += __popc(Pall[w]);
             ua += __popc(Uafter[w]);
         }
-        if (stats != nullptr) {
-            stats[0] = ub;
-            stats[1] = np;
-            stats[2] = ua;
-            for (int i = 3; i < 7; ++i) stats[i] = sstats[i];
-            stats[7] = 0;
-        }
+        stats[0] = ub;
+        stats[1] = np;
+        stats[2] = ua;
+        for (int i = 3; i < 7; ++i) stats[i] = sstats[i];
+        stats[7] = 0;
     }
-    if (union_bitmap != nullptr && threadIdx.x < (N + 31) / 32) union_bitmap[threadIdx.x] = Pbits[threadIdx.x];
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
+}
+
+template <int PL>
+static cudaError_t sere_launch_pl(const float* logits, int do_rank, int T, int N, int k, bool renorm, int32_t* ids,
+                                  float* gates, int ld, const moe_sere_params& p, moe_dev_status* st, cudaStream_t s,
+                                  bool stage, size_t smem, int csize) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(rank_sere_kernel<PL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSereStageN * kSereStageN * 4 + kSereStageN + 16));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(csize);
+    cfg.blockDim = dim3(32 * kSereWarps);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const int renorm_i = renorm ? 1 : 0, stage_i = stage ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, rank_sere_kernel<PL>, logits, do_rank, T, N, k, renorm_i, ids, gates, ld,
+                              p.k_primary, p.rho, p.sim, p.protect, p.union_bitmap, p.stats, st, stage_i);
+}
+
+// Stages sim in shared memory when it fits and can be copied with 16-byte
+// transfers; the cluster has one CTA per 8 tokens, at most 8 CTAs.
+static cudaError_t sere_launch(const float* logits, int do_rank, int T, int N, int k, bool renorm, int32_t* ids,
+                               float* gates, int ld, const moe_sere_params& p, moe_dev_status* st, cudaStream_t s) {
+    const bool stage = N <= kSereStageN && (N % 2) == 0 && (reinterpret_cast<uintptr_t>(p.sim) & 15u) == 0;
+    const size_t smem = stage ? (static_cast<size_t>(N) * N * 4 + N + 15) / 16 * 16 : 0;
+    int csize = (T + kSereWarps - 1) / kSereWarps;
+    csize = csize < 1 ? 1 : (csize > 8 ? 8 : csize);
+    if (N <= 32) return sere_launch_pl<1>(logits, do_rank, T, N, k, renorm, ids, gates, ld, p, st, s, stage, smem, csize);
+    if (N <= 64) return sere_launch_pl<2>(logits, do_rank, T, N, k, renorm, ids, gates, ld, p, st, s, stage, smem, csize);
+    if (N <= 128) return sere_launch_pl<4>(logits, do_rank, T, N, k, renorm, ids, gates, ld, p, st, s, stage, smem, csize);
+    return sere_launch_pl<8>(logits, do_rank, T, N, k, renorm, ids, gates, ld, p, st, s, stage, smem, csize);
 }
 
 cudaError_t launch_rank_sere(const float* logits, int T, int N, int k, bool renorm, int32_t* ids, float* gates,
                              const moe_sere_params& p, moe_dev_status* st, cudaStream_t s) {
-    rank_sere_kernel<<<1, 1024, 0, s>>>(logits, 1, T, N, k, renorm ? 1 : 0, ids, gates, k, p.k_primary, p.rho,
-                                        p.sim, p.protect, p.union_bitmap, p.stats, st);
-    return cudaGetLastError();
+    return sere_launch(logits, 1, T, N, k, renorm, ids, gates, k, p, st, s);
 }
 
 cudaError_t launch_sere(int32_t* ids, float* gates, int ld, int T, int N, int k, const moe_sere_params& p,
                         moe_dev_status* st, cudaStream_t s) {
-    rank_sere_kernel<<<1, 1024, 0, s>>>(nullptr, 0, T, N, k, 0, ids, gates, ld, p.k_primary, p.rho, p.sim,
-                                        p.protect, p.union_bitmap, p.stats, st);
-    return cudaGetLastError();
+    return sere_launch(nullptr, 0, T, N, k, false, ids, gates, ld, p, st, s);
 }
 
 }  // namespace moe

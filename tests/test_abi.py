@@ -43,7 +43,7 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    assert abi.workspace_size(abi.MOE_OP_FFN, 32, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16) >= 256 * 2048 * 2
+    assert abi.workspace_size(abi.MOE_OP_FFN, 32, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16) == 0
     assert abi.workspace_size(abi.MOE_OP_FFN, 32, 64, 128, 8, 2, 2, False, abi.MOE_DTYPE_F32) == 0
     capped = abi.workspace_size(abi.MOE_OP_DISPATCH, 8192, 2048, 768, 128, 8, 10, True, abi.MOE_DTYPE_BF16)
     assert capped >= 2 * 128 * 8192 * 4
@@ -112,9 +112,12 @@ def test_ffn_rejects(lib):
              None) == -2
     assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 128, 96, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, 1 << 30, None,
              None) == -2
-    # missing workspace
-    assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 128, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, None, 0, None,
-             None) == -4
+    # misaligned x and a misaligned workspace
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert f(odd, 1, FAKE, FAKE, FAKE, 4, 128, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, None, 0, None,
+             None) == -1
+    assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 128, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, odd, 1 << 20, None,
+             None) == -1
     # unknown dtype and unknown flag
     assert f(FAKE, 7, FAKE, FAKE, FAKE, 4, 128, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, 1 << 30, None,
              None) == -1
