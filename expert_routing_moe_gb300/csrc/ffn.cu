@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
             __syncwarp();
             if (lane == 0) {
                 const int wrow = e * I + s * C::BI;
+                const int n_g4 = (nrows + 3) / 4;
                 for (int kt = 0; kt < KT + MT; ++kt) {
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
@@ -242,11 +243,12 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
                     const uint32_t dst = ring_a + stage * C::STAGE;
                     const uint32_t fb = bar(B_FULL + stage);
                     if (kt < KT) {
-                        mbar_arrive_expect_tx(fb, C::STAGE);
+                        // only the gathers that hold real rows; the MMA's N covers them, rows past
+                        // nrows in the last 16-row group belong to columns that are never used
+                        mbar_arrive_expect_tx(fb, C::W_BYTES + n_g4 * 512);
                         tma_load_2d(dst, &tm_wg, kt * C::BK, wrow, fb, pol_w);
                         tma_load_2d(dst + C::W_BOX, &tm_wu, kt * C::BK, wrow, fb, pol_w);
-#pragma unroll
-                        for (int g = 0; g < NT / 4; ++g)
+                        for (int g = 0; g < n_g4; ++g)
                             tma_gather4(dst + C::W_BYTES + g * 512, &tm_x, kt * C::BK, ptok[4 * g], ptok[4 * g + 1],
                                         ptok[4 * g + 2], ptok[4 * g + 3], fb, pol_x);
                     } else {
@@ -275,11 +277,15 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            const uint32_t idesc = idesc_bf16_f32(128, NT);
             int stage = 0, j = 0;
             uint32_t phase = 0, n2 = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++j) {
+                // the MMA's N is the unit's row count rounded up to 16
+                int ue, us, urow0, unrows;
+                unit_info(tb, u, S, NT, ue, us, urow0, unrows);
+                const int n_eff = min(NT, max(16, (unrows + 15) & ~15));
+                const uint32_t idesc = idesc_bf16_f32(128, n_eff);
                 if (!mbar_wait(bar(B_TMEMFREE), (j & 1) ^ 1, abort_flag, st, kSiteMmaTmemFree)) break;
                 tc_fence_after();
                 for (int kt = 0; kt < KT && ok; ++kt) {
@@ -367,9 +373,11 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
 #pragma unroll
                 for (int c8 = 0; c8 < CW / 8; ++c8) {
                     uint32_t g[8], v[8];
-                    tmem_ld8(t_gate + lane_off + c_lo + c8 * 8, g);
-                    tmem_ld8(t_up + lane_off + c_lo + c8 * 8, v);
-                    tmem_ld_wait();
+                    if (c_lo + c8 * 8 < nrows) {   // warp-uniform
+                        tmem_ld8(t_gate + lane_off + c_lo + c8 * 8, g);
+                        tmem_ld8(t_up + lane_off + c_lo + c8 * 8, v);
+                        tmem_ld_wait();
+                    }
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) {
                         const int t = c_lo + c8 * 8 + jj;
@@ -406,24 +414,41 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t v[CW];
-                tmem_ld_cols<CW>(t_acc2 + b * NT + lane_off + c_lo, v);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(bar(B_ACC2E + b));   // the accumulator is free again; reductions follow
+                // read the accumulator in chunks of up to 16 columns; it is released right
+                // after the last read, before the last chunk's reductions
+                constexpr int CH = CW < 16 ? CW : 16;
                 const int h = m * C::BH + row;
 #pragma unroll
-                for (int jj = 0; jj < CW; ++jj) {
-                    const int t = c_lo + jj;
-                    if (t < nrows) {
-                        if (fuse_combine)
-                            atomicAdd(out + static_cast<size_t>(etok[jj]) * H + h, egt[jj] * __uint_as_float(v[jj]));
-                        else
-                            atomicAdd(out + static_cast<size_t>(row0 + t) * H + h, __uint_as_float(v[jj]));
+                for (int c16 = 0; c16 < CW / CH; ++c16) {
+                    const bool any = c_lo + c16 * CH < nrows;   // warp-uniform
+                    uint32_t v[CH];
+                    if (any) {
+                        if constexpr (CH == 8) {
+                            tmem_ld8(t_acc2 + b * NT + lane_off + c_lo, v);
+                        } else {
+                            tmem_ld16(t_acc2 + b * NT + lane_off + c_lo + c16 * CH, v);
+                        }
+                        tmem_ld_wait();
+                    }
+                    if (c16 == CW / CH - 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar(B_ACC2E + b));
+                    }
+                    if (!any) continue;
+#pragma unroll
+                    for (int jj = 0; jj < CH; ++jj) {
+                        const int t = c_lo + c16 * CH + jj;
+                        const int js = c16 * CH + jj;   // index into this warp's token slice
+                        if (t < nrows) {
+                            if (fuse_combine)
+                                atomicAdd(out + static_cast<size_t>(etok[js]) * H + h, egt[js] * __uint_as_float(v[jj]));
+                            else
+                                atomicAdd(out + static_cast<size_t>(row0 + t) * H + h, __uint_as_float(v[jj]));
+                        }
                     }
                 }
             }
-            __syncwarp();
+            __syncwarp();   // the warp's token slice is rewritten for the next unit
             if (!ok) break;
         }
     }

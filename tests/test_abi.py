@@ -111,7 +111,7 @@ def test_ffn_rejects(lib):
     assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 96, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, 1 << 30, None,
              None) == -2
     assert f(FAKE, 1, FAKE, FAKE, FAKE, 4, 128, 96, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, 1 << 30, None,
-             None) == -2
+             None) == -2   # I % 128
     # misaligned x and a misaligned workspace
     odd = ctypes.c_void_p((1 << 20) + 8)
     assert f(odd, 1, FAKE, FAKE, FAKE, 4, 128, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, 1, FAKE, None, 0, None,

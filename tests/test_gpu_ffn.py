@@ -89,6 +89,14 @@ def test_small_bf16_multi_chunk_ragged(g):
     _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
 
 
+def test_small_bf16_odd_slice_count(g):
+    """I = 384: three 128-row slices per expert; H = 256: two down-projection tiles."""
+    L = syn.qwen_layer(24, H=256, N=8, k=3, I=384)
+    D = g.DevLayer(L)
+    ids, gates = _route(L, L.x_bf16, 24)
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
+
+
 def test_repeat_calls_are_stable(g, qwen):
     L, D = qwen
     ids, gates = _route(L, L.x_bf16, L.T)
