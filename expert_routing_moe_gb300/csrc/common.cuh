@@ -24,6 +24,7 @@ enum WaitSite : int {
     kSiteEpiActFree = 7,
     kSiteEpiAcc2Full = 8,
     kSiteDrain = 9,
+    kSiteDependency = 10,
 };
 
 // Longest time a single on-chip wait may take before the kernel gives up
@@ -192,6 +193,40 @@ __device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int x, int y) 
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy accesses to global memory with its
+// later (or earlier) async-proxy ones, e.g. TMA loads of data that another
+// CTA stored with plain st.global.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Named barrier 1 over `nthreads` threads (whole warps) that returns the AND
+// of every participant's `v`.  Callers pass it the same number of times in
+// every participating warp, so that a failed wait in one warp cannot strand
+// the others at a barrier: they all learn of it here and leave together.
+__device__ __forceinline__ bool named_sync_and(int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------------------

@@ -7,16 +7,10 @@
 // active experts' weights (the decode bottleneck the SERE article measures in
 // sec. 1.2 / 2.2).
 //
-// bf16 path (tensor cores): a persistent kernel, one CTA per SM, walks work
-// units (expert e, token chunk of <= NT rows, 128-row slice of I).  For a
-// unit it streams W_gate/W_up[e][slice][:] and W_down[e][:][slice] once
-// through a TMA ring in shared memory and runs two tcgen05 GEMMs with the
-// weights as the 128-row MMA operand and the tokens as the N operand:
-//   GEMM1  D_g, D_u [128 x NT] = W_{gate,up}[slice] . X_chunk^T    (K = H)
-//   SwiGLU A = silu(D_g) * D_u  -> bf16 in shared memory            (epilogue)
-//   GEMM2  D_y [128 x NT] = W_down[h-tile][slice] . A^T            (K = 128)
-// and adds gate * D_y into y with coalesced fp32 reductions.  Warp roles:
-// warp 0 TMA producer, warp 1 MMA issuer + TMEM owner, warps 2-5 epilogue.
+// bf16 path (tensor cores): one persistent kernel, one CTA per SM, with the
+// weights as the 128-row MMA operand and the tokens as the N operand (decode
+// batches give each expert only a handful of rows); it is described at
+// ffn_stream_kernel below.
 // fp32 path: a CUDA-core kernel, one CTA per row.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -28,44 +22,30 @@
 namespace moe {
 
 
-// ---------------------------------------------------------------------------
-// Tile configuration of the tensor-core kernel.
-// ---------------------------------------------------------------------------
-template <int NT>
-struct TcCfg {
-    static constexpr int BI = 128;                 // slice of I per unit (GEMM1 M)
-    static constexpr int BK = 64;                  // K tile: 64 bf16 = one 128-byte swizzle row
-    static constexpr int BH = 128;                 // H tile of GEMM2 (GEMM2 M)
-    static constexpr int W_BOX = 128 * 64 * 2;     // one 128x64 bf16 box = 16 KiB
-    static constexpr int W_BYTES = 2 * W_BOX;      // two boxes per stage
-    static constexpr int X_BYTES = NT * 64 * 2;    // token tile per stage (NT gathered rows)
-    static constexpr int STAGE = W_BYTES + X_BYTES;
-    static constexpr int NSTAGE = (NT <= 16) ? 6 : 5;
-    static constexpr int ACT_BYTES = NT * BI * 2;  // two 64-column swizzle atoms of NT rows
-    static constexpr int NACC2 = (NT <= 32) ? 4 : 2;
-    static constexpr int EPI_WARPS = 8;            // two warps per TMEM lane quadrant
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-    static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-    static constexpr int CW = NT / 2;              // token columns per epilogue warp
-    static constexpr int NBAR = 2 * NSTAGE + 5 + 2 * NACC2;
-    static constexpr int TABLE_INTS = 4 * MOE_MAX_EXPERTS + 4;
-    static constexpr int SMEM =
-        1024 + NSTAGE * STAGE + ACT_BYTES + NBAR * 8 + 16 + 64 * 4 + TABLE_INTS * 4 + EPI_WARPS * 32 * 8;
-    static constexpr uint32_t TMEM_COLS = 256;
-    static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
-    static_assert((2 + NACC2) * NT <= (int)TMEM_COLS, "TMEM columns");
-    static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(CW == 8 || CW == 16 || CW == 32, "epilogue column split");
-};
+// Token-chunk width of the bf16 kernels for a batch of T tokens.
+static int ffn_nt(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
 
-size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype) {
-    (void)T; (void)H; (void)I; (void)N; (void)k; (void)dtype;
-    return 0;  // the tensor-core path reads token rows straight from x
+// Upper bound on the items (expert, chunk of <= nt rows) of a dispatch of M rows.
+static long long ffn_max_items(int T, int N, int k, int nt) {
+    const long long M = static_cast<long long>(T) * k;
+    return (N < M ? N : M) + (M + nt - 1) / nt;
 }
 
-// Work units: for every active expert a, ceil(rows/NT) token chunks, each
-// split into I/128 slices.  The table (built once per CTA in shared memory)
-// holds, per active expert, its id, first row, row count and first chunk.
+static size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// bf16 workspace: the work counter and the per-item phase-1 completion
+// counters (int32), then the SwiGLU activations A [T*k][I] bf16 (row =
+// dispatch row).
+size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype) {
+    (void)H;
+    if (dtype != MOE_DTYPE_BF16 || T <= 0) return 0;
+    const long long items = ffn_max_items(T, N, k, ffn_nt(T));
+    return align256(static_cast<size_t>(items + 1) * 4) + static_cast<size_t>(T) * k * I * 2;
+}
+
+// Items: for every active expert a, ceil(rows/NT) token chunks.  The table
+// (built once per CTA in shared memory) holds, per active expert, its id,
+// first row, row count and first item.
 struct UnitTable {
     int* e;      // [na]
     int* row;    // [na]
@@ -74,10 +54,68 @@ struct UnitTable {
     int na;
 };
 
-__device__ __forceinline__ void unit_info(const UnitTable& tb, int u, int S, int NT, int& e, int& s, int& row0,
-                                          int& nrows) {
-    const int item = u / S;
-    s = u - item * S;
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+// ---------------------------------------------------------------------------
+// Two-phase streamed kernel (the bf16 path).
+//
+// Decode moves the active experts' weights once and does little else, so
+// the kernel is cut into many small units that keep every SM streaming to
+// the end.  (One unit per (chunk, I-slice) with its whole down-projection
+// moves 1.5 MiB, and a batch of a few dozen active experts then splits into
+// too few units to fill 152 SMs evenly.)  The FFN of every item (expert,
+// token chunk) runs as
+//   phase 1, S = I/128 units:  A[rows][slice] = silu(W_gate[slice] X^T) *
+//            (W_up[slice] X^T), the full K = H, rounded to bf16 and stored
+//            in a row-major activation buffer in the workspace;
+//   phase 2, H/128 units:      D[h-tile] = W_down[h-tile][:] A^T over the
+//            full K = I, added as gate * D into y.
+// A phase-2 unit starts once the S phase-1 units of its item have
+// published their part of A (a per-item counter, release/acquire).  Units
+// are handed out by a global work counter, all phase-1 units first and
+// item by item, so SMs that stream faster simply take more units and the
+// kernel ends within about one 192 KiB phase-2 unit of the last SM.  A unit
+// is only ever taken by a running CTA, and a phase-2 unit waits only for
+// phase-1 units already taken, so the waits end whatever the residency of
+// the grid; a wait that outlasts kWaitLimitNs reports MOE_DEV_TIMEOUT.
+// ---------------------------------------------------------------------------
+template <int NT>
+struct StCfg {
+    static constexpr int BI = 128;                  // I-slice of a phase-1 unit (MMA M)
+    static constexpr int BH = 128;                  // H-tile of a phase-2 unit (MMA M)
+    static constexpr int BK = 64;                   // one 128-byte swizzle row of bf16
+    static constexpr int W_BOX = 128 * 64 * 2;      // one 128 x 64 bf16 box = 16 KiB
+    static constexpr int W_BYTES = 2 * W_BOX;       // gate + up (phase 1) or two K halves of W_down (phase 2)
+    static constexpr int X_ATOM = NT * 128;         // NT rows of one 64-column swizzle atom
+    static constexpr int X_BYTES = 2 * X_ATOM;      // phase 2 stages 128 columns of A
+    static constexpr int STAGE = W_BYTES + X_BYTES;
+    static constexpr int NSTAGE = NT <= 16 ? 6 : (NT <= 32 ? 5 : 4);
+    static constexpr int EPI_WARPS = 8;             // two warps per TMEM lane quadrant
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+    static constexpr int CW = NT / 2;               // token columns per epilogue warp
+    static constexpr int QN = 4;                    // unit ids in flight between the warp roles
+    static constexpr int NBAR = 2 * NSTAGE + 5 + 2 * QN;
+    static constexpr int MISC_INTS = 8 + 64;        // tmem slot, abort flag, table size, unit ring, token list
+    static constexpr int TABLE_INTS = 4 * MOE_MAX_EXPERTS + 4;
+    static constexpr int SMEM =
+        1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + TABLE_INTS * 4 + EPI_WARPS * 32 * 8;
+    static constexpr uint32_t TMEM_COLS = 4 * NT;   // two accumulator slots of 2 x NT columns
+    static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
+    static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256, "TMEM allocation");
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(CW == 8 || CW == 16 || CW == 32, "epilogue column split");
+};
+
+__device__ __forceinline__ void item_info(const UnitTable& tb, int item, int NT, int& e, int& row0, int& nrows) {
     int lo = 0, hi = tb.na - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -89,61 +127,35 @@ __device__ __forceinline__ void unit_info(const UnitTable& tb, int u, int S, int
     nrows = min(NT, tb.cnt[lo] - c * NT);
 }
 
-// ---------------------------------------------------------------------------
-// The tensor-core kernel.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-    return true;
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
-
-template <int CW>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[CW]) {
-    if constexpr (CW == 8) {
-        tmem_ld8(taddr, v);
-    } else {
-#pragma unroll
-        for (int c = 0; c < CW / 16; ++c) {
-            uint32_t w[16];
-            tmem_ld16(taddr + c * 16, w);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[c * 16 + j] = w[j];
-        }
-    }
-}
-
 template <int NT>
-__global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
-    ffn_tc_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
-                  const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
-                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ active,
-                  const int32_t* __restrict__ row_token, const float* __restrict__ row_gate,
-                  float* __restrict__ out, int H, int I, int N, int fuse_combine, moe_dev_status* st) {
-    using C = TcCfg<NT>;
+__global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
+    ffn_stream_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
+                      const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
+                      const __grid_constant__ CUtensorMap tm_act, const int32_t* __restrict__ offsets,
+                      const int32_t* __restrict__ active, const int32_t* __restrict__ row_token,
+                      const float* __restrict__ row_gate, __nv_bfloat16* __restrict__ act_g, int* counters,
+                      float* __restrict__ out, int H, int I, int N, int fuse_combine, moe_dev_status* st) {
+    using C = StCfg<NT>;
     constexpr int CW = C::CW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
-    uint8_t* act = smem + C::NSTAGE * C::STAGE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(act + C::ACT_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* s_units = reinterpret_cast<int*>(tmem_slot + 2);
-    int* ptok = reinterpret_cast<int*>(tmem_slot + 4);           // [64] token rows of the producer's unit
-    int* table = ptok + 64;
-    int* etok_all = table + C::TABLE_INTS;                           // [EPI_WARPS][32] tokens of each epilogue warp
-    float* egt_all = reinterpret_cast<float*>(etok_all + C::EPI_WARPS * 32);  // [EPI_WARPS][32] their gates
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + C::NSTAGE * C::STAGE);
+    int* misc = reinterpret_cast<int*>(bars + C::NBAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = misc + 1;
+    int* s_items = misc + 2;                         // active experts, items
+    volatile int* uring = misc + 4;                  // [QN] unit ids, -1 = no more work
+    int* ptok = misc + 8;                            // [64] token rows of the producer's phase-1 unit
+    int* table = misc + C::MISC_INTS;
+    int* etok_all = table + C::TABLE_INTS;           // [EPI_WARPS][32] tokens of each epilogue warp
+    float* egt_all = reinterpret_cast<float*>(etok_all + C::EPI_WARPS * 32);   // [EPI_WARPS][32] their gates
     UnitTable tb{table, table + MOE_MAX_EXPERTS, table + 2 * MOE_MAX_EXPERTS, table + 3 * MOE_MAX_EXPERTS, 0};
 
-    const uint32_t ring_a = smem_u32(ring), act_a = smem_u32(act);
+    const uint32_t ring_a = smem_u32(ring);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
-    const int B_FULL = 0, B_EMPTY = C::NSTAGE, B_G1 = 2 * C::NSTAGE, B_ACTRDY = B_G1 + 1, B_TMEMFREE = B_G1 + 2,
-              B_ACTFREE = B_G1 + 3, B_DRAIN = B_G1 + 4, B_ACC2F = B_G1 + 5, B_ACC2E = B_ACC2F + C::NACC2;
+    const int B_FULL = 0, B_EMPTY = C::NSTAGE, B_ACCF = 2 * C::NSTAGE, B_ACCE = B_ACCF + 2, B_DRAIN = B_ACCE + 2,
+              B_QFULL = B_DRAIN + 1, B_QEMPTY = B_QFULL + C::QN;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -151,14 +163,14 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
             mbar_init(bar(B_FULL + i), 1);
             mbar_init(bar(B_EMPTY + i), 1);
         }
-        mbar_init(bar(B_G1), 1);
-        mbar_init(bar(B_ACTRDY), C::EPI_THREADS);
-        mbar_init(bar(B_TMEMFREE), C::EPI_THREADS);
-        mbar_init(bar(B_ACTFREE), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_ACCF + b), 1);
+            mbar_init(bar(B_ACCE + b), C::EPI_THREADS);
+        }
         mbar_init(bar(B_DRAIN), 1);
-        for (int b = 0; b < C::NACC2; ++b) {
-            mbar_init(bar(B_ACC2F + b), 1);
-            mbar_init(bar(B_ACC2E + b), C::EPI_THREADS);
+        for (int i = 0; i < C::QN; ++i) {
+            mbar_init(bar(B_QFULL + i), 1);
+            mbar_init(bar(B_QEMPTY + i), 2);   // the MMA thread and the epilogue
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -168,12 +180,13 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
         tma_prefetch_desc(&tm_wu);
         tma_prefetch_desc(&tm_wd);
         tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_act);
     }
-    // everything above is private to this CTA; the dispatch outputs and y are read below
+    const int S = I / C::BI, MT = H / C::BH;
     pdl_wait();
     pdl_trigger();
     if (warp == 2) {
-        // work-unit table: prefix over active experts of their chunk counts
+        // item table: prefix over active experts of their chunk counts
         const int na = min(active[0], N);
         int run = 0;
         for (int base = 0; base < na; base += 32) {
@@ -201,15 +214,17 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
         }
         if (lane == 0) {
             tb.pre[na] = run;
-            s_units[0] = na;
-            s_units[1] = run * (I / C::BI);
+            s_items[0] = na;
+            s_items[1] = run;
         }
     }
     __syncthreads();
-    tb.na = s_units[0];
-    const int n_units = s_units[1];
-    const int S = I / C::BI;
-    if (static_cast<int>(blockIdx.x) >= n_units) return;
+    tb.na = s_items[0];
+    // units: phase 1 = [0, n1) as item * S + slice, phase 2 = [n1, n1 + n2) as n1 + item * MT + h-tile
+    const int n1 = s_items[1] * S, n_total = n1 + s_items[1] * MT;
+    if (n_total == 0) return;
+    int* const work_head = counters;           // next unit to hand out
+    int* const item_done = counters + 1;       // phase-1 units finished, per item
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
@@ -217,8 +232,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_gate = tmem, t_up = tmem + NT, t_acc2 = tmem + 2 * NT;
-    const int KT = H / C::BK, MT = H / C::BH;
+    const int KT1 = H / C::BK, KT2 = I / (2 * C::BK);
 
     if (warp == 0) {
         // ---------------- TMA producer (lane 0 issues; the warp loads token lists) ----------------
@@ -226,25 +240,66 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
         int stage = 0;
         uint32_t phase = 0, pend = 0, pend_par = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-            int e, s, row0, nrows;
-            unit_info(tb, u, S, NT, e, s, row0, nrows);
-            // rows past the chunk repeat its first token; their columns are never used
-            for (int t = lane; t < NT; t += 32) ptok[t] = row_token[row0 + (t < nrows ? t : 0)];
-            __syncwarp();
+        int cur = (lane == 0) ? atomicAdd(work_head, 1) : 0;
+        cur = __shfl_sync(kFull, cur, 0);
+        for (int j = 0;; ++j) {
+            const bool done = cur >= n_total;
             if (lane == 0) {
-                const int wrow = e * I + s * C::BI;
+                // hand the unit (or the end mark) to the MMA and epilogue warps
+                const int qs = j % C::QN;
+                ok = mbar_wait(bar(B_QEMPTY + qs), ((j / C::QN) & 1) ^ 1, abort_flag, st, kSiteProducerEmpty);
+                if (ok) {
+                    uring[qs] = done ? -1 : cur;
+                    mbar_arrive(bar(B_QFULL + qs));
+                }
+            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (!ok || done) break;
+            // the next unit's id arrives while this unit's copies are issued
+            int nxt = 0;
+            if (lane == 0) nxt = atomicAdd(work_head, 1);
+            const bool p1 = cur < n1;
+            const int v = p1 ? cur : cur - n1;
+            const int item = p1 ? v / S : v / MT;
+            const int sub = p1 ? v - item * S : v - item * MT;   // I-slice or H-tile
+            int e, row0, nrows;
+            item_info(tb, item, NT, e, row0, nrows);
+            if (p1) {
+                // rows past the chunk repeat its first token; their columns are never used
+                for (int t = lane; t < NT; t += 32) ptok[t] = row_token[row0 + (t < nrows ? t : 0)];
+                __syncwarp();
+            }
+            if (lane == 0) {
+                if (!p1) {
+                    // A of this item: all S phase-1 units must have published their slices
+                    const unsigned long long t0 = global_ns();
+                    while (ld_acquire_gpu(item_done + item) < S) {
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        if (global_ns() - t0 > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            report(st, MOE_DEV_TIMEOUT, kSiteDependency);
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    fence_proxy_async_global();
+                }
                 const int n_g4 = (nrows + 3) / 4;
-                for (int kt = 0; kt < KT + MT; ++kt) {
+                const int n16 = (min(NT, max(16, (nrows + 15) & ~15))) / 16;
+                const int nk = p1 ? KT1 : KT2;
+                for (int kt = 0; kt < nk && ok; ++kt) {
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
                     const uint32_t dst = ring_a + stage * C::STAGE;
                     const uint32_t fb = bar(B_FULL + stage);
-                    if (kt < KT) {
-                        // only the gathers that hold real rows; the MMA's N covers them, rows past
-                        // nrows in the last 16-row group belong to columns that are never used
+                    if (p1) {
+                        const int wrow = e * I + sub * C::BI;
                         mbar_arrive_expect_tx(fb, C::W_BYTES + n_g4 * 512);
                         tma_load_2d(dst, &tm_wg, kt * C::BK, wrow, fb, pol_w);
                         tma_load_2d(dst + C::W_BOX, &tm_wu, kt * C::BK, wrow, fb, pol_w);
@@ -252,10 +307,14 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
                             tma_gather4(dst + C::W_BYTES + g * 512, &tm_x, kt * C::BK, ptok[4 * g], ptok[4 * g + 1],
                                         ptok[4 * g + 2], ptok[4 * g + 3], fb, pol_x);
                     } else {
-                        const int m = kt - KT;
-                        mbar_arrive_expect_tx(fb, C::W_BYTES);
-                        tma_load_2d(dst, &tm_wd, s * C::BI, e * H + m * C::BH, fb, pol_w);
-                        tma_load_2d(dst + C::W_BOX, &tm_wd, s * C::BI + 64, e * H + m * C::BH, fb, pol_w);
+                        const int wrow = e * H + sub * C::BH;
+                        mbar_arrive_expect_tx(fb, C::W_BYTES + 2 * n16 * 2048);
+                        tma_load_2d(dst, &tm_wd, kt * 2 * C::BK, wrow, fb, pol_w);
+                        tma_load_2d(dst + C::W_BOX, &tm_wd, kt * 2 * C::BK + C::BK, wrow, fb, pol_w);
+                        for (int a = 0; a < 2; ++a)
+                            for (int g = 0; g < n16; ++g)
+                                tma_load_2d(dst + C::W_BYTES + a * C::X_ATOM + g * 2048, &tm_act,
+                                            kt * 2 * C::BK + a * C::BK, row0 + 16 * g, fb, pol_x);
                     }
                     pend |= 1u << stage;
                     pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -267,6 +326,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
             }
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
+            cur = __shfl_sync(kFull, nxt, 0);
         }
         if (!ok && lane == 0) {
             // let every copy still in flight land before the CTA exits
@@ -277,32 +337,49 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            int stage = 0, j = 0;
-            uint32_t phase = 0, n2 = 0;
+            int stage = 0;
+            uint32_t phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++j) {
-                // the MMA's N is the unit's row count rounded up to 16
-                int ue, us, urow0, unrows;
-                unit_info(tb, u, S, NT, ue, us, urow0, unrows);
-                const int n_eff = min(NT, max(16, (unrows + 15) & ~15));
-                const uint32_t idesc = idesc_bf16_f32(128, n_eff);
-                if (!mbar_wait(bar(B_TMEMFREE), (j & 1) ^ 1, abort_flag, st, kSiteMmaTmemFree)) break;
+            for (int j = 0; ok; ++j) {
+                const int qs = j % C::QN;
+                if (!mbar_wait(bar(B_QFULL + qs), (j / C::QN) & 1, abort_flag, st, kSiteMmaFull)) break;
+                const int un = uring[qs];
+                mbar_arrive(bar(B_QEMPTY + qs));
+                if (un < 0) break;
+                const bool p1 = un < n1;
+                const int v = p1 ? un : un - n1;
+                const int item = p1 ? v / S : v / MT;
+                int e, row0, nrows;
+                item_info(tb, item, NT, e, row0, nrows);
+                // the MMA's N is the item's row count rounded up to 16
+                const uint32_t idesc = idesc_bf16_f32(128, min(NT, max(16, (nrows + 15) & ~15)));
+                const int b = j & 1;
+                const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
+                if (!mbar_wait(bar(B_ACCE + b), ((j >> 1) & 1) ^ 1, abort_flag, st, kSiteMmaTmemFree)) break;
                 tc_fence_after();
-                for (int kt = 0; kt < KT && ok; ++kt) {
+                const int nk = p1 ? KT1 : KT2;
+                for (int kt = 0; kt < nk; ++kt) {
                     if (!mbar_wait(bar(B_FULL + stage), phase, abort_flag, st, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a = ring_a + stage * C::STAGE;
+                    if (p1) {
 #pragma unroll
-                    for (int kk = 0; kk < C::BK / 16; ++kk) {
-                        const uint64_t dg = sw128_desc(a + kk * 32);
-                        const uint64_t du = sw128_desc(a + C::W_BOX + kk * 32);
-                        const uint64_t dx = sw128_desc(a + C::W_BYTES + kk * 32);
-                        const uint32_t acc = (kt | kk) != 0;
-                        tc_mma_bf16(t_gate, dg, dx, idesc, acc);
-                        tc_mma_bf16(t_up, du, dx, idesc, acc);
+                        for (int kk = 0; kk < C::BK / 16; ++kk) {
+                            const uint64_t dx = sw128_desc(a + C::W_BYTES + kk * 32);
+                            const uint32_t acc = (kt | kk) != 0;
+                            tc_mma_bf16(acc0, sw128_desc(a + kk * 32), dx, idesc, acc);
+                            tc_mma_bf16(acc1, sw128_desc(a + C::W_BOX + kk * 32), dx, idesc, acc);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 2 * C::BK / 16; ++kk) {
+                            const uint64_t dw = sw128_desc(a + (kk >> 2) * C::W_BOX + (kk & 3) * 32);
+                            const uint64_t dx = sw128_desc(a + C::W_BYTES + (kk >> 2) * C::X_ATOM + (kk & 3) * 32);
+                            tc_mma_bf16(acc0, dw, dx, idesc, (kt | kk) != 0);
+                        }
                     }
                     tc_commit(bar(B_EMPTY + stage));
                     if (++stage == C::NSTAGE) {
@@ -311,36 +388,7 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                tc_commit(bar(B_G1));
-                if (!mbar_wait(bar(B_ACTRDY), j & 1, abort_flag, st, kSiteMmaActReady)) break;
-                tc_fence_after();
-                for (int m = 0; m < MT; ++m, ++n2) {
-                    if (!mbar_wait(bar(B_FULL + stage), phase, abort_flag, st, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t b = n2 % C::NACC2, use = n2 / C::NACC2;
-                    if (!mbar_wait(bar(B_ACC2E + b), (use & 1u) ^ 1u, abort_flag, st, kSiteMmaAcc2Empty)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a = ring_a + stage * C::STAGE;
-#pragma unroll
-                    for (int kk = 0; kk < C::BI / 16; ++kk) {
-                        const uint64_t dw = sw128_desc(a + (kk >> 2) * C::W_BOX + (kk & 3) * 32);
-                        const uint64_t da = sw128_desc(act_a + (kk >> 2) * (NT * 128) + (kk & 3) * 32);
-                        tc_mma_bf16(t_acc2 + b * NT, dw, da, idesc, kk != 0);
-                    }
-                    tc_commit(bar(B_EMPTY + stage));
-                    tc_commit(bar(B_ACC2F + b));
-                    if (++stage == C::NSTAGE) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                tc_commit(bar(B_ACTFREE));
+                tc_commit(bar(B_ACCF + b));
             }
             // every issued MMA has finished before TMEM is released
             tc_commit(bar(B_DRAIN));
@@ -351,105 +399,101 @@ __global__ void __launch_bounds__(TcCfg<NT>::THREADS, 1)
         // ---------------- epilogue: warps 2..9, two per TMEM lane quadrant ----------------
         const int q = warp & 3;                        // TMEM lane quadrant of this warp
         const int half = (warp - 2) >> 2;              // which half of the token columns
-        const int row = q * 32 + lane;                 // row within the 128-row tile
+        const int row = q * 32 + lane;                 // row of the 128-row tile (I row or H row)
         const int c_lo = half * CW;                    // first token column of this warp
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        const int c = row >> 6, ci = row & 63;
-        int j = 0;
-        uint32_t n2 = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++j) {
-            int e, s, row0, nrows;
-            unit_info(tb, u, S, NT, e, s, row0, nrows);
+        int* etok = etok_all + (warp - 2) * 32;
+        float* egt = egt_all + (warp - 2) * 32;
+        for (int j = 0;; ++j) {
+            const int qs = j % C::QN;
             // every lane polls; the warp proceeds only if all lanes saw the phase complete
-            bool okw = mbar_wait(bar(B_G1), j & 1, abort_flag, st, kSiteEpiG1Done);
-            if (!__all_sync(kFull, okw)) break;
-            okw = mbar_wait(bar(B_ACTFREE), (j & 1) ^ 1, abort_flag, st, kSiteEpiActFree);
-            if (!__all_sync(kFull, okw)) break;
-            tc_fence_after();
-            {
-                // SwiGLU of this thread's I row for its token columns -> bf16 B operand of GEMM2,
-                // eight columns at a time
-                const uint32_t col_base = act_a + c * (NT * 128);
-#pragma unroll
-                for (int c8 = 0; c8 < CW / 8; ++c8) {
-                    uint32_t g[8], v[8];
-                    if (c_lo + c8 * 8 < nrows) {   // warp-uniform
-                        tmem_ld8(t_gate + lane_off + c_lo + c8 * 8, g);
-                        tmem_ld8(t_up + lane_off + c_lo + c8 * 8, v);
-                        tmem_ld_wait();
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int t = c_lo + c8 * 8 + jj;
-                        const float a =
-                            (t < nrows) ? silu_mul(__uint_as_float(g[jj]), __uint_as_float(v[jj])) : 0.f;
-                        const __nv_bfloat16 hb = __float2bfloat16_rn(a);
-                        const uint32_t addr = col_base + t * 128 + ((((ci >> 3) ^ (t & 7)) << 4) | ((ci & 7) << 1));
-                        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
-                                     "h"(*reinterpret_cast<const uint16_t*>(&hb))
-                                     : "memory");
-                    }
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(bar(B_TMEMFREE));
-            fence_proxy_async_smem();
-            mbar_arrive(bar(B_ACTRDY));
-            // token and gate of each of this warp's columns, for the reductions below
-            int* etok = etok_all + (warp - 2) * 32;
-            float* egt = egt_all + (warp - 2) * 32;
-            if (lane < CW) {
-                const int t = c_lo + lane;
-                etok[lane] = (t < nrows) ? row_token[row0 + t] : 0;
-                egt[lane] = (t < nrows) ? row_gate[row0 + t] : 0.f;
-            }
-            __syncwarp();
-            // down-projection tiles: add gate * E_e(x) into y
-            bool ok = true;
-            for (int m = 0; m < H / C::BH; ++m, ++n2) {
-                const uint32_t b = n2 % C::NACC2, use = n2 / C::NACC2;
-                const bool okw2 = mbar_wait(bar(B_ACC2F + b), use & 1u, abort_flag, st, kSiteEpiAcc2Full);
-                if (!__all_sync(kFull, okw2)) {
-                    ok = false;
-                    break;
-                }
+            bool okw = __all_sync(kFull, mbar_wait(bar(B_QFULL + qs), (j / C::QN) & 1, abort_flag, st, kSiteEpiG1Done));
+            const int un = okw ? uring[qs] : -1;
+            if (!named_sync_and(C::EPI_THREADS, okw)) break;
+            if (un < 0) break;   // the same value in every epilogue thread
+            const bool p1 = un < n1;
+            const int v = p1 ? un : un - n1;
+            const int item = p1 ? v / S : v / MT;
+            const int sub = p1 ? v - item * S : v - item * MT;
+            int e, row0, nrows;
+            item_info(tb, item, NT, e, row0, nrows);
+            const int b = j & 1;
+            const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
+            okw = __all_sync(kFull, mbar_wait(bar(B_ACCF + b), (j >> 1) & 1, abort_flag, st, kSiteEpiG1Done));
+            if (okw) {
                 tc_fence_after();
-                // read the accumulator in chunks of up to 16 columns; it is released right
-                // after the last read, before the last chunk's reductions
-                constexpr int CH = CW < 16 ? CW : 16;
-                const int h = m * C::BH + row;
+                if (p1) {
+                    // SwiGLU of this thread's I row for the warp's token columns -> A (bf16, row-major)
+                    __nv_bfloat16* dst = act_g + static_cast<size_t>(row0) * I + sub * C::BI + row;
 #pragma unroll
-                for (int c16 = 0; c16 < CW / CH; ++c16) {
-                    const bool any = c_lo + c16 * CH < nrows;   // warp-uniform
-                    uint32_t v[CH];
-                    if (any) {
-                        if constexpr (CH == 8) {
-                            tmem_ld8(t_acc2 + b * NT + lane_off + c_lo, v);
-                        } else {
-                            tmem_ld16(t_acc2 + b * NT + lane_off + c_lo + c16 * CH, v);
-                        }
+                    for (int c8 = 0; c8 < CW / 8; ++c8) {
+                        if (c_lo + c8 * 8 >= nrows) break;   // warp-uniform
+                        uint32_t g[8], u[8];
+                        tmem_ld8(acc0 + lane_off + c_lo + c8 * 8, g);
+                        tmem_ld8(acc1 + lane_off + c_lo + c8 * 8, u);
                         tmem_ld_wait();
-                    }
-                    if (c16 == CW / CH - 1) {
-                        tc_fence_before();
-                        mbar_arrive(bar(B_ACC2E + b));
-                    }
-                    if (!any) continue;
 #pragma unroll
-                    for (int jj = 0; jj < CH; ++jj) {
-                        const int t = c_lo + c16 * CH + jj;
-                        const int js = c16 * CH + jj;   // index into this warp's token slice
-                        if (t < nrows) {
-                            if (fuse_combine)
-                                atomicAdd(out + static_cast<size_t>(etok[js]) * H + h, egt[js] * __uint_as_float(v[jj]));
-                            else
-                                atomicAdd(out + static_cast<size_t>(row0 + t) * H + h, __uint_as_float(v[jj]));
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int t = c_lo + c8 * 8 + jj;
+                            if (t < nrows)
+                                dst[static_cast<size_t>(t) * I] =
+                                    __float2bfloat16_rn(silu_mul(__uint_as_float(g[jj]), __uint_as_float(u[jj])));
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(bar(B_ACCE + b));
+                    // make the stores visible to the phase-2 TMA loads of other CTAs
+                    fence_proxy_async_global();
+                    __threadfence();
+                } else {
+                    if (lane < CW) {
+                        const int t = c_lo + lane;
+                        etok[lane] = (t < nrows) ? row_token[row0 + t] : 0;
+                        egt[lane] = (t < nrows) ? row_gate[row0 + t] : 0.f;
+                    }
+                    __syncwarp();
+                    // read the accumulator in chunks of up to 16 columns; it is released right
+                    // after the last read, before the last chunk's reductions
+                    constexpr int CH = CW < 16 ? CW : 16;
+                    const int h = sub * C::BH + row;
+#pragma unroll
+                    for (int c16 = 0; c16 < CW / CH; ++c16) {
+                        const bool any = c_lo + c16 * CH < nrows;   // warp-uniform
+                        uint32_t vv[CH];
+                        if (any) {
+                            if constexpr (CH == 8) {
+                                tmem_ld8(acc0 + lane_off + c_lo, vv);
+                            } else {
+                                tmem_ld16(acc0 + lane_off + c_lo + c16 * CH, vv);
+                            }
+                            tmem_ld_wait();
+                        }
+                        if (c16 == CW / CH - 1) {
+                            tc_fence_before();
+                            mbar_arrive(bar(B_ACCE + b));
+                        }
+                        if (!any) continue;
+#pragma unroll
+                        for (int jj = 0; jj < CH; ++jj) {
+                            const int t = c_lo + c16 * CH + jj;
+                            const int js = c16 * CH + jj;
+                            if (t < nrows) {
+                                if (fuse_combine)
+                                    atomicAdd(out + static_cast<size_t>(etok[js]) * H + h,
+                                              egt[js] * __uint_as_float(vv[jj]));
+                                else
+                                    atomicAdd(out + static_cast<size_t>(row0 + t) * H + h, __uint_as_float(vv[jj]));
+                            }
                         }
                     }
                 }
             }
-            __syncwarp();   // the warp's token slice is rewritten for the next unit
-            if (!ok) break;
+            // all epilogue warps pass here once per unit; a failure anywhere ends them together
+            if (!named_sync_and(C::EPI_THREADS, okw)) break;
+            if (threadIdx.x == 64) {
+                if (p1) red_release_gpu_add(item_done + item, 1);
+                mbar_arrive(bar(B_QEMPTY + qs));   // every epilogue thread has read the unit id
+            }
         }
     }
     __syncthreads();
@@ -504,29 +548,35 @@ static int sm_count() {
     return cached[dev];
 }
 
-__global__ void zero_kernel(float* p, long long n);
+__global__ void zero_kernel(float* p, long long n, int* c, int nc);
 
-static cudaError_t launch_zero(float* p, long long n, cudaStream_t s) {
+// Clears p[0, n) (fp32) and c[0, nc) (int32) in one launch.
+static cudaError_t launch_zero(float* p, long long n, cudaStream_t s, int* c = nullptr, int nc = 0) {
     int grid = static_cast<int>((n / 4 + 255) / 256);
     grid = grid < 1 ? 1 : (grid > 1024 ? 1024 : grid);
-    return launch_pdl(zero_kernel, dim3(grid), dim3(256), 0, s, p, n);
+    return launch_pdl(zero_kernel, dim3(grid), dim3(256), 0, s, p, n, c, nc);
 }
 
 template <int NT>
-static cudaError_t run_tc(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I, int N,
-                          int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
-                          const int32_t* active, uint32_t flags, float* out, moe_dev_status* st, cudaStream_t s) {
-    using C = TcCfg<NT>;
+static cudaError_t run_stream(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
+                              int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
+                              const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
+                              cudaStream_t s) {
+    using C = StCfg<NT>;
     const bool fuse = (flags & MOE_FFN_FUSE_COMBINE) != 0;
-    if (fuse && (flags & MOE_FFN_ZERO_Y)) {
-        cudaError_t e = launch_zero(out, static_cast<long long>(T) * H, s);
-        if (e != cudaSuccess) return e;
-    }
-    CUtensorMap tm_wg, tm_wu, tm_wd, tm_x;
+    const long long M = static_cast<long long>(T) * k;
+    const long long items = ffn_max_items(T, N, k, NT);
+    int* counters = static_cast<int*>(ws);
+    __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + align256((items + 1) * 4));
+    cudaError_t e = launch_zero(out, (fuse && (flags & MOE_FFN_ZERO_Y)) ? static_cast<long long>(T) * H : 0, s,
+                                counters, static_cast<int>(items + 1));
+    if (e != cudaSuccess) return e;
+    CUtensorMap tm_wg, tm_wu, tm_wd, tm_x, tm_act;
     if (!make_tmap(&tm_wg, wg, H, static_cast<uint64_t>(N) * I, 64, 128) ||
         !make_tmap(&tm_wu, wu, H, static_cast<uint64_t>(N) * I, 64, 128) ||
         !make_tmap(&tm_wd, wd, I, static_cast<uint64_t>(N) * H, 64, 128) ||
-        !make_tmap(&tm_x, x, H, static_cast<uint64_t>(T), 64, 1))
+        !make_tmap(&tm_x, x, H, static_cast<uint64_t>(T), 64, 1) ||
+        !make_tmap(&tm_act, act, I, static_cast<uint64_t>(M), 64, 16))
         return cudaErrorInvalidValue;
     // the attribute is set once per device, on the first (uncaptured) call
     static bool attr_set[64] = {};
@@ -534,27 +584,33 @@ static cudaError_t run_tc(const void* x, const void* wg, const void* wu, const v
     cudaGetDevice(&devi);
     if (devi < 0 || devi >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[devi]) {
-        cudaError_t ae = cudaFuncSetAttribute(ffn_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t ae =
+            cudaFuncSetAttribute(ffn_stream_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (ae != cudaSuccess) return ae;
         attr_set[devi] = true;
     }
-    const int Mmax = T * k;
-    const long long max_items = (N < Mmax ? N : Mmax) + (Mmax + NT - 1) / NT;
-    const long long max_units = max_items * (I / C::BI);
+    const long long max_units = items * (I / C::BI + H / C::BH);
     int grid = sm_count();
     if (max_units < grid) grid = static_cast<int>(max_units > 0 ? max_units : 1);
-    return launch_pdl(ffn_tc_kernel<NT>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wd, tm_x, offsets,
-                      active, row_token, row_gate, out, H, I, N, fuse ? 1 : 0, st);
+    return launch_pdl(ffn_stream_kernel<NT>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wd, tm_x,
+                      tm_act, offsets, active, row_token, row_gate, act, counters, out, H, I, N, fuse ? 1 : 0, st);
 }
 
 cudaError_t launch_ffn_bf16(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
                             int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                             const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
                             cudaStream_t s) {
-    (void)ws;
-    if (T <= 16) return run_tc<16>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, st, s);
-    if (T <= 32) return run_tc<32>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, st, s);
-    return run_tc<64>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, st, s);
+    switch (ffn_nt(T)) {
+        case 16:
+            return run_stream<16>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws,
+                                  st, s);
+        case 32:
+            return run_stream<32>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws,
+                                  st, s);
+        default:
+            return run_stream<64>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws,
+                                  st, s);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -604,9 +660,10 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float* __restrict__ 
     }
 }
 
-__global__ void zero_kernel(float* p, long long n) {
+__global__ void zero_kernel(float* p, long long n, int* c, int nc) {
     pdl_wait();
     pdl_trigger();
+    for (int i = blockIdx.x * 256 + threadIdx.x; i < nc; i += 256 * gridDim.x) c[i] = 0;
     const long long n4 = n / 4;
     float4* p4 = reinterpret_cast<float4*>(p);
     for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n4; i += 256ll * gridDim.x)

@@ -224,7 +224,12 @@ moe_status_t moe_dispatch_capacity_static(const int32_t* ids, const float* gates
  *   offsets [N+1], row_token [T*k], row_gate [T*k], active [N+1]  from dispatch
  *   out     FUSE_COMBINE: y [T][H] fp32 (accumulated into); otherwise
  *           rows_out [T*k][H] fp32, row r = E_e(x_token(r)) without the gate
- *   workspace  device scratch of moe_workspace_size(MOE_OP_FFN, ...) bytes
+ *   workspace  device scratch of moe_workspace_size(MOE_OP_FFN, ...) bytes,
+ *           256-byte aligned.  BF16 needs it: a work counter, one counter
+ *           per (expert, token chunk) and the bf16 SwiGLU activations of
+ *           every row (T*k*I*2 bytes plus a few KiB); F32 needs none.  Each
+ *           call clears what must start at zero.  Two calls in flight at
+ *           once must not share a workspace.
  * BF16 runs on the tensor cores (tcgen05, TMA-fed) with fp32 accumulation;
  * the SwiGLU activation is rounded to bf16 before the down projection.
  * F32 runs a CUDA-core kernel in fp32.
