@@ -179,11 +179,9 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def run_ours(args):
+def _gpu_setup():
     import torch
     import expert_routing_moe_gb300 as moe
-    from expert_routing_moe_gb300 import synthetic as syn
-
     ws, rank, local = dist_env()
     if ws > 1:
         import torch.distributed as dist
@@ -194,17 +192,120 @@ def run_ours(args):
     from expert_routing_moe_gb300 import build as b
     b.build()
     moe.load()
+    return torch, moe, dev, ws, rank, local
 
-    # ---- inputs: one host-generated copy of the layer + device-generated copies ----
+
+def _device_copies(torch, dev, L, n_copies, seed):
+    """Expert weights: the host layer's own copy plus n_copies-1 device-drawn
+    N(0, 0.02) bf16 copies of the same shapes (to rotate past the L2)."""
+    Nn, Ii, Hh = L.N, L.I, L.H
+    copies = [tuple(torch.from_numpy(a).view(torch.bfloat16).to(dev) for a in (L.w_gate, L.w_up, L.w_down))]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    for _ in range(1, n_copies):
+        copies.append(tuple((torch.randn(shape, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+                            for shape in ((Nn, Ii, Hh), (Nn, Ii, Hh), (Nn, Hh, Ii))))
+    return copies
+
+
+def _capture(torch, stream, layers, xs, sere, token_w=None):
+    """Per (batch, weight copy): a routing+dispatch graph and an FFN graph."""
+    graphs = []
+    with torch.cuda.stream(stream):
+        for bidx, x in enumerate(xs):
+            lay = layers[bidx % len(layers)]
+            T = x.shape[0]
+            for _ in range(2):  # eager warm-up on the capture stream
+                lay.forward(x, sere=sere, token_w=token_w)
+            stream.synchronize()
+            g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=stream):
+                lay.route(x, sere)
+                lay.dispatch(T, token_w)
+            with torch.cuda.graph(g2, stream=stream):
+                lay.ffn(x)
+            graphs.append((g1, g2))
+    torch.cuda.synchronize()
+    return graphs
+
+
+def _active_counts(torch, moe, stream, layers, xs, sere, token_w=None):
+    us, rows = [], []
+    for bidx, x in enumerate(xs):
+        lay = layers[bidx % len(layers)]
+        with torch.cuda.stream(stream):
+            lay.forward(x, sere=sere, token_w=token_w)
+        stream.synchronize()
+        code, detail = lay.device_status()
+        if code != 0:
+            raise RuntimeError("device status %d (%s) detail %d" % (code, moe.status_string(code, True), detail))
+        us.append(int(lay.active[0].item()))
+        rows.append(int(lay.offsets[lay.N].item()))
+    return us, rows
+
+
+def _timed(torch, stream, graphs, steps, warmup, ws):
+    """Replays `steps` steps (both graphs of one batch each); CUDA events on
+    the replay stream around the whole run and around every FFN graph."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    nb = len(graphs)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            g1, g2 = graphs[i % nb]
+            g1.replay()
+            g2.replay()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    f0 = [ev() for _ in range(steps)]
+    f1 = [ev() for _ in range(steps)]
+    e0, e1 = ev(), ev()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            g1, g2 = graphs[i % nb]
+            g1.replay()
+            f0[i].record(stream)
+            g2.replay()
+            f1[i].record(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    return e0.elapsed_time(e1), [a.elapsed_time(b) for a, b in zip(f0, f1)]
+
+
+def _max_over_ranks(torch, dev, ws, v):
+    if ws == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _soak(torch, stream, graphs, seconds):
+    """Untimed replays so that the clock record covers a loaded GPU."""
+    t_end = time.perf_counter() + seconds
+    with torch.cuda.stream(stream):
+        i = 0
+        while time.perf_counter() < t_end:
+            for _ in range(50):
+                g1, g2 = graphs[i % len(graphs)]
+                g1.replay()
+                g2.replay()
+                i += 1
+            stream.synchronize()
+
+
+def run_ours(args):
+    torch, moe, dev, ws, rank, local = _gpu_setup()
+    from expert_routing_moe_gb300 import synthetic as syn
+
     L = syn.decode(T)
     w_r = torch.from_numpy(L.w_r).to(dev)
     sim = torch.from_numpy(L.sim).to(dev)
-    copies = [tuple(torch.from_numpy(a).view(torch.bfloat16).to(dev) for a in (L.w_gate, L.w_up, L.w_down))]
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1000 * syn.CONFIG_DECODE + 10 * (rank + 1))
-    for c in range(1, N_COPIES):
-        copies.append(tuple((torch.randn(shape, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
-                            for shape in ((N, I, H), (N, I, H), (N, H, I))))
+    copies = _device_copies(torch, dev, L, N_COPIES, 1000 * syn.CONFIG_DECODE + 10 * (rank + 1))
     xs = []
     for bidx in range(N_BATCHES):
         Lb = syn.decode(T, with_weights=False, token_stream_offset=bidx + 97 * rank)
@@ -213,103 +314,24 @@ def run_ours(args):
               for c in range(N_COPIES)]
     stream = torch.cuda.Stream(device=dev)
 
-    # ---- capture each (batch, copy) step as two graphs: routing+dispatch, FFN ----
-    def capture(sere):
-        graphs = []
-        with torch.cuda.stream(stream):
-            for bidx in range(N_BATCHES):
-                lay = layers[bidx % N_COPIES]
-                x = xs[bidx]
-                for _ in range(2):  # eager warm-up on the capture stream
-                    lay.forward(x, sere=sere)
-                stream.synchronize()
-                g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g1, stream=stream):
-                    lay.route(x, sere)
-                    lay.dispatch(T)
-                with torch.cuda.graph(g2, stream=stream):
-                    lay.ffn(x)
-                graphs.append((g1, g2))
-        torch.cuda.synchronize()
-        return graphs
-
-    def active_counts(sere):
-        us = []
-        for bidx in range(N_BATCHES):
-            lay = layers[bidx % N_COPIES]
-            with torch.cuda.stream(stream):
-                lay.forward(xs[bidx], sere=sere)
-            stream.synchronize()
-            code, detail = lay.device_status()
-            if code != 0:
-                raise RuntimeError("device status %d (%s) detail %d" % (code, moe.status_string(code, True),
-                                                                          detail))
-            us.append(int(lay.active[0].item()))
-        return us
-
-    def timed(graphs, us, steps, warmup):
-        ev = lambda: torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            for i in range(warmup):
-                g1, g2 = graphs[i % N_BATCHES]
-                g1.replay()
-                g2.replay()
-        torch.cuda.synchronize()
-        if ws > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        f0 = [ev() for _ in range(steps)]
-        f1 = [ev() for _ in range(steps)]
-        e0, e1 = ev(), ev()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for i in range(steps):
-                g1, g2 = graphs[i % N_BATCHES]
-                g1.replay()
-                f0[i].record(stream)
-                g2.replay()
-                f1[i].record(stream)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        if ws > 1:
-            torch.distributed.barrier()
-        total_ms = e0.elapsed_time(e1)
-        ffn_ms = [a.elapsed_time(b) for a, b in zip(f0, f1)]
-        ffn_bytes = [us[i % N_BATCHES] * EXPERT_BYTES + T * H * 2 + T * H * 4 for i in range(steps)]
-        return total_ms, ffn_ms, ffn_bytes
-
-    def max_over_ranks(v):
-        if ws == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
-    us_sere = active_counts(True)
-    us_top8 = active_counts(False)
-    g_sere = capture(True)
-    g_top8 = capture(False)
-    launches_per_step = 4  # router, rank+SERE, permute, FFN tensor-core kernel (plus a memset node for y)
+    us_sere, _ = _active_counts(torch, moe, stream, layers, xs, True)
+    us_top8, _ = _active_counts(torch, moe, stream, layers, xs, False)
+    g_sere = _capture(torch, stream, layers, xs, True)
+    g_top8 = _capture(torch, stream, layers, xs, False)
+    # router, rank+SERE, permute, FFN zero/counter clear, FFN tensor-core kernel
+    launches_per_step = 5
 
     clk = ClockSampler(local if ws > 1 else 0)
     clk.start()
     if args.clock_soak > 0:
-        # untimed replays so that the clock record covers a loaded GPU, not just a few ms
-        t_end = time.perf_counter() + args.clock_soak
-        with torch.cuda.stream(stream):
-            i = 0
-            while time.perf_counter() < t_end:
-                for _ in range(50):
-                    g1, g2 = g_sere[i % N_BATCHES]
-                    g1.replay()
-                    g2.replay()
-                    i += 1
-                stream.synchronize()
-    total_ms, ffn_ms, ffn_bytes = timed(g_sere, us_sere, args.steps, args.warmup)
+        _soak(torch, stream, g_sere, args.clock_soak)
+    total_ms, ffn_ms = _timed(torch, stream, g_sere, args.steps, args.warmup, ws)
     clocks = clk.stop()
-    total_ms = max_over_ranks(total_ms)
-    t8_ms, t8_ffn_ms, t8_bytes = timed(g_top8, us_top8, args.steps, args.warmup)
-    t8_ms = max_over_ranks(t8_ms)
+    total_ms = _max_over_ranks(torch, dev, ws, total_ms)
+    ffn_bytes = [us_sere[i % N_BATCHES] * EXPERT_BYTES + T * H * 2 + T * H * 4 for i in range(args.steps)]
+    t8_ms, t8_ffn_ms = _timed(torch, stream, g_top8, args.steps, args.warmup, ws)
+    t8_ms = _max_over_ranks(torch, dev, ws, t8_ms)
+    t8_bytes = [us_top8[i % N_BATCHES] * EXPERT_BYTES + T * H * 2 + T * H * 4 for i in range(args.steps)]
 
     # ---- end to end through the public API: pinned host x in, host y out, every step ----
     xs_host = [x.cpu().pin_memory() for x in xs]
@@ -335,15 +357,14 @@ def run_ours(args):
             y_host.copy_(y, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e_ms = _max_over_ranks(torch, dev, ws, e0.elapsed_time(e1))
     for lay in layers:
         code, detail = lay.device_status()
         if code != 0:
             raise RuntimeError("device status %d detail %d after the timed runs" % (code, detail))
 
     peak, peak_src = load_peaks()
-    ffn_s = sum(ffn_ms) / 1e3
-    achieved = sum(ffn_bytes) / ffn_s / 1e9
+    achieved = sum(ffn_bytes) / (sum(ffn_ms) / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": ws * T * args.steps / (total_ms / 1e3), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -352,7 +373,7 @@ def run_ours(args):
         "config": workload_config({"parallelism": "replicas" if ws > 1 else "single GPU",
                                    "cuda_graphs": "per step: routing+dispatch graph, FFN graph"}),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "moe_ffn_grouped (y clear + tcgen05 FFN kernel)",
+                     "traffic": args.traffic, "kernel": "moe_ffn_grouped (counter clear + tcgen05 FFN kernel)",
                      "peak_source": peak_src,
                      "bytes_per_launch_mean": float(np.mean(ffn_bytes)),
                      "ms_per_launch_mean": float(np.mean(ffn_ms))},
@@ -380,6 +401,165 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# Further workloads (not the headline line): batch sweep, prefill, 48-layer stack
+# ---------------------------------------------------------------------------
+def run_sweep(args):
+    """Decode batch sweep with 16 protected experts: top-8 and SERE K'=1, 2 at
+    rho = 0.5, batch in {1, 8, 32, 64, 128}; per-layer time, union, FFN GB/s."""
+    torch, moe, dev, ws, rank, local = _gpu_setup()
+    from expert_routing_moe_gb300 import synthetic as syn
+    peak, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    rows = []
+    L0 = syn.sweep(32)
+    copies = _device_copies(torch, dev, L0, N_COPIES, 1000 * syn.CONFIG_SWEEP + 10 * (rank + 1))
+    clk = ClockSampler(local if ws > 1 else 0)
+    clk.start()
+    for B in (1, 8, 32, 64, 128):
+        Lb0 = syn.sweep(B, with_weights=False)
+        w_r = torch.from_numpy(Lb0.w_r).to(dev)
+        sim = torch.from_numpy(Lb0.sim).to(dev)
+        prot = torch.from_numpy(Lb0.protect).to(dev)
+        xs = [torch.from_numpy(syn.sweep(B, with_weights=False, token_stream_offset=b).x_bf16)
+              .view(torch.bfloat16).to(dev) for b in range(N_BATCHES)]
+        for mode, kp in (("top8", 0), ("sere_k1", 1), ("sere_k2", 2)):
+            layers = [moe.MoELayer(w_r, *copies[c], k=K_TOP, max_tokens=B, sim=sim, protect=prot,
+                                   k_primary=max(kp, 1), rho=RHO) for c in range(N_COPIES)]
+            sere = kp > 0
+            us, _ = _active_counts(torch, moe, stream, layers, xs, sere)
+            graphs = _capture(torch, stream, layers, xs, sere)
+            tot, ffn = _timed(torch, stream, graphs, args.steps, args.warmup, ws)
+            byt = [us[i % N_BATCHES] * EXPERT_BYTES + B * H * 6 for i in range(args.steps)]
+            gbs = sum(byt) / (sum(ffn) / 1e3) / 1e9
+            rows.append({"batch": B, "mode": mode, "active_experts_mean": float(np.mean(us)),
+                         "ms_per_layer": tot / args.steps, "tokens_per_s": B * args.steps / (tot / 1e3),
+                         "ffn_us_mean": float(np.mean(ffn)) * 1e3, "ffn_gbs": gbs, "ffn_frac": gbs / peak})
+            del graphs, layers
+    clocks = clk.stop()
+    if rank == 0:
+        print(json.dumps({"workload": "decode batch sweep, 16 protected experts per layer, rho=0.5",
+                          "metric": "MoE-layer decode tokens/s and FFN HBM GB/s", "peak_gbs": peak,
+                          "peak_source": peak_src, "steps": args.steps, "warmup": args.warmup,
+                          "l2": "%d weight copies and %d token batches rotated" % (N_COPIES, N_BATCHES),
+                          "rows": rows, "clocks": clocks}), flush=True)
+    return 0
+
+
+def run_prefill(args):
+    """Capacity-mode prefill layer: T=8192 (70% visual tokens with w~Beta(2,5)),
+    R=10, gamma=1.25.  Tensor-bound: FFN TFLOP/s = 2*3*H*I*rows / FFN time."""
+    torch, moe, dev, ws, rank, local = _gpu_setup()
+    from expert_routing_moe_gb300 import synthetic as syn
+    L = syn.prefill()
+    t = lambda a, dt=None: (torch.from_numpy(a).view(dt) if dt else torch.from_numpy(a)).to(dev)
+    lay = moe.MoELayer(t(L.w_r), t(L.w_gate, torch.bfloat16), t(L.w_up, torch.bfloat16),
+                       t(L.w_down, torch.bfloat16), k=L.k, max_tokens=L.T, R=L.R, capacity_factor=L.gamma)
+    x = t(L.x_bf16, torch.bfloat16)
+    tw = t(L.token_w)
+    stream = torch.cuda.Stream(device=dev)
+    us, rows = _active_counts(torch, moe, stream, [lay], [x], False, token_w=tw)
+    graphs = _capture(torch, stream, [lay], [x], False, token_w=tw)
+    clk = ClockSampler(local if ws > 1 else 0)
+    clk.start()
+    steps = max(3, args.steps // 20)
+    tot, ffn = _timed(torch, stream, graphs, steps, args.warmup, ws)
+    clocks = clk.stop()
+    tf = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"] \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+    flops = 2.0 * 3 * H * I * rows[0]
+    ffn_s = float(np.mean(ffn)) / 1e3
+    if rank == 0:
+        print(json.dumps({"workload": "capacity-mode prefill layer: 8192 tokens (70%% visual, w~Beta(2,5)), "
+                                      "hidden 2048, 128 experts, top-8, R=10, gamma=1.25, intermediate 768",
+                          "metric": "prefill layer tokens/s and FFN tensor TFLOP/s",
+                          "tokens_per_s": L.T * steps / (tot / 1e3), "ms_per_layer": tot / steps,
+                          "ffn_ms": ffn_s * 1e3, "rows_admitted": rows[0], "active_experts": us[0],
+                          "ffn_tflops": flops / ffn_s / 1e12, "peak_tflops": tf,
+                          "ffn_frac": flops / ffn_s / 1e12 / tf, "steps": steps, "clocks": clocks}), flush=True)
+    return 0
+
+
+def run_stack(args):
+    """48 decode layers (batch 64), each with its own ~1.2 GB of experts, router,
+    similarity and protection; x_{l+1} = x_l + y_l.  One CUDA graph per step,
+    SERE K'=2 vs top-8."""
+    torch, moe, dev, ws, rank, local = _gpu_setup()
+    from expert_routing_moe_gb300 import synthetic as syn
+    nl, B = args.layers, syn.STACK_BATCH
+    x0f, x0b = syn.stack_tokens(B, H)
+    x0_f32 = torch.from_numpy(x0f).to(dev)
+    x0_bf16 = torch.from_numpy(x0b).view(torch.bfloat16).to(dev)
+    layers = []
+    for l in range(nl):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(syn.stack_weight_seed(l))
+        w = [(torch.randn(shape, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+             for shape in ((N, I, H), (N, I, H), (N, H, I))]
+        layers.append(moe.MoELayer(torch.from_numpy(syn.stack_router(x0f, l)).to(dev), *w, k=K_TOP, max_tokens=B,
+                                   sim=torch.from_numpy(syn.stack_sim(l)).to(dev),
+                                   protect=torch.from_numpy(syn.stack_protect(l)).to(dev), k_primary=K_PRIMARY,
+                                   rho=RHO))
+    xres = torch.empty(B, H, dtype=torch.float32, device=dev)
+    xb = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(sere):
+        xres.copy_(x0_f32)
+        xb.copy_(x0_bf16)
+        for lay in layers:
+            lay.route(xb, sere)
+            lay.dispatch(B)
+            lay.ffn(xb, accumulate_into=xres)
+            xb.copy_(xres)
+
+    res = {}
+    for mode, sere in (("top8", False), ("sere_k2", True)):
+        with torch.cuda.stream(stream):
+            step(sere)
+        stream.synchronize()
+        us = [int(l.active[0].item()) for l in layers]
+        for l in layers:
+            code, detail = l.device_status()
+            if code != 0:
+                raise RuntimeError("device status %d detail %d" % (code, detail))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            step(sere)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                step(sere)
+            for _ in range(args.warmup):
+                g.replay()
+        torch.cuda.synchronize()
+        clk = ClockSampler(local if ws > 1 else 0)
+        clk.start()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        steps = max(3, args.steps // 50)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        clocks = clk.stop()
+        ms = e0.elapsed_time(e1) / steps
+        byt = sum(us) * EXPERT_BYTES
+        res[mode] = {"ms_per_step": ms, "tokens_per_s": B / (ms / 1e3), "active_experts_per_layer": us,
+                     "active_experts_mean": float(np.mean(us)), "expert_gbs": byt / (ms / 1e3) / 1e9,
+                     "steps": steps, "clocks": clocks}
+        del g
+    peak, peak_src = load_peaks()
+    if rank == 0:
+        print(json.dumps({"workload": "decode step over %d MoE layers, batch %d, hidden 2048, 128 experts, top-8, "
+                                      "intermediate 768, %.1f GB of bf16 experts resident; SERE K'=2, rho=0.5, "
+                                      "per-layer similarity and 16 protected experts" % (nl, B, nl * N * EXPERT_BYTES / 1e9),
+                          "metric": "decode step tokens/s (one CUDA graph per step)", "peak_gbs": peak,
+                          "peak_source": peak_src, "residual": "x_{l+1} = x_l + y_l in fp32, cast to bf16 per layer",
+                          **res}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -390,6 +570,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=4, help="expert-weight copies rotated per step")
     ap.add_argument("--clock-soak", type=float, default=1.5, help="seconds of untimed load while sampling clocks")
+    ap.add_argument("--workload", choices=["decode", "sweep", "prefill", "stack"], default="decode",
+                    help="decode (the headline line) or one of the further workloads")
+    ap.add_argument("--layers", type=int, default=48, help="layers of the stack workload")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per FFN launch from an ncu capture of the same kernel build, if known")
     args = ap.parse_args()
     global N_COPIES
     N_COPIES = max(1, args.copies)
@@ -397,6 +582,12 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "sweep":
+        return run_sweep(args)
+    if args.workload == "prefill":
+        return run_prefill(args)
+    if args.workload == "stack":
+        return run_stack(args)
     return run_ours(args)
 
 

@@ -70,11 +70,14 @@ class MoELayer:
                                   self.load_q if self.capacity_factor > 0 else None,
                                   self.cap_q if self.capacity_factor > 0 else None, self.status, stream)
 
-    def ffn(self, x: torch.Tensor, stream=None):
+    def ffn(self, x: torch.Tensor, stream=None, accumulate_into: Optional[torch.Tensor] = None):
+        """y = sum_j G_j E_j(x) into the layer's buffer, or added to
+        `accumulate_into` ([T][H] fp32, e.g. a residual stream)."""
         T = x.shape[0]
+        out = self.y[:T] if accumulate_into is None else accumulate_into
+        flags = abi.MOE_FFN_FUSE_COMBINE | (abi.MOE_FFN_ZERO_Y if accumulate_into is None else 0)
         abi.moe_ffn_grouped(x, self.w_gate, self.w_up, self.w_down, self.k, self.offsets, self.row_token,
-                            self.row_gate, self.active, self.y[:T], self.ws_ffn,
-                            abi.MOE_FFN_FUSE_COMBINE | abi.MOE_FFN_ZERO_Y, self.status, stream)
+                            self.row_gate, self.active, out, self.ws_ffn, flags, self.status, stream)
 
     def forward(self, x: torch.Tensor, sere: bool = False, token_w: Optional[torch.Tensor] = None, stream=None):
         """y[T][H] fp32 (a view of the layer's output buffer)."""

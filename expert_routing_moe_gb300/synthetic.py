@@ -231,3 +231,40 @@ def sweep(T: int, layer: int = 0, **kw) -> Layer:
 def prefill(T: int = 8192, layer: int = 0, **kw) -> Layer:
     """Capacity-mode prefill layer: 70% visual (w ~ Beta(2,5)), 30% text (w = 1)."""
     return qwen_layer(T, config=CONFIG_PREFILL, layer=layer, capacity=True, **kw)
+
+
+# ---------------------------------------------------------------------------
+# 48-layer decode stack: x_{l+1} = x_l + y_l over layers with their own weights.
+# ---------------------------------------------------------------------------
+STACK_LAYERS, STACK_BATCH, STACK_PROTECT = 48, 64, 16
+
+
+def stack_tokens(T: int = STACK_BATCH, H: int = 2048, token_stream_offset: int = 0):
+    """x_0 [T][H] ~ N(0,1), rounded to bf16: (fp32 values, bf16 bits)."""
+    rt = np.random.default_rng(seed_for(CONFIG_STACK, 0, STREAM_TOKENS) + 7919 * token_stream_offset)
+    bits = f32_to_bf16_bits(rt.standard_normal((T, H), dtype=np.float32))
+    return bf16_bits_to_f32(bits), bits
+
+
+def stack_router(x0: np.ndarray, layer: int, N: int = 128) -> np.ndarray:
+    """Router of stack layer `layer` [N][H] fp32: the minimum-norm W_r with
+    x_0 W_r^T equal to that layer's Dirichlet-skewed logits, so every layer
+    keeps its own expert popularity while the residual stream stays close to
+    x_0 (the layers' outputs are small next to it)."""
+    logits = skewed_logits(rng_for(CONFIG_STACK, layer, STREAM_ROUTER), x0.shape[0], N)
+    w = np.linalg.pinv(x0.astype(np.float64)) @ logits      # [H][N]
+    return np.ascontiguousarray(w.T).astype(np.float32)
+
+
+def stack_sim(layer: int, N: int = 128) -> np.ndarray:
+    return clustered_sim(rng_for(CONFIG_STACK, layer, STREAM_SIM), N)
+
+
+def stack_protect(layer: int, N: int = 128) -> np.ndarray:
+    return protect_bits(rng_for(CONFIG_STACK, layer, STREAM_PROTECT), N, STACK_PROTECT)
+
+
+def stack_weight_seed(layer: int) -> int:
+    """Seed of the torch generator that draws a stack layer's expert weights
+    (N(0, 0.02), fp32 then bf16) on the device, in the order gate, up, down."""
+    return seed_for(CONFIG_STACK, layer, STREAM_WEIGHTS)
