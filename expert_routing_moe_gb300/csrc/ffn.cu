@@ -22,7 +22,15 @@
 namespace moe {
 
 
-// Token-chunk width of the bf16 kernels for a batch of T tokens.
+// Batches of at least this many tokens run the token-major kernels (about 64
+// rows per expert at top-8 of 128); smaller ones the weight-major one.
+constexpr int kTokenMajorMinT = 1024;
+constexpr int kTmRows = 128;   // token rows per item of the token-major kernel (its MMA M)
+constexpr int kTmCols = 256;   // its MMA N (H-tile of the down projection)
+
+static bool token_major(int T, int H) { return T >= kTokenMajorMinT && H % kTmCols == 0; }
+
+// Token-chunk width of the weight-major kernel for a batch of T tokens.
 static int ffn_nt(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
 
 // Upper bound on the items (expert, chunk of <= nt rows) of a dispatch of M rows.
@@ -33,12 +41,34 @@ static long long ffn_max_items(int T, int N, int k, int nt) {
 
 static size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
-// bf16 workspace: the work counter and the per-item phase-1 completion
-// counters (int32), then the SwiGLU activations A [T*k][I] bf16 (row =
-// dispatch row).
+// Token-major workspace (byte offsets): the work counter and per-item
+// counters followed by the per-token row counts (one zeroed range), the
+// token -> rows map [T][k], A [T*k][I] bf16, the rows' activations in expert
+// order X_rows [T*k][H] bf16 and the rows' outputs [T*k][H] fp32.
+struct TmLayout {
+    long long items, n_zero;
+    size_t tok_cnt, tok_rows, act, xp, rows, total;
+};
+
+static TmLayout tm_layout(int T, int H, int I, int N, int k) {
+    TmLayout L;
+    const size_t M = static_cast<size_t>(T) * k;
+    L.items = ffn_max_items(T, N, k, kTmRows);
+    L.n_zero = L.items + 1 + T;
+    L.tok_cnt = static_cast<size_t>(L.items + 1) * 4;
+    L.tok_rows = align256(static_cast<size_t>(L.n_zero) * 4);
+    L.act = L.tok_rows + align256(M * 4);
+    L.xp = L.act + align256(M * I * 2);
+    L.rows = L.xp + align256(M * H * 2);
+    L.total = L.rows + M * H * 4;
+    return L;
+}
+
+// bf16 workspace.  Weight-major: the work counter and per-item counters
+// (int32), then A [T*k][I] bf16 (row = dispatch row).  Token-major: tm_layout.
 size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype) {
-    (void)H;
     if (dtype != MOE_DTYPE_BF16 || T <= 0) return 0;
+    if (token_major(T, H)) return tm_layout(T, H, I, N, k).total;
     const long long items = ffn_max_items(T, N, k, ffn_nt(T));
     return align256(static_cast<size_t>(items + 1) * 4) + static_cast<size_t>(T) * k * I * 2;
 }
@@ -504,6 +534,448 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Token-major kernel for large batches (prefill).
+//
+// With hundreds of rows per expert the FFN is a dense contraction, so the
+// 128-row MMA operand becomes the tokens and every weight tile is used by
+// 128 rows at once:
+//   phase 1 unit (item = expert, chunk of <= 128 rows; I-slice s of 128):
+//       D [128 x 256] = X_rows . [W_gate[s]; W_up[s]]^T over K = H, the 128
+//       gate and 128 up rows of the slice loaded back to back as one N = 256
+//       operand; SwiGLU -> bf16 A[rows][s*128 ...] in the workspace;
+//   phase 2 unit (item, 256-row H-tile):
+//       D [128 x 256] = A_rows . W_down[h-tile]^T over K = I, stored as the
+//       rows' E_e(x) (each element has one writer: plain 16-byte stores).
+// A prep kernel first copies the token rows into expert order (X_rows), so
+// that every operand tile is one TMA box: four-row TMA gathers and fp32
+// reductions into y cost about as much again as the whole contraction at
+// these sizes.  A combine kernel then sums gate * E_e(x) per token over its
+// rows in ascending row order (deterministic).  The work queue, the
+// per-item counters and the warp roles are those of ffn_stream_kernel.
+// Units are handed out expert by expert, so the chunks of one expert run
+// side by side and read its weights from HBM about once.
+// ---------------------------------------------------------------------------
+struct PfCfg {
+    static constexpr int BM = kTmRows;              // token rows per item (MMA M)
+    static constexpr int BN = kTmCols;              // MMA N: gate+up of a 128-row slice, or 256 rows of H
+    static constexpr int BK = 64;
+    static constexpr int A_BYTES = BM * 64 * 2;     // 16 KiB
+    static constexpr int B_BOX = 128 * 64 * 2;      // 16 KiB
+    static constexpr int B_BYTES = 2 * B_BOX;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int NSTAGE = 4;
+    static constexpr int QN = 4;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+    static constexpr int NBAR = 2 * NSTAGE + 5 + 2 * QN;
+    static constexpr int MISC_INTS = 8;             // tmem slot, abort flag, table size, unit ring
+    static constexpr int TABLE_INTS = 4 * MOE_MAX_EXPERTS + 4;
+    static constexpr int SMEM = 1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + TABLE_INTS * 4;
+    static constexpr uint32_t TMEM_COLS = 512;      // two accumulator slots of 256 columns
+    static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(PfCfg::THREADS, 1)
+    ffn_prefill_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
+                       const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_xp,
+                       const __grid_constant__ CUtensorMap tm_act, const int32_t* __restrict__ offsets,
+                       const int32_t* __restrict__ active, const int32_t* __restrict__ row_token,
+                       __nv_bfloat16* __restrict__ act_g, int* counters, int* tok_cnt, int* tok_rows,
+                       float* __restrict__ rows_out, int rows_accumulate, int H, int I, int N, int k,
+                       moe_dev_status* st) {
+    using C = PfCfg;
+    constexpr int NT = C::BM;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + C::NSTAGE * C::STAGE);
+    int* misc = reinterpret_cast<int*>(bars + C::NBAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = misc + 1;
+    int* s_items = misc + 2;                         // active experts, items
+    volatile int* uring = misc + 4;                  // [QN] unit ids, -1 = no more work
+    int* table = misc + C::MISC_INTS;
+    UnitTable tb{table, table + MOE_MAX_EXPERTS, table + 2 * MOE_MAX_EXPERTS, table + 3 * MOE_MAX_EXPERTS, 0};
+
+    const uint32_t ring_a = smem_u32(ring);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    const int B_FULL = 0, B_EMPTY = C::NSTAGE, B_ACCF = 2 * C::NSTAGE, B_ACCE = B_ACCF + 2, B_DRAIN = B_ACCE + 2,
+              B_QFULL = B_DRAIN + 1, B_QEMPTY = B_QFULL + C::QN;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NSTAGE; ++i) {
+            mbar_init(bar(B_FULL + i), 1);
+            mbar_init(bar(B_EMPTY + i), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B_ACCF + b), 1);
+            mbar_init(bar(B_ACCE + b), C::EPI_THREADS);
+        }
+        mbar_init(bar(B_DRAIN), 1);
+        for (int i = 0; i < C::QN; ++i) {
+            mbar_init(bar(B_QFULL + i), 1);
+            mbar_init(bar(B_QEMPTY + i), 2);   // the MMA thread and the epilogue
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_wg);
+        tma_prefetch_desc(&tm_wu);
+        tma_prefetch_desc(&tm_wd);
+        tma_prefetch_desc(&tm_xp);
+        tma_prefetch_desc(&tm_act);
+    }
+    const int S = I / 128, MT = H / C::BN;
+    pdl_wait();
+    pdl_trigger();
+    if (warp == 2) {
+        const int na = min(active[0], N);
+        int run = 0;
+        for (int base = 0; base < na; base += 32) {
+            const int a = base + lane;
+            int e = 0, r0 = 0, cnt = 0, ch = 0;
+            if (a < na) {
+                e = active[1 + a];
+                r0 = offsets[e];
+                cnt = offsets[e + 1] - r0;
+                ch = (cnt + NT - 1) / NT;
+            }
+            int inc = ch;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(kFull, inc, off);
+                if (lane >= off) inc += o;
+            }
+            if (a < na) {
+                tb.e[a] = e;
+                tb.row[a] = r0;
+                tb.cnt[a] = cnt;
+                tb.pre[a] = run + inc - ch;
+            }
+            run += __shfl_sync(kFull, inc, 31);
+        }
+        if (lane == 0) {
+            tb.pre[na] = run;
+            s_items[0] = na;
+            s_items[1] = run;
+        }
+    }
+    __syncthreads();
+    tb.na = s_items[0];
+    const int n1 = s_items[1] * S, n_total = n1 + s_items[1] * MT;
+    if (n_total == 0) return;
+    int* const work_head = counters;
+    int* const item_done = counters + 1;
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int KT1 = H / C::BK, KT2 = I / C::BK;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        const uint64_t pol_w = l2_policy_evict_last(), pol_x = l2_policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0, pend = 0, pend_par = 0;
+        bool ok = true;
+        int cur = (lane == 0) ? atomicAdd(work_head, 1) : 0;
+        cur = __shfl_sync(kFull, cur, 0);
+        for (int j = 0;; ++j) {
+            const bool done = cur >= n_total;
+            if (lane == 0) {
+                const int qs = j % C::QN;
+                ok = mbar_wait(bar(B_QEMPTY + qs), ((j / C::QN) & 1) ^ 1, abort_flag, st, kSiteProducerEmpty);
+                if (ok) {
+                    uring[qs] = done ? -1 : cur;
+                    mbar_arrive(bar(B_QFULL + qs));
+                }
+            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (!ok || done) break;
+            int nxt = 0;
+            if (lane == 0) nxt = atomicAdd(work_head, 1);
+            const bool p1 = cur < n1;
+            const int v = p1 ? cur : cur - n1;
+            const int item = p1 ? v / S : v / MT;
+            const int sub = p1 ? v - item * S : v - item * MT;
+            int e, row0, nrows;
+            item_info(tb, item, NT, e, row0, nrows);
+            if (lane == 0) {
+                if (!p1) {
+                    const unsigned long long t0 = global_ns();
+                    while (ld_acquire_gpu(item_done + item) < S) {
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        if (global_ns() - t0 > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            report(st, MOE_DEV_TIMEOUT, kSiteDependency);
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                    fence_proxy_async_global();
+                }
+                const int nk = p1 ? KT1 : KT2;
+                for (int kt = 0; kt < nk && ok; ++kt) {
+                    if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = ring_a + stage * C::STAGE;
+                    const uint32_t fb = bar(B_FULL + stage);
+                    if (p1) {
+                        const int wrow = e * I + sub * 128;
+                        mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                        tma_load_2d(dst, &tm_xp, kt * C::BK, row0, fb, pol_x);
+                        tma_load_2d(dst + C::A_BYTES, &tm_wg, kt * C::BK, wrow, fb, pol_w);
+                        tma_load_2d(dst + C::A_BYTES + C::B_BOX, &tm_wu, kt * C::BK, wrow, fb, pol_w);
+                    } else {
+                        const int wrow = e * H + sub * C::BN;
+                        mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                        tma_load_2d(dst, &tm_act, kt * C::BK, row0, fb, pol_x);
+                        tma_load_2d(dst + C::A_BYTES, &tm_wd, kt * C::BK, wrow, fb, pol_w);
+                        tma_load_2d(dst + C::A_BYTES + C::B_BOX, &tm_wd, kt * C::BK, wrow + 128, fb, pol_w);
+                    }
+                    pend |= 1u << stage;
+                    pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::NSTAGE) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            cur = __shfl_sync(kFull, nxt, 0);
+        }
+        if (!ok && lane == 0) {
+            for (int i = 0; i < C::NSTAGE; ++i)
+                if (pend >> i & 1u) mbar_drain(bar(B_FULL + i), pend_par >> i & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer: D[128 x 256] per unit ----------------
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 256);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int j = 0; ok; ++j) {
+                const int qs = j % C::QN;
+                if (!mbar_wait(bar(B_QFULL + qs), (j / C::QN) & 1, abort_flag, st, kSiteMmaFull)) break;
+                const int un = uring[qs];
+                mbar_arrive(bar(B_QEMPTY + qs));
+                if (un < 0) break;
+                const int b = j & 1;
+                const uint32_t acc = tmem + b * C::BN;
+                if (!mbar_wait(bar(B_ACCE + b), ((j >> 1) & 1) ^ 1, abort_flag, st, kSiteMmaTmemFree)) break;
+                tc_fence_after();
+                const int nk = (un < n1) ? KT1 : KT2;
+                for (int kt = 0; kt < nk; ++kt) {
+                    if (!mbar_wait(bar(B_FULL + stage), phase, abort_flag, st, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = ring_a + stage * C::STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 16; ++kk)
+                        tc_mma_bf16(acc, sw128_desc(a + kk * 32), sw128_desc(a + C::A_BYTES + kk * 32), idesc,
+                                    (kt | kk) != 0);
+                    tc_commit(bar(B_EMPTY + stage));
+                    if (++stage == C::NSTAGE) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(bar(B_ACCF + b));
+            }
+            tc_commit(bar(B_DRAIN));
+            mbar_drain(bar(B_DRAIN), 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warps 2..9; thread = token row, warp pair splits the columns ----------------
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int r = q * 32 + lane;                   // row of the item
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        for (int j = 0;; ++j) {
+            const int qs = j % C::QN;
+            bool okw = __all_sync(kFull, mbar_wait(bar(B_QFULL + qs), (j / C::QN) & 1, abort_flag, st, kSiteEpiG1Done));
+            const int un = okw ? uring[qs] : -1;
+            if (!named_sync_and(C::EPI_THREADS, okw)) break;
+            if (un < 0) break;
+            const bool p1 = un < n1;
+            const int v = p1 ? un : un - n1;
+            const int item = p1 ? v / S : v / MT;
+            const int sub = p1 ? v - item * S : v - item * MT;
+            int e, row0, nrows;
+            item_info(tb, item, NT, e, row0, nrows);
+            const int b = j & 1;
+            const uint32_t acc = tmem + b * C::BN + lane_off;
+            const bool live = r < nrows;
+            okw = __all_sync(kFull, mbar_wait(bar(B_ACCF + b), (j >> 1) & 1, abort_flag, st, kSiteEpiG1Done));
+            if (okw) {
+                tc_fence_after();
+                if (p1) {
+                    // this warp: I columns [64*half, 64*half + 64) of the slice; gate at +0, up at +128
+                    __nv_bfloat16* dst = act_g + static_cast<size_t>(row0 + r) * I + sub * 128 + 64 * half;
+#pragma unroll
+                    for (int c16 = 0; c16 < 4; ++c16) {
+                        uint32_t g[16], u[16];
+                        tmem_ld16(acc + 64 * half + 16 * c16, g);
+                        tmem_ld16(acc + 128 + 64 * half + 16 * c16, u);
+                        tmem_ld_wait();
+                        if (c16 == 3) {
+                            tc_fence_before();
+                            mbar_arrive(bar(B_ACCE + b));
+                        }
+                        if (live) {
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                                    silu_mul(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                    silu_mul(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+                                pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+                            }
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c16);
+                            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        }
+                    }
+                    // the first slice of an item records its rows under their tokens for the combine
+                    if (sub == 0 && half == 0 && live && tok_cnt != nullptr) {
+                        const int t = row_token[row0 + r];
+                        tok_rows[static_cast<size_t>(t) * k + atomicAdd(tok_cnt + t, 1)] = row0 + r;
+                    }
+                    fence_proxy_async_global();
+                    __threadfence();
+                } else {
+                    // this warp: H columns [128*half, 128*half + 128) of the 256-row tile; every
+                    // element of rows_out has exactly this one writer
+                    float* dst = rows_out + static_cast<size_t>(row0 + r) * H + sub * C::BN + 128 * half;
+#pragma unroll 1
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        uint32_t d[16];
+                        tmem_ld16(acc + 128 * half + 16 * c16, d);
+                        tmem_ld_wait();
+                        if (c16 == 7) {
+                            tc_fence_before();
+                            mbar_arrive(bar(B_ACCE + b));
+                        }
+                        if (live) {
+                            float4* d4 = reinterpret_cast<float4*>(dst + 16 * c16);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                float4 v = make_float4(__uint_as_float(d[4 * i]), __uint_as_float(d[4 * i + 1]),
+                                                       __uint_as_float(d[4 * i + 2]), __uint_as_float(d[4 * i + 3]));
+                                if (rows_accumulate) {
+                                    const float4 o = d4[i];
+                                    v.x += o.x;
+                                    v.y += o.y;
+                                    v.z += o.z;
+                                    v.w += o.w;
+                                }
+                                d4[i] = v;
+                            }
+                        }
+                    }
+                }
+            }
+            if (!named_sync_and(C::EPI_THREADS, okw)) break;
+            if (threadIdx.x == 64) {
+                if (p1) red_release_gpu_add(item_done + item, 1);
+                mbar_arrive(bar(B_QEMPTY + qs));
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// Token-major path, before the FFN kernel: clears the work, item and token
+// counters and copies every dispatch row's activations into expert order,
+// X_rows[r] = x[row_token[r]] (16-byte vectors, one warp per row).
+__global__ void __launch_bounds__(256) ffn_tm_prep_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ row_token,
+                                                          const int32_t* __restrict__ offsets, int N, int H,
+                                                          uint4* __restrict__ xp, int* zero, int n_zero) {
+    pdl_wait();
+    pdl_trigger();
+    const int gtid = blockIdx.x * 256 + threadIdx.x, nthr = gridDim.x * 256;
+    for (int i = gtid; i < n_zero; i += nthr) zero[i] = 0;
+    const int M = offsets[N];
+    const int v = H / 8;
+    const int lane = threadIdx.x & 31;
+    for (int r = gtid >> 5; r < M; r += nthr >> 5) {
+        const uint4* src = x + static_cast<size_t>(row_token[r]) * v;
+        uint4* d = xp + static_cast<size_t>(r) * v;
+        for (int c = lane; c < v; c += 32) d[c] = src[c];
+    }
+}
+
+// Token-major path, after the FFN kernel: y[t] = (y[t] or 0) + sum over the
+// token's rows, in ascending row order, of gate * E_e(x_t).
+__global__ void __launch_bounds__(256) ffn_tm_combine_kernel(const float* __restrict__ rows,
+                                                             const int* __restrict__ tok_cnt,
+                                                             const int* __restrict__ tok_rows,
+                                                             const float* __restrict__ row_gate, int T, int H,
+                                                             int k, int zero_y, float* __restrict__ y) {
+    __shared__ int srow[MOE_MAX_RANKS];
+    __shared__ float sg[MOE_MAX_RANKS];
+    __shared__ int sn;
+    pdl_wait();
+    pdl_trigger();
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        if (threadIdx.x == 0) {
+            const int n = min(tok_cnt[t], k);
+            for (int i = 0; i < n; ++i) {
+                const int v = tok_rows[static_cast<size_t>(t) * k + i];
+                int j = i;
+                while (j > 0 && srow[j - 1] > v) {
+                    srow[j] = srow[j - 1];
+                    --j;
+                }
+                srow[j] = v;
+            }
+            for (int i = 0; i < n; ++i) sg[i] = row_gate[srow[i]];
+            sn = n;
+        }
+        __syncthreads();
+        const int n = sn;
+        float4* yt = reinterpret_cast<float4*>(y + static_cast<size_t>(t) * H);
+        for (int h4 = threadIdx.x; h4 < H / 4; h4 += 256) {
+            float4 a = zero_y ? make_float4(0.f, 0.f, 0.f, 0.f) : yt[h4];
+            for (int i = 0; i < n; ++i) {
+                const float4 v = reinterpret_cast<const float4*>(rows + static_cast<size_t>(srow[i]) * H)[h4];
+                a.x = fmaf(sg[i], v.x, a.x);
+                a.y = fmaf(sg[i], v.y, a.y);
+                a.z = fmaf(sg[i], v.z, a.z);
+                a.w = fmaf(sg[i], v.w, a.w);
+            }
+            yt[h4] = a;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side of the tensor-core path.
 // ---------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -596,10 +1068,62 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
                       tm_act, offsets, active, row_token, row_gate, act, counters, out, H, I, N, fuse ? 1 : 0, st);
 }
 
+static cudaError_t run_tokmajor(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
+                                int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
+                                const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
+                                cudaStream_t s) {
+    using C = PfCfg;
+    const bool fuse = (flags & MOE_FFN_FUSE_COMBINE) != 0;
+    const long long M = static_cast<long long>(T) * k;
+    const TmLayout Lw = tm_layout(T, H, I, N, k);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    int* counters = reinterpret_cast<int*>(base);
+    int* tok_cnt = reinterpret_cast<int*>(base + Lw.tok_cnt);
+    int* tok_rows = reinterpret_cast<int*>(base + Lw.tok_rows);
+    __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(base + Lw.act);
+    void* xp = base + Lw.xp;
+    float* rows = reinterpret_cast<float*>(base + Lw.rows);
+    const int sms = sm_count();
+    cudaError_t e = launch_pdl(ffn_tm_prep_kernel, dim3(4 * sms), dim3(256), 0, s, static_cast<const uint4*>(x),
+                               row_token, offsets, N, H, static_cast<uint4*>(xp), counters,
+                               static_cast<int>(Lw.n_zero));
+    if (e != cudaSuccess) return e;
+    CUtensorMap tm_wg, tm_wu, tm_wd, tm_xp, tm_act;
+    if (!make_tmap(&tm_wg, wg, H, static_cast<uint64_t>(N) * I, 64, 128) ||
+        !make_tmap(&tm_wu, wu, H, static_cast<uint64_t>(N) * I, 64, 128) ||
+        !make_tmap(&tm_wd, wd, I, static_cast<uint64_t>(N) * H, 64, 128) ||
+        !make_tmap(&tm_xp, xp, H, static_cast<uint64_t>(M), 64, 128) ||
+        !make_tmap(&tm_act, act, I, static_cast<uint64_t>(M), 64, 128))
+        return cudaErrorInvalidValue;
+    static bool attr_set[64] = {};
+    int devi = 0;
+    cudaGetDevice(&devi);
+    if (devi < 0 || devi >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[devi]) {
+        cudaError_t ae = cudaFuncSetAttribute(ffn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (ae != cudaSuccess) return ae;
+        attr_set[devi] = true;
+    }
+    const long long max_units = Lw.items * (I / 128 + H / C::BN);
+    int grid = sms;
+    if (max_units < grid) grid = static_cast<int>(max_units > 0 ? max_units : 1);
+    e = launch_pdl(ffn_prefill_kernel, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wd, tm_xp, tm_act,
+                   offsets, active, row_token, act, counters, fuse ? tok_cnt : static_cast<int*>(nullptr), tok_rows,
+                   fuse ? rows : out, fuse ? 0 : 1, H, I, N, k, st);
+    if (e != cudaSuccess || !fuse) return e;
+    const int cgrid = T < 8 * sms ? T : 8 * sms;
+    return launch_pdl(ffn_tm_combine_kernel, dim3(cgrid), dim3(256), 0, s, static_cast<const float*>(rows),
+                      static_cast<const int*>(tok_cnt), static_cast<const int*>(tok_rows), row_gate, T, H, k,
+                      (flags & MOE_FFN_ZERO_Y) ? 1 : 0, out);
+}
+
 cudaError_t launch_ffn_bf16(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
                             int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                             const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
                             cudaStream_t s) {
+    // batches with many rows per expert run token-major on the tensor cores
+    if (token_major(T, H))
+        return run_tokmajor(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws, st, s);
     switch (ffn_nt(T)) {
         case 16:
             return run_stream<16>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws,

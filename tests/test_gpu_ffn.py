@@ -108,3 +108,44 @@ def test_repeat_calls_are_stable(g, qwen):
         g.assert_y_close(y, yref, "repeat")
     # fp32 atomics reorder sums only: repeated results agree far inside the bar
     assert np.max(np.abs(ys[0] - ys[1])) <= 1e-4 * np.sqrt(np.mean(yref ** 2))
+
+
+def _skewed_ids(rng, T, N, k, hot=0, hole_frac=0.1):
+    """Every token routes to expert `hot` plus k-1 others: `hot` gets T rows
+    (many 128-row chunks and a ragged tail), the rest a few dozen each."""
+    ids = np.stack([np.concatenate([[hot], rng.choice(np.delete(np.arange(N), hot), k - 1, replace=False)])
+                    for _ in range(T)]).astype(np.int32)
+    gates = rng.random((T, k)).astype(np.float32)
+    ids[rng.random(ids.shape) < hole_frac] = -1
+    gates[ids < 0] = 0
+    return ids, gates
+
+
+@pytest.mark.parametrize("fuse", [True, False])
+def test_token_major_multi_chunk_ragged(g, fuse):
+    """T = 1100 runs the token-major (prefill) kernel: expert 0 holds ~990
+    rows (eight 128-row chunks, the last one ragged), the other experts hold
+    one partial chunk each; H spans two 256-row down-projection tiles."""
+    L = syn.qwen_layer(1100, H=512, N=8, k=2, I=256)
+    D = g.DevLayer(L)
+    ids, gates = _skewed_ids(np.random.default_rng(3), 1100, 8, 2)
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=fuse)
+
+
+def test_token_major_odd_tiles(g):
+    """I = 384 (three slices) and H = 768 (three 256-row tiles) in the token-major kernel."""
+    L = syn.qwen_layer(1024, H=768, N=6, k=3, I=384)
+    D = g.DevLayer(L)
+    ids, gates = _route(L, L.x_bf16, 1024)
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
+
+
+def test_token_major_prefill_shape_sampled(g, qwen):
+    """The prefill shape (T = 8192, H = 2048, I = 768, 128 experts, top-8) on
+    plain top-8 routing; sampled tokens against the oracle."""
+    L, D = qwen
+    Lt = syn.prefill(with_weights=False)
+    x_dev = g.dev(Lt.x_bf16, torch.bfloat16)
+    ids, gates = _route(L, Lt.x_bf16, Lt.T)
+    tokens = np.arange(0, Lt.T, 337, dtype=np.int32)
+    _ffn_case(g, L, D, Lt.x_bf16, x_dev, ids, gates, tokens)
