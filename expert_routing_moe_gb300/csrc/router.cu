@@ -15,9 +15,11 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// Router GEMM, small batches: one warp per expert, four tokens per warp, the
-// lanes split H (4 consecutive elements each, 16-byte weight loads) and a
-// fixed xor-butterfly reduces the partial sums.  Grid (ceil(N/8), ceil(T/4)).
+// Router GEMM, small batches: four warps per expert (one per quarter of H,
+// so that a warp issues all of its loads at once), four tokens per warp, the
+// lanes split the quarter (4 consecutive elements each, 16-byte weight
+// loads); a fixed xor-butterfly and a fixed-order sum of the quarters reduce
+// the partial sums.  Two experts per CTA: grid (ceil(N/2), ceil(T/4)).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
     float4 q = *reinterpret_cast<const float4*>(p);
@@ -39,10 +41,10 @@ __global__ void __launch_bounds__(256) router_warp_kernel(const XT* __restrict__
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int j = blockIdx.x * 4 + (warp >> 1);   // two warps per expert, one per half of H
+    const int j = blockIdx.x * 2 + (warp >> 2);   // four warps per expert, one per quarter of H
     const int t0 = blockIdx.y * 4;
-    const int hmid = ((H >> 1) + 127) / 128 * 128;
-    const int hbeg = (warp & 1) ? hmid : 0, hend = (warp & 1) ? H : min(hmid, H);
+    const int hq = ((H >> 2) + 127) / 128 * 128;
+    const int hbeg = min((warp & 3) * hq, H), hend = min(hbeg + hq, H);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (j < N) {
         const float* wr = w + static_cast<size_t>(j) * H;
@@ -81,10 +83,12 @@ __global__ void __launch_bounds__(256) router_warp_kernel(const XT* __restrict__
     }
     if (lane < 4) part[warp][lane] = (lane == 0) ? acc[0] : (lane == 1) ? acc[1] : (lane == 2) ? acc[2] : acc[3];
     __syncthreads();
-    if (threadIdx.x < 16) {
+    if (threadIdx.x < 8) {
         const int jl = threadIdx.x >> 2, tt = threadIdx.x & 3;
-        const int jj = blockIdx.x * 4 + jl;
-        if (jj < N && t0 + tt < T) logits[static_cast<size_t>(t0 + tt) * N + jj] = part[2 * jl][tt] + part[2 * jl + 1][tt];
+        const int jj = blockIdx.x * 2 + jl;
+        if (jj < N && t0 + tt < T)
+            logits[static_cast<size_t>(t0 + tt) * N + jj] =
+                (part[4 * jl][tt] + part[4 * jl + 1][tt]) + (part[4 * jl + 2][tt] + part[4 * jl + 3][tt]);
     }
 }
 
@@ -152,7 +156,7 @@ cudaError_t launch_router(const void* x, int x_dtype, const float* w_router, int
                           cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (T <= 256) {
-        dim3 grid((N + 3) / 4, (T + 3) / 4);
+        dim3 grid((N + 1) / 2, (T + 3) / 4);
         if (x_dtype == MOE_DTYPE_BF16)
             return launch_pdl(router_warp_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
                               static_cast<const __nv_bfloat16*>(x), w_router, T, H, N, logits);
