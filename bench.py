@@ -37,6 +37,11 @@ N_COPIES = 4  # expert-weight copies rotated per step (--copies)
 METRIC = "MoE-layer decode tokens/s (SERE K'=2, rho=0.5; top-8 alongside)"
 UNIT = "tokens/s"
 EXPERT_BYTES = 3 * H * I * 2
+# DRAM bytes (read + write) of one FFN launch from an ncu capture of the current
+# kernel (--set full, SERE batch 4 of this workload: 34 active experts, whose
+# algorithmic bytes are 34 * EXPERT_BYTES + T * H * 6).  Set it to None whenever
+# the FFN kernel changes, until it has been captured again.
+FFN_TRAFFIC_CAPTURE = {"dram_bytes": 324.34e6, "algorithmic_bytes": 321.26e6, "active_experts": 34}
 
 
 def workload_config(extra=None):
@@ -421,7 +426,11 @@ def run_ours(args):
                                                   "steps as a routing graph and an FFN graph with CUDA events "
                                                   "around the FFN graph"}),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": args.traffic, "kernel": "moe_ffn_grouped (counter clear + tcgen05 FFN kernel)",
+                     "traffic": args.traffic if args.traffic is not None else
+                     (FFN_TRAFFIC_CAPTURE["dram_bytes"] if FFN_TRAFFIC_CAPTURE else None),
+                     "traffic_launch_algorithmic_bytes": FFN_TRAFFIC_CAPTURE["algorithmic_bytes"]
+                     if FFN_TRAFFIC_CAPTURE and args.traffic is None else None,
+                     "kernel": "moe_ffn_grouped (counter clear + tcgen05 FFN kernel)",
                      "peak_source": peak_src,
                      "bytes_per_launch_mean": float(np.mean(ffn_bytes)),
                      "ms_per_launch_mean": float(np.mean(ffn_ms))},
