@@ -43,7 +43,7 @@ moe_status_t moe_route(const void* x, int x_dtype, const float* w_router, int T,
     }
     cudaStream_t s = as_stream(stream);
     if (!from_logits) {
-        cudaError_t e = moe::launch_router(x, x_dtype, w_router, T, H, N, logits, s);
+        cudaError_t e = moe::launch_router(x, x_dtype, w_router, T, H, N, logits, st, s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     const bool renorm = (flags & MOE_ROUTE_RENORM_TOPK) != 0;

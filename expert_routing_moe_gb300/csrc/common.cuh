@@ -146,6 +146,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Waits (bounded, ignoring the abort flag) for a phase that must complete
+// before shared memory or TMEM is released, e.g. copies still in flight.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) wrappers.
 // ---------------------------------------------------------------------------

@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 
 namespace moe {
 
@@ -83,14 +84,6 @@ struct UnitTable {
     int* pre;    // [na + 1]: exclusive prefix of chunk counts
     int na;
 };
-
-__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-    return true;
-}
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
@@ -978,48 +971,6 @@ __global__ void __launch_bounds__(256) ffn_tm_combine_kernel(const float* __rest
 // ---------------------------------------------------------------------------
 // Host side of the tensor-core path.
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
-// boxes of box_inner x box_outer with the 128-byte swizzle.
-static bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                      uint32_t box_outer) {
-    auto fn = encode_fn();
-    if (fn == nullptr) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-static int sm_count() {
-    static int cached[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 1;
-    if (cached[dev] == 0) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 1;
-    }
-    return cached[dev];
-}
-
 __global__ void zero_kernel(float* p, long long n, int* c, int nc);
 
 // Clears p[0, n) (fp32) and c[0, nc) (int32) in one launch.

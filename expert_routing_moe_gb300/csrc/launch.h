@@ -31,7 +31,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // ---- routing (router.cu) ----
 cudaError_t launch_router(const void* x, int x_dtype, const float* w_router, int T, int H, int N, float* logits,
-                          cudaStream_t s);
+                          moe_dev_status* st, cudaStream_t s);
 cudaError_t launch_rank(const float* logits, int T, int N, int R, int k, bool renorm, int32_t* ids, float* gates,
                         moe_dev_status* st, cudaStream_t s);
 cudaError_t launch_rank_sere(const float* logits, int T, int N, int k, bool renorm, int32_t* ids, float* gates,

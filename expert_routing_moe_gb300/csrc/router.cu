@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "routing.cuh"
+#include "tmap.h"
 
 namespace moe {
 
@@ -153,9 +154,231 @@ __global__ void __launch_bounds__(256) router_tiled_kernel(const XT* __restrict_
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Router GEMM on the tensor cores, large batches of bf16 tokens.
+//
+// W_r is fp32.  Each element is split exactly into three bf16 parts,
+// w = hi + mid + lo (hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid);
+// both differences are exact in fp32 and lo carries the last bits to within
+// 2^-27 |w|), so every bf16 x bf16 product is exact and the tcgen05 MMA sums
+// x.w over the three planes with fp32 accumulation.  CTA = 128 tokens x 64
+// experts.  Per 64-wide K chunk: warp 0 brings the x tile (TMA, 128-byte
+// swizzle) and the fp32 W chunk (TMA, unswizzled) into a 3-stage ring; warps
+// 2-5 split W into three swizzled bf16 planes; warp 1 issues 3 x 4 MMAs of
+// 128 x 64 x 16 into a 64-column TMEM accumulator.  Warps 2-5 then store the
+// logits.  Every wait is bounded.
+// ---------------------------------------------------------------------------
+constexpr int kRouterTcMinT = 256;   // larger batches use the tensor-core router
+
+struct RtCfg {
+    static constexpr int BM = 128, BN = 64, BK = 64;
+    static constexpr int X_BYTES = BM * BK * 2;      // 16 KiB, bf16 tokens
+    static constexpr int PLANE = BN * BK * 2;        // 8 KiB, one bf16 part of W
+    static constexpr int W32_BYTES = BN * BK * 4;    // 16 KiB, the fp32 W chunk
+    static constexpr int OFF_PLANES = X_BYTES;
+    static constexpr int OFF_W32 = X_BYTES + 3 * PLANE;
+    static constexpr int STAGE = X_BYTES + 3 * PLANE + W32_BYTES;   // 56 KiB
+    static constexpr int NSTAGE = 3;
+    static constexpr int THREADS = 192;
+    static constexpr int CONV_THREADS = 128;
+    static constexpr int NBAR = 3 * NSTAGE + 2;
+    static constexpr int SMEM = 1024 + NSTAGE * STAGE + NBAR * 8 + 16;
+    static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
+};
+
+__global__ void __launch_bounds__(RtCfg::THREADS, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, int T,
+                     int H, int N, float* __restrict__ logits, moe_dev_status* st) {
+    using C = RtCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::NSTAGE * C::STAGE);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t ring_a = smem_u32(smem);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    const int B_FULL = 0, B_CONV = C::NSTAGE, B_EMPTY = 2 * C::NSTAGE, B_ACC = 3 * C::NSTAGE, B_DRAIN = B_ACC + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * C::BM, n0 = blockIdx.y * C::BN;
+    const int KT = H / C::BK;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NSTAGE; ++i) {
+            mbar_init(bar(B_FULL + i), 1);
+            mbar_init(bar(B_CONV + i), C::CONV_THREADS);
+            mbar_init(bar(B_EMPTY + i), 1);
+        }
+        mbar_init(bar(B_ACC), 1);
+        mbar_init(bar(B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::BN);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_last();
+            uint32_t pend = 0, pend_par = 0;
+            bool ok = true;
+            for (int c = 0; c < KT; ++c) {
+                const int s = c % C::NSTAGE;
+                const uint32_t ph = (c / C::NSTAGE) & 1;
+                if (!mbar_wait(bar(B_EMPTY + s), ph ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = ring_a + s * C::STAGE;
+                mbar_arrive_expect_tx(bar(B_FULL + s), C::X_BYTES + C::W32_BYTES);
+                tma_load_2d(dst, &tm_x, c * C::BK, t0, bar(B_FULL + s), pol);
+                tma_load_2d(dst + C::OFF_W32, &tm_w, c * C::BK, n0, bar(B_FULL + s), pol);
+                pend |= 1u << s;
+                pend_par = (pend_par & ~(1u << s)) | (ph << s);
+            }
+            if (!ok)
+                for (int i = 0; i < C::NSTAGE; ++i)
+                    if (pend >> i & 1u) mbar_drain(bar(B_FULL + i), pend_par >> i & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(C::BM, C::BN);
+            bool ok = true;
+            for (int c = 0; c < KT && ok; ++c) {
+                const int s = c % C::NSTAGE;
+                if (!mbar_wait(bar(B_CONV + s), (c / C::NSTAGE) & 1, abort_flag, st, kSiteMmaFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = ring_a + s * C::STAGE;
+#pragma unroll
+                for (int p = 0; p < 3; ++p)
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 16; ++kk)
+                        tc_mma_bf16(tmem, sw128_desc(a + kk * 32), sw128_desc(a + C::OFF_PLANES + p * C::PLANE + kk * 32),
+                                    idesc, (c | p | kk) != 0);
+                tc_commit(bar(B_EMPTY + s));
+            }
+            if (ok) tc_commit(bar(B_ACC));
+            tc_commit(bar(B_DRAIN));
+            mbar_drain(bar(B_DRAIN), 0);
+        }
+        __syncwarp();
+    } else {
+        // ---- split W into three bf16 planes (swizzled K-major), then the epilogue ----
+        const int ct = threadIdx.x - 64;           // 0..127
+        const int r = ct >> 1, kh = ct & 1;        // W row (expert) and which half of the 64 k
+        bool ok = true;
+        for (int c = 0; c < KT; ++c) {
+            const int s = c % C::NSTAGE;
+            ok = __all_sync(kFull, mbar_wait(bar(B_FULL + s), (c / C::NSTAGE) & 1, abort_flag, st, kSiteEpiG1Done));
+            if (!ok) break;
+            uint8_t* stage = smem + s * C::STAGE;
+            const float* wrow = reinterpret_cast<const float*>(stage + C::OFF_W32) + r * C::BK + kh * 32;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = (jj + r) & 3;            // rotated so that neighbouring rows use other banks
+                const float4 a = reinterpret_cast<const float4*>(wrow)[2 * j];
+                const float4 b = reinterpret_cast<const float4*>(wrow)[2 * j + 1];
+                const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                uint32_t ph[4], pm[4], pl[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * q]), h1 = __float2bfloat16_rn(v[2 * q + 1]);
+                    const float r0 = __fsub_rn(v[2 * q], __bfloat162float(h0));
+                    const float r1 = __fsub_rn(v[2 * q + 1], __bfloat162float(h1));
+                    __nv_bfloat16 m0 = __float2bfloat16_rn(r0), m1 = __float2bfloat16_rn(r1);
+                    __nv_bfloat16 l0 = __float2bfloat16_rn(__fsub_rn(r0, __bfloat162float(m0)));
+                    __nv_bfloat16 l1 = __float2bfloat16_rn(__fsub_rn(r1, __bfloat162float(m1)));
+                    ph[q] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                            (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+                    pm[q] = static_cast<uint32_t>(__bfloat16_as_ushort(m0)) |
+                            (static_cast<uint32_t>(__bfloat16_as_ushort(m1)) << 16);
+                    pl[q] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                            (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+                }
+                // 16-byte chunk (kh*4 + j) of row r, 128-byte swizzle: chunk index ^ (r & 7)
+                const int chunk = (kh * 4 + j) ^ (r & 7);
+                const int off = r * 128 + chunk * 16;
+                *reinterpret_cast<uint4*>(stage + C::OFF_PLANES + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                *reinterpret_cast<uint4*>(stage + C::OFF_PLANES + C::PLANE + off) =
+                    make_uint4(pm[0], pm[1], pm[2], pm[3]);
+                *reinterpret_cast<uint4*>(stage + C::OFF_PLANES + 2 * C::PLANE + off) =
+                    make_uint4(pl[0], pl[1], pl[2], pl[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(B_CONV + s));
+        }
+        if (ok) ok = __all_sync(kFull, mbar_wait(bar(B_ACC), 0, abort_flag, st, kSiteEpiAcc2Full));
+        if (ok) {
+            tc_fence_after();
+            const int q = warp & 3;
+            const int t = t0 + q * 32 + lane;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+            for (int c16 = 0; c16 < C::BN / 16; ++c16) {
+                uint32_t v[16];
+                tmem_ld16(taddr + c16 * 16, v);
+                tmem_ld_wait();
+                if (t < T) {
+                    float4* dst = reinterpret_cast<float4*>(logits + static_cast<size_t>(t) * N + n0 + c16 * 16);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::BN);
+    }
+}
+
+// The tensor-core router applies to bf16 tokens with H % 64 == 0, N % 64 == 0
+// and 16-byte aligned logits.
+static bool router_tc_ok(int x_dtype, int H, int N, const float* logits) {
+    return x_dtype == MOE_DTYPE_BF16 && H % RtCfg::BK == 0 && N % RtCfg::BN == 0 &&
+           (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
+}
+
+static cudaError_t launch_router_tc(const void* x, const float* w_router, int T, int H, int N, float* logits,
+                                    moe_dev_status* st, cudaStream_t s) {
+    using C = RtCfg;
+    CUtensorMap tm_x, tm_w;
+    if (!make_tmap(&tm_x, x, H, static_cast<uint64_t>(T), C::BK, C::BM) ||
+        !make_tmap_f32(&tm_w, w_router, H, static_cast<uint64_t>(N), C::BK, C::BN))
+        return cudaErrorInvalidValue;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid((T + C::BM - 1) / C::BM, N / C::BN);
+    return launch_pdl(router_tc_kernel, grid, dim3(C::THREADS), C::SMEM, s, tm_x, tm_w, T, H, N, logits, st);
+}
+
 cudaError_t launch_router(const void* x, int x_dtype, const float* w_router, int T, int H, int N, float* logits,
-                          cudaStream_t s) {
+                          moe_dev_status* st, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
+    if (T > kRouterTcMinT && router_tc_ok(x_dtype, H, N, logits))
+        return launch_router_tc(x, w_router, T, H, N, logits, st, s);
     if (T <= 256) {
         dim3 grid((N + 1) / 2, (T + 3) / 4);
         if (x_dtype == MOE_DTYPE_BF16)
