@@ -193,68 +193,231 @@ __device__ __forceinline__ long long capacity_value(unsigned long long S, int k,
 }
 
 // Phase-1 bucketing: fixed-point weights, total S, copies of the slots, and
-// each slot appended to its expert's bucket (order fixed later by the sort).
-__global__ void cap_bucket_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gates, int ld, int T,
-                                  int N, int k, const float* __restrict__ token_w, DispatchWs w, moe_dev_status* st) {
+// each slot appended to its expert's bucket (order fixed later by the keys).
+// S is summed per block (one global atomic per block); a token's k slots are
+// loaded together; slots of one warp that name the same expert reserve their
+// bucket positions with one atomic.
+__global__ void __launch_bounds__(128) cap_bucket_kernel(const int32_t* __restrict__ ids,
+                                                         const float* __restrict__ gates, int ld, int T, int N,
+                                                         int k, const float* __restrict__ token_w, DispatchWs w,
+                                                         moe_dev_status* st) {
     pdl_wait();
     pdl_trigger();
+    __shared__ unsigned long long sS;
+    if (threadIdx.x == 0) sS = 0ull;
+    __syncthreads();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= T) return;
-    float wt = token_w ? token_w[t] : 1.0f;
-    if (!isfinite(wt) || wt < 0.f) {
-        report(st, MOE_DEV_NONFINITE, t);
-        wt = 0.f;
-    }
-    atomicAdd(w.S, static_cast<unsigned long long>(fixed_weight(wt)));
-    for (int r = 0; r < k; ++r) {
-        const size_t si = static_cast<size_t>(t) * ld + r;
-        const size_t so = static_cast<size_t>(t) * k + r;
-        const int e = ids[si];
-        w.wids[so] = e;
-        w.wgates[so] = gates[si];
-        w.status[so] = kPending;
-        if (e < 0 || e >= N) {
-            report(st, MOE_DEV_BAD_INDEX, e);
-            w.status[so] = MOE_SLOT_DROPPED;
-            w.wids[so] = -1;
-            continue;
+    const int lane = threadIdx.x & 31;
+    unsigned long long wq = 0ull;
+    int ev[MOE_MAX_RANKS];
+    float gv[MOE_MAX_RANKS];
+    if (t < T) {
+        float wt = token_w ? token_w[t] : 1.0f;
+        if (!isfinite(wt) || wt < 0.f) {
+            report(st, MOE_DEV_NONFINITE, t);
+            wt = 0.f;
         }
-        const int pos = atomicAdd(&w.cnt1[e], 1);
-        if (pos >= T) {  // only possible if a token holds the same expert twice
-            report(st, MOE_DEV_BAD_INDEX, e);
-            continue;
+        wq = static_cast<unsigned long long>(fixed_weight(wt));
+#pragma unroll
+        for (int r = 0; r < MOE_MAX_RANKS; ++r) {
+            if (r < k) {
+                ev[r] = ids[static_cast<size_t>(t) * ld + r];
+                gv[r] = gates[static_cast<size_t>(t) * ld + r];
+            }
         }
-        w.bucket1[static_cast<size_t>(e) * T + pos] = static_cast<uint32_t>(t) * 16u + static_cast<uint32_t>(r);
     }
+    for (int off = 16; off >= 1; off >>= 1) wq += __shfl_xor_sync(kFull, wq, off);
+    if (lane == 0) atomicAdd(&sS, wq);
+#pragma unroll
+    for (int r = 0; r < MOE_MAX_RANKS; ++r) {
+        if (r >= k) break;
+        int e = -1;
+        if (t < T) {
+            const size_t so = static_cast<size_t>(t) * k + r;
+            e = ev[r];
+            w.wids[so] = e;
+            w.wgates[so] = gv[r];
+            w.status[so] = kPending;
+            if (e < 0 || e >= N) {
+                report(st, MOE_DEV_BAD_INDEX, e);
+                w.status[so] = MOE_SLOT_DROPPED;
+                w.wids[so] = -1;
+                e = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(kFull, e);
+        if (e >= 0) {
+            const int leader = __ffs(peers) - 1;
+            int pos0 = 0;
+            if (lane == leader) pos0 = atomicAdd(&w.cnt1[e], __popc(peers));
+            const int pos = __shfl_sync(peers, pos0, leader) + __popc(peers & ((1u << lane) - 1u));
+            if (pos >= T) {   // only possible if a token holds the same expert twice
+                report(st, MOE_DEV_BAD_INDEX, e);
+            } else {
+                w.bucket1[static_cast<size_t>(e) * T + pos] = static_cast<uint32_t>(t) * 16u + static_cast<uint32_t>(r);
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(w.S, sS);
 }
 
-// One CTA per expert: sort its candidates by (gate desc, token asc), admit
-// while load + running weight <= C.  `round` < 0 is phase 1 (candidates are
-// the expert's own slots); round i >= 0 admits overflow offers as rerouted.
+// One CTA per expert: admit its candidates in (gate desc, token asc) order
+// while load + running weight <= C (a strict prefix).  `round` < 0 is phase 1
+// (candidates are the expert's own slots); round i >= 0 admits overflow
+// offers as rerouted.
+//
+// The prefix is found without sorting everything.  Keys (~gate bits, token,
+// slot) ascend in admission order.  If all candidates fit, all are admitted.
+// Otherwise a weight histogram over 1024 bins of the key range locates the
+// one bin b* in which the running weight crosses C: every candidate in an
+// earlier bin is admitted, every one in a later bin is not, and only b*'s
+// candidates are sorted (bitonic) and admitted in exact order.  The outcome
+// equals that of sorting all candidates.
+constexpr int kCapBins = 1024;
+constexpr int kCapPer = kCapacityMaxT / 1024;   // candidates per thread at most
+
+__device__ __forceinline__ float cap_weight(const float* token_w, int t) {
+    float wt = token_w ? token_w[t] : 1.0f;
+    return (!isfinite(wt) || wt < 0.f) ? 0.f : wt;
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* red) {
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    unsigned long long s = 0ull;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) s += red[i];
+    return s;
+}
+
 __global__ void __launch_bounds__(1024) cap_admit_kernel(const float* __restrict__ gates, int ld, int T, int N,
                                                          int k, float gamma, const float* __restrict__ token_w,
                                                          int round, DispatchWs w) {
     pdl_wait();
     pdl_trigger();
-    extern __shared__ unsigned long long keys[];
-    __shared__ long long part[1024];
-    __shared__ unsigned long long admitted_max;
+    extern __shared__ unsigned long long keys[];       // [P2(T)] candidate keys, then [T] float weights
+    __shared__ unsigned long long hist[kCapBins];
+    __shared__ unsigned long long red[32];
+    __shared__ unsigned long long s_kmin, s_kmax, s_adm;
+    __shared__ long long s_excl;
+    __shared__ int s_bstar, s_m;
+    int P2T = 1;
+    while (P2T < T) P2T <<= 1;
+    float* wts = reinterpret_cast<float*>(keys + P2T);
     const int e = blockIdx.x;
     const int n = min((round < 0) ? w.cnt1[e] : w.cnt2[e], T);
     const uint32_t* bucket = ((round < 0) ? w.bucket1 : w.bucket2) + static_cast<size_t>(e) * T;
-    int P2 = 1;
-    while (P2 < n) P2 <<= 1;
-    for (int i = threadIdx.x; i < P2; i += blockDim.x) {
-        unsigned long long key = ~0ull;
+    const long long C = capacity_value(*w.S, k, gamma, N);
+    const long long base = (round < 0) ? 0ll : w.load[e];
+    auto admit = [&](uint32_t tr) {
+        const size_t so = static_cast<size_t>(tr >> 4) * k + (tr & 15u);
+        if (round < 0) {
+            w.status[so] = MOE_SLOT_KEPT;
+        } else {
+            w.status[so] = MOE_SLOT_REROUTED;
+            w.wids[so] = e;
+        }
+    };
+    // candidates: keys and weights (independent loads, batched per thread)
+    unsigned long long tot = 0ull, kmin = ~0ull, kmax = 0ull;
+#pragma unroll
+    for (int j = 0; j < kCapPer; ++j) {
+        const int i = threadIdx.x + j * 1024;
         if (i < n) {
             const uint32_t tr = bucket[i];
-            const int t = static_cast<int>(tr >> 4), r = static_cast<int>(tr & 15u);
-            const float g = gates[static_cast<size_t>(t) * ld + r];
-            key = (static_cast<unsigned long long>(~__float_as_uint(g)) << 32) | tr;
+            const int t = static_cast<int>(tr >> 4);
+            const float g = gates[static_cast<size_t>(t) * ld + (tr & 15u)];
+            const unsigned long long key = (static_cast<unsigned long long>(~__float_as_uint(g)) << 32) | tr;
+            const float wt = cap_weight(token_w, t);
+            keys[i] = key;
+            wts[i] = wt;
+            tot += static_cast<unsigned long long>(fixed_weight(wt));
+            kmin = min(kmin, key);
+            kmax = max(kmax, key);
         }
-        keys[i] = key;
     }
-    if (threadIdx.x == 0) admitted_max = 0ull;
+    for (int off = 16; off >= 1; off >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, off));
+        kmax = max(kmax, __shfl_xor_sync(kFull, kmax, off));
+    }
+    if (threadIdx.x == 0) {
+        s_kmin = ~0ull;
+        s_kmax = 0ull;
+        s_adm = 0ull;
+        s_m = 0;
+        s_bstar = -1;   // stays -1 only if no bin crosses C: then nothing beyond the load is admitted
+        s_excl = 0;
+    }
+    for (int i = threadIdx.x; i < kCapBins; i += blockDim.x) hist[i] = 0ull;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+        atomicMin(&s_kmin, kmin);
+        atomicMax(&s_kmax, kmax);
+    }
+    tot = block_sum_u64(tot, red);   // includes a __syncthreads
+    if (n == 0) {
+        if (threadIdx.x == 0 && round < 0) w.load[e] = base;
+        return;
+    }
+    if (base + static_cast<long long>(tot) <= C) {
+        // everything fits
+        for (int i = threadIdx.x; i < n; i += blockDim.x) admit(static_cast<uint32_t>(keys[i] & 0xffffffffull));
+        if (threadIdx.x == 0) w.load[e] = base + static_cast<long long>(tot);
+        return;
+    }
+    const unsigned long long k0 = s_kmin, span = s_kmax - s_kmin;
+    const int shift = (span >> 10) == 0ull ? 0 : 64 - __clzll(static_cast<long long>(span >> 10));
+    auto bin_of = [&](unsigned long long key) { return static_cast<int>((key - k0) >> shift); };
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+        atomicAdd(&hist[bin_of(keys[i])], static_cast<unsigned long long>(fixed_weight(wts[i])));
+    __syncthreads();
+    // exclusive scan of the bins (thread b owns bin b), then the crossing bin
+    {
+        const int b = threadIdx.x;
+        const unsigned long long hv = (b < kCapBins) ? hist[b] : 0ull;
+        unsigned long long inc = hv;
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned long long o = __shfl_up_sync(kFull, inc, off);
+            if ((b & 31) >= off) inc += o;
+        }
+        if ((b & 31) == 31) red[b >> 5] = inc;
+        __syncthreads();
+        unsigned long long wpre = 0ull;
+        for (int i = 0; i < (b >> 5); ++i) wpre += red[i];
+        const long long incl = static_cast<long long>(wpre + inc), excl = incl - static_cast<long long>(hv);
+        if (b < kCapBins && base + excl <= C && base + incl > C) {
+            s_bstar = b;
+            s_excl = excl;
+        }
+    }
+    __syncthreads();
+    const int bstar = s_bstar;
+    const long long excl = s_excl;
+    // admit the bins before b*; collect b*'s candidates at the front of keys[]
+    unsigned long long mine[kCapPer];
+    int nm = 0;
+#pragma unroll
+    for (int j = 0; j < kCapPer; ++j) {
+        const int i = threadIdx.x + j * 1024;
+        if (i < n) {
+            const unsigned long long key = keys[i];
+            const int bb = bin_of(key);
+            if (bb < bstar) admit(static_cast<uint32_t>(key & 0xffffffffull));
+            else if (bb == bstar) mine[nm++] = key;
+        }
+    }
+    __syncthreads();   // every key is in registers before the front of keys[] is rewritten
+    if (nm > 0) {
+        const int pos = atomicAdd(&s_m, nm);
+        for (int j = 0; j < nm; ++j) keys[pos + j] = mine[j];
+    }
+    __syncthreads();
+    const int m = s_m;
+    int P2 = 1;
+    while (P2 < m) P2 <<= 1;
+    for (int i = m + threadIdx.x; i < P2; i += blockDim.x) keys[i] = ~0ull;
     __syncthreads();
     for (int size = 2; size <= P2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -262,58 +425,59 @@ __global__ void __launch_bounds__(1024) cap_admit_kernel(const float* __restrict
                 const int lo = 2 * i - (i & (stride - 1));
                 const int hi = lo + stride;
                 const bool up = (lo & size) == 0;
-                const unsigned long long a = keys[lo], b = keys[hi];
-                if ((a > b) == up) {
-                    keys[lo] = b;
-                    keys[hi] = a;
+                const unsigned long long x0 = keys[lo], x1 = keys[hi];
+                if ((x0 > x1) == up) {
+                    keys[lo] = x1;
+                    keys[hi] = x0;
                 }
             }
             __syncthreads();
         }
     }
-    // running weight in sorted order: each thread owns a contiguous chunk
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int i0 = threadIdx.x * per;
-    long long local = 0;
-    for (int i = i0; i < min(n, i0 + per); ++i) {
-        const int t = static_cast<int>((keys[i] & 0xffffffffull) >> 4);
-        float wt = token_w ? token_w[t] : 1.0f;
-        if (!isfinite(wt) || wt < 0.f) wt = 0.f;
-        local += fixed_weight(wt);
-    }
-    part[threadIdx.x] = local;
-    __syncthreads();
-    // inclusive Hillis-Steele scan over the 1024 chunk sums
-    for (int off = 1; off < 1024; off <<= 1) {
-        const long long v = (threadIdx.x >= off) ? part[threadIdx.x - off] : 0ll;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    const long long C = capacity_value(*w.S, k, gamma, N);
-    const long long base = (round < 0) ? 0ll : w.load[e];
-    long long cum = part[threadIdx.x] - local;
-    unsigned long long best = 0ull;
-    for (int i = i0; i < min(n, i0 + per); ++i) {
-        const uint32_t tr = static_cast<uint32_t>(keys[i] & 0xffffffffull);
-        const int t = static_cast<int>(tr >> 4), r = static_cast<int>(tr & 15u);
-        float wt = token_w ? token_w[t] : 1.0f;
-        if (!isfinite(wt) || wt < 0.f) wt = 0.f;
-        cum += fixed_weight(wt);
-        if (base + cum <= C) {
-            const size_t so = static_cast<size_t>(t) * k + r;
-            if (round < 0) {
-                w.status[so] = MOE_SLOT_KEPT;
-            } else {
-                w.status[so] = MOE_SLOT_REROUTED;
-                w.wids[so] = e;
+    // running weight through b* in sorted order (m is small: one thread walks it when m <= 64)
+    if (m <= 64) {
+        if (threadIdx.x == 0) {
+            long long cum = base + excl;
+            unsigned long long adm = 0ull;
+            for (int i = 0; i < m; ++i) {
+                const uint32_t tr = static_cast<uint32_t>(keys[i] & 0xffffffffull);
+                cum += fixed_weight(cap_weight(token_w, static_cast<int>(tr >> 4)));
+                if (cum > C) break;
+                admit(tr);
+                adm = static_cast<unsigned long long>(cum - base - excl);
             }
-            best = static_cast<unsigned long long>(cum);
+            s_adm = adm;
         }
+    } else {
+        // each thread a contiguous chunk, block scan of the chunk sums
+        const int per = (m + blockDim.x - 1) / blockDim.x;
+        const int i0 = threadIdx.x * per;
+        long long local = 0;
+        for (int i = i0; i < min(m, i0 + per); ++i)
+            local += fixed_weight(cap_weight(token_w, static_cast<int>((keys[i] & 0xffffffffull) >> 4)));
+        unsigned long long inc = static_cast<unsigned long long>(local);
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned long long o = __shfl_up_sync(kFull, inc, off);
+            if ((threadIdx.x & 31) >= off) inc += o;
+        }
+        __syncthreads();
+        if ((threadIdx.x & 31) == 31) red[threadIdx.x >> 5] = inc;
+        __syncthreads();
+        unsigned long long wpre = 0ull;
+        for (int i = 0; i < static_cast<int>(threadIdx.x >> 5); ++i) wpre += red[i];
+        long long cum = base + excl + static_cast<long long>(wpre + inc) - local;
+        unsigned long long best = 0ull;
+        for (int i = i0; i < min(m, i0 + per); ++i) {
+            const uint32_t tr = static_cast<uint32_t>(keys[i] & 0xffffffffull);
+            cum += fixed_weight(cap_weight(token_w, static_cast<int>(tr >> 4)));
+            if (cum > C) break;
+            admit(tr);
+            best = static_cast<unsigned long long>(cum - base - excl);
+        }
+        if (best > 0ull) atomicMax(&s_adm, best);
     }
-    if (best > 0ull) atomicMax(&admitted_max, best);
     __syncthreads();
-    if (threadIdx.x == 0) w.load[e] = base + static_cast<long long>(admitted_max);
+    if (threadIdx.x == 0) w.load[e] = base + excl + static_cast<long long>(s_adm);
 }
 
 // Overflow round i: each token offers its lowest-rank pending slot to its
@@ -378,12 +542,12 @@ cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int 
     if (err != cudaSuccess) return err;
     const int tb = 256;
     if (T > 0) {
-        err = launch_pdl(cap_bucket_kernel, dim3((T + tb - 1) / tb), dim3(tb), 0, s, ids, gates, ld, T, N, k, token_w,
+        err = launch_pdl(cap_bucket_kernel, dim3((T + 127) / 128), dim3(128), 0, s, ids, gates, ld, T, N, k, token_w,
                          w, st);
         if (err != cudaSuccess) return err;
         size_t P2 = 1;
         while (P2 < static_cast<size_t>(T)) P2 <<= 1;
-        const size_t smem = P2 * sizeof(unsigned long long);
+        const size_t smem = P2 * sizeof(unsigned long long) + static_cast<size_t>(T) * sizeof(float);
         err = cudaFuncSetAttribute(cap_admit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem));
         if (err != cudaSuccess) return err;
