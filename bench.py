@@ -543,53 +543,60 @@ def run_prefill(args):
 
 def run_stack(args):
     """48 decode layers (batch 64), each with its own ~1.2 GB of experts, router,
-    similarity and protection; x_{l+1} = x_l + y_l.  One CUDA graph per step,
-    SERE K'=2 vs top-8."""
+    similarity and protection; x_{l+1} = x_l + y_l.  One CUDA graph per step.
+    Modes: plain top-8, SERE K'=2 and K'=1 at rho = 0.5, and plain top-2 (the
+    fixed top-K' baseline, same weights, for the latency and union comparison
+    only)."""
     torch, moe, dev, ws, rank, local = _gpu_setup()
     from expert_routing_moe_gb300 import synthetic as syn
     nl, B = args.layers, syn.STACK_BATCH
     x0f, x0b = syn.stack_tokens(B, H)
     x0_f32 = torch.from_numpy(x0f).to(dev)
     x0_bf16 = torch.from_numpy(x0b).view(torch.bfloat16).to(dev)
-    layers = []
+    layers, layers_k1, layers_top2 = [], [], []
     for l in range(nl):
         gen = torch.Generator(device=dev)
         gen.manual_seed(syn.stack_weight_seed(l))
         w = [(torch.randn(shape, generator=gen, device=dev) * 0.02).to(torch.bfloat16)
              for shape in ((N, I, H), (N, I, H), (N, H, I))]
-        layers.append(moe.MoELayer(torch.from_numpy(syn.stack_router(x0f, l)).to(dev), *w, k=K_TOP, max_tokens=B,
-                                   sim=torch.from_numpy(syn.stack_sim(l)).to(dev),
-                                   protect=torch.from_numpy(syn.stack_protect(l)).to(dev), k_primary=K_PRIMARY,
+        w_r = torch.from_numpy(syn.stack_router(x0f, l)).to(dev)
+        sim = torch.from_numpy(syn.stack_sim(l)).to(dev)
+        prot = torch.from_numpy(syn.stack_protect(l)).to(dev)
+        layers.append(moe.MoELayer(w_r, *w, k=K_TOP, max_tokens=B, sim=sim, protect=prot, k_primary=K_PRIMARY,
                                    rho=RHO))
+        layers_k1.append(moe.MoELayer(w_r, *w, k=K_TOP, max_tokens=B, sim=sim, protect=prot, k_primary=1, rho=RHO))
+        layers_top2.append(moe.MoELayer(w_r, *w, k=2, max_tokens=B))
     xres = torch.empty(B, H, dtype=torch.float32, device=dev)
     xb = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step(sere):
+    def step(stack, sere):
         xres.copy_(x0_f32)
         xb.copy_(x0_bf16)
-        for lay in layers:
+        for lay in stack:
             lay.route(xb, sere)
             lay.dispatch(B)
             lay.ffn(xb, accumulate_into=xres)
             xb.copy_(xres)
 
     res = {}
-    for mode, sere in (("top8", False), ("sere_k2", True)):
+    for mode, stack, sere in (("top8", layers, False), ("sere_k2", layers, True), ("sere_k1", layers_k1, True),
+                              ("top2", layers_top2, False)):
+        step_fn = lambda: step(stack, sere)
         with torch.cuda.stream(stream):
-            step(sere)
+            step_fn()
         stream.synchronize()
-        us = [int(l.active[0].item()) for l in layers]
-        for l in layers:
+        us = [int(l.active[0].item()) for l in stack]
+        for l in stack:
             code, detail = l.device_status()
             if code != 0:
                 raise RuntimeError("device status %d detail %d" % (code, detail))
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            step(sere)
+            step_fn()
             stream.synchronize()
             with torch.cuda.graph(g, stream=stream):
-                step(sere)
+                step_fn()
             for _ in range(args.warmup):
                 g.replay()
         torch.cuda.synchronize()
@@ -613,8 +620,9 @@ def run_stack(args):
     peak, peak_src = load_peaks()
     if rank == 0:
         print(json.dumps({"workload": "decode step over %d MoE layers, batch %d, hidden 2048, 128 experts, top-8, "
-                                      "intermediate 768, %.1f GB of bf16 experts resident; SERE K'=2, rho=0.5, "
-                                      "per-layer similarity and 16 protected experts" % (nl, B, nl * N * EXPERT_BYTES / 1e9),
+                                      "intermediate 768, %.1f GB of bf16 experts resident; SERE K'=2 and K'=1 at "
+                                      "rho=0.5 with per-layer similarity and 16 protected experts, plain top-8, "
+                                      "plain top-2" % (nl, B, nl * N * EXPERT_BYTES / 1e9),
                           "metric": "decode step tokens/s (one CUDA graph per step)", "peak_gbs": peak,
                           "peak_source": peak_src, "residual": "x_{l+1} = x_l + y_l in fp32, cast to bf16 per layer",
                           **res}), flush=True)
