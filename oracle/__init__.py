@@ -60,6 +60,8 @@ def lib():
             L.orc_permute.argtypes = [c_p, c_p, c_i, c_i, c_i, c_i, c_p, c_p, c_p, c_p, c_p]
             L.orc_ffn_combine.argtypes = [c_p, c_i, c_p, c_p, c_p, c_i, c_i, c_i, c_i, c_i, c_p, c_p, c_i, c_i,
                                           c_p, c_i, c_p]
+            c_d = ctypes.c_double
+            L.orc_token_weights.argtypes = [c_p, c_i, c_i, c_i, c_p, c_d, c_d, c_p, c_p, c_p]
             _lib = L
     return _lib
 
@@ -179,6 +181,21 @@ def ffn_combine(x, w_gate, w_up, w_down, ids, gates, k: int, tokens=None, x_dtyp
     _check(lib().orc_ffn_combine(_p(x), x_dtype, _p(w_gate), _p(w_up), _p(w_down), w_dtype, T, H, I, N,
                                  _p(ids), _p(gates), ld, k, _p(tok), len(tok), _p(y)), "ffn_combine")
     return y
+
+
+def token_weights(x: np.ndarray, is_visual: np.ndarray, delta: float = 1.0, eps: float = 1e-6,
+                  x_dtype: int = DT_F32):
+    """[MACS] Eqs. (4)-(5), (7): per-token entropy of Softmax(x_t), the
+    entropy weights w and the effective visual ratio R_v (float64)."""
+    x = np.ascontiguousarray(x)
+    T, H = x.shape
+    vis = np.ascontiguousarray(is_visual, dtype=np.uint8)
+    ent = np.zeros(max(T, 1), dtype=np.float64)
+    w = np.zeros(max(T, 1), dtype=np.float64)
+    rv = np.zeros(1, dtype=np.float64)
+    _check(lib().orc_token_weights(_p(x), x_dtype, T, H, _p(vis), float(delta), float(eps), _p(ent), _p(w),
+                                   _p(rv)), "token_weights")
+    return ent[:T], w[:T], float(rv[0])
 
 
 def layer(L, sere_on: bool, capacity_on: bool = False, tokens=None, renorm_k: int = 0, logits=None):

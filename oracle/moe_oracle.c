@@ -33,6 +33,10 @@
  *                      hand-worked golden case.
  *   orc_permute        pinned: numpy lexsort on (expert, token).
  *   orc_ffn_combine    pinned: dense numpy float64 evaluation of Eq. (1).
+ *   orc_token_weights  pinned: entropy against scipy's entropy of softmax,
+ *                      closed forms (uniform z -> ln D, one raised entry,
+ *                      shift invariance), two-token z-score -> sigmoid(+-delta),
+ *                      text weight 1, delta = 0 -> 1/2, R_v bounds.
  */
 #include <math.h>
 #include <stdint.h>
@@ -481,5 +485,66 @@ int orc_ffn_combine(const void* x, int x_dtype, const void* w_gate, const void* 
     }
     free(xv);
     free(act);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Entropy-weighted token load.  [MACS] 3.2 Eqs. (4)-(5), 3.3 Eq. (7).   */
+/*                                                                      */
+/* For every token t, its feature vector z (the layer's input row,      */
+/* D = H values) gives p = Softmax(z) and the Shannon entropy           */
+/*   H(t) = -sum_d p_d ln p_d = ln Z - (sum_d e_d (z_d - m)) / Z,        */
+/* with m = max z, e_d = exp(z_d - m), Z = sum e_d.  Over the batch's   */
+/* visual tokens: mu = mean H, sigma = population standard deviation    */
+/* (Eq. 4's batch statistics), Htilde = (H - mu) / (sigma + eps).        */
+/* Weights (Eq. 5): w = sigmoid(-delta * Htilde) for visual tokens, 1    */
+/* for text tokens.  Effective visual ratio (Eq. 7):                     */
+/*   R_v = sum_{visual} w / sum_{all} w  (0 for an empty batch).         */
+/* Everything in double.  The entropy is computed for every token; only */
+/* the visual ones enter the statistics.                                */
+/* ------------------------------------------------------------------ */
+int orc_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, double delta, double eps,
+                      double* entropy, double* w, double* r_v) {
+    if (T < 0 || H < 1 || (T > 0 && (x == NULL || is_visual == NULL || entropy == NULL || w == NULL)))
+        return ORC_EINVAL;
+    for (int t = 0; t < T; ++t) {
+        double m = -INFINITY;
+        for (int d = 0; d < H; ++d) {
+            const double z = ld_val(x, x_dtype, (size_t)t * H + d);
+            if (z > m) m = z;
+        }
+        double Z = 0.0, S1 = 0.0;
+        for (int d = 0; d < H; ++d) {
+            const double z = ld_val(x, x_dtype, (size_t)t * H + d) - m;
+            const double e = exp(z);
+            Z += e;
+            S1 += e * z;
+        }
+        entropy[t] = log(Z) - S1 / Z;
+    }
+    int nv = 0;
+    double sum = 0.0;
+    for (int t = 0; t < T; ++t)
+        if (is_visual[t]) {
+            ++nv;
+            sum += entropy[t];
+        }
+    const double mu = nv > 0 ? sum / nv : 0.0;
+    double var = 0.0;
+    for (int t = 0; t < T; ++t)
+        if (is_visual[t]) var += (entropy[t] - mu) * (entropy[t] - mu);
+    const double sigma = nv > 0 ? sqrt(var / nv) : 0.0;
+    double wv = 0.0, wall = 0.0;
+    for (int t = 0; t < T; ++t) {
+        if (is_visual[t]) {
+            const double ht = (entropy[t] - mu) / (sigma + eps);
+            w[t] = 1.0 / (1.0 + exp(delta * ht));
+            wv += w[t];
+        } else {
+            w[t] = 1.0;
+        }
+        wall += w[t];
+    }
+    if (r_v != NULL) *r_v = wall > 0.0 ? wv / wall : 0.0;
     return ORC_OK;
 }
