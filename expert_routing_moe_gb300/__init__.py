@@ -4,10 +4,10 @@ fused in, behind the C ABI of include/moe_gb300.h."""
 from ._abi import (MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_FFN_FUSE_COMBINE, MOE_FFN_ZERO_Y, MOE_OP_DISPATCH,
                    MOE_OP_FFN, MOE_ROUTE_FROM_LOGITS, MOE_ROUTE_RENORM_TOPK, MoeError, SereParams, load,
                    moe_combine, moe_dispatch_capacity, moe_ffn_grouped, moe_reroute_sere, moe_route,
-                   status_string, workspace_size)
+                   moe_token_weights, status_string, workspace_size)
 from .layer import MoELayer
 
 __all__ = ["MoELayer", "SereParams", "MoeError", "load", "moe_route", "moe_reroute_sere", "moe_dispatch_capacity",
-           "moe_ffn_grouped", "moe_combine", "workspace_size", "status_string", "MOE_DTYPE_BF16", "MOE_DTYPE_F32",
-           "MOE_FFN_FUSE_COMBINE", "MOE_FFN_ZERO_Y", "MOE_OP_DISPATCH", "MOE_OP_FFN", "MOE_ROUTE_FROM_LOGITS",
+           "moe_ffn_grouped", "moe_combine", "moe_token_weights", "workspace_size", "status_string",
+           "MOE_DTYPE_BF16", "MOE_DTYPE_F32", "MOE_FFN_FUSE_COMBINE", "MOE_FFN_ZERO_Y", "MOE_OP_DISPATCH", "MOE_OP_FFN", "MOE_ROUTE_FROM_LOGITS",
            "MOE_ROUTE_RENORM_TOPK"]

@@ -42,7 +42,7 @@ class _SereParams(ctypes.Structure):
 
 
 EXPORTS = ["moe_route", "moe_reroute_sere", "moe_dispatch_capacity", "moe_ffn_grouped", "moe_combine",
-           "moe_workspace_size", "moe_status_string"]
+           "moe_token_weights", "moe_workspace_size", "moe_status_string"]
 
 
 def load(path: str = LIB_PATH):
@@ -69,6 +69,8 @@ def load(path: str = LIB_PATH):
             L.moe_ffn_grouped.restype = i
             L.moe_combine.argtypes = [p, p, p, i, i, i, p, p]
             L.moe_combine.restype = i
+            L.moe_token_weights.argtypes = [p, i, i, i, p, f, f, p, p, p, p, p]
+            L.moe_token_weights.restype = i
             L.moe_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
             L.moe_workspace_size.restype = sz
             L.moe_status_string.argtypes = [i, i]
@@ -194,3 +196,13 @@ def moe_combine(rows_out, slot_row, slot_gate, y, stream=None):
     H = y.shape[1]
     rc = load().moe_combine(_ptr(rows_out), _ptr(slot_row), _ptr(slot_gate), T, H, k, _ptr(y), _stream(stream))
     _check(rc, "moe_combine")
+
+
+def moe_token_weights(x, is_visual, entropy, token_w, r_v=None, delta: float = 1.0, eps: float = 1e-6, st=None,
+                      stream=None):
+    """MACS entropy-weighted token load: entropy [T], token_w [T] and R_v [1]
+    (fp32 CUDA tensors) from the token features x [T][H] and is_visual [T] uint8."""
+    T, H = x.shape
+    rc = load().moe_token_weights(_ptr(x), _dtype_code(x), T, H, _ptr(is_visual), float(delta), float(eps),
+                                  _ptr(entropy), _ptr(token_w), _ptr(r_v), _ptr(st), _stream(stream))
+    _check(rc, "moe_token_weights")

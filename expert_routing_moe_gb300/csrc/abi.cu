@@ -131,6 +131,20 @@ moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const
                                           active, flags, out, workspace, st, s));
 }
 
+moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
+                               float eps, float* entropy, float* token_w, float* r_v, moe_dev_status* st,
+                               void* stream) {
+    if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
+    if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !(delta == delta) || delta - delta != 0.f) return MOE_ERR_INVALID_ARG;   // eps > 0, delta finite
+    if (T == 0) return MOE_OK;
+    if (x == nullptr || is_visual == nullptr || entropy == nullptr || token_w == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x)) return MOE_ERR_INVALID_ARG;
+    if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    return from_cuda(moe::launch_token_weights(x, x_dtype, T, H, is_visual, delta, eps, entropy, token_w, r_v, st,
+                                               as_stream(stream)));
+}
+
 moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const float* slot_gate, int T, int H, int k,
                          float* y, void* stream) {
     if (T < 0 || H < 1 || k < 1 || k > MOE_MAX_RANKS) return MOE_ERR_INVALID_ARG;

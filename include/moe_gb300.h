@@ -15,6 +15,9 @@
  *                                weighted capacity with overflow reroute / drop
  *               moe_ffn_grouped  grouped SwiGLU expert FFN, combine fused in
  *               moe_combine      weighted combine of per-row expert outputs
+ *               moe_token_weights
+ *                                entropy-weighted token load for the capacity
+ *                                dispatch, and the effective visual ratio
  *
  * Conventions for every entry point
  *  - Pointers named "host" are host memory; every other pointer is device
@@ -241,6 +244,31 @@ moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const
                              const int32_t* row_token, const float* row_gate, const int32_t* active,
                              uint32_t flags, float* out, void* workspace, size_t ws_bytes,
                              moe_dev_status* st, void* stream);
+
+/*
+ * Entropy-weighted token load ("MACS" sec. 3.2 Eqs. (4)-(5) and sec. 3.3
+ * Eq. (7)): the per-token load weights that moe_dispatch_capacity takes as
+ * token_w, and the batch's effective visual ratio.
+ *
+ *   x          [T][H] token features z (the layer's input rows), BF16 or F32,
+ *              16-byte aligned, H % 8 == 0
+ *   is_visual  [T] uint8, nonzero = visual token, 0 = text token
+ *   delta      sensitivity of the entropy-to-weight map (finite)
+ *   eps        added to the standard deviation (> 0)
+ *   entropy    [T] fp32 out: Shannon entropy (natural log) of Softmax(z), every token
+ *   token_w    [T] fp32 out: sigmoid(-delta * (H - mu) / (sigma + eps)) for
+ *              visual tokens, where mu and sigma are the mean and population
+ *              standard deviation of the visual tokens' entropies in this
+ *              batch; 1 for text tokens
+ *   r_v        [1] fp32 out (may be NULL): sum of visual weights / sum of all
+ *              weights (0 when T == 0)
+ * Entropies are computed in fp32 (one warp per token); the statistics, the
+ * weights and R_v in double, in a fixed order, so results are reproducible.
+ * A non-finite feature sets MOE_DEV_NONFINITE (detail = token) in st.
+ */
+moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
+                               float eps, float* entropy, float* token_w, float* r_v, moe_dev_status* st,
+                               void* stream);
 
 /*
  * Weighted combine ("MACS" Eq. (1)): y[t] = sum_r gate[t][r] * rows_out[slot_row[t][r]]

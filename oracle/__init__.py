@@ -56,7 +56,10 @@ def lib():
             L.orc_fixed_weight.argtypes = [c_f]
             L.orc_capacity_value.restype = ctypes.c_int64
             L.orc_capacity_value.argtypes = [ctypes.c_int64, c_i, c_f, c_i]
-            L.orc_capacity.argtypes = [c_p, c_p, c_i, c_i, c_i, c_i, c_i, c_p, c_f, c_p, c_p, c_p, c_p, c_p]
+            L.orc_capacity.argtypes = [c_p, c_p, c_i, c_i, c_i, c_i, c_i, c_p, c_f, c_p, c_p, c_p, c_p, c_p, c_p,
+                                       c_f]
+            L.orc_capacity_expert.restype = ctypes.c_int64
+            L.orc_capacity_expert.argtypes = [ctypes.c_int64, c_i, c_f, c_i, c_i, c_f]
             L.orc_permute.argtypes = [c_p, c_p, c_i, c_i, c_i, c_i, c_p, c_p, c_p, c_p, c_p]
             L.orc_ffn_combine.argtypes = [c_p, c_i, c_p, c_p, c_p, c_i, c_i, c_i, c_i, c_i, c_p, c_p, c_i, c_i,
                                           c_p, c_i, c_p]
@@ -133,20 +136,30 @@ def capacity_value(S: int, k: int, gamma: float, N: int) -> int:
     return int(lib().orc_capacity_value(int(S), k, float(gamma), N))
 
 
-def capacity(ids: np.ndarray, gates: np.ndarray, N: int, k: int, R: int, token_w, gamma: float):
-    """Capacity dispatch.  Returns (out_ids [T][k], out_gates [T][k], status [T][k], load [N], C)."""
+def capacity(ids: np.ndarray, gates: np.ndarray, N: int, k: int, R: int, token_w, gamma: float,
+             bias=None, r_v: float = 0.5):
+    """Capacity dispatch.  Returns (out_ids [T][k], out_gates [T][k], status [T][k], load [N], C) with C the
+    static capacity.  With `bias` ([N] int8 modality bias m_j) each expert's capacity is
+    capacity_expert(S, k, gamma, N, m_j, r_v) instead."""
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     gates = np.ascontiguousarray(gates, dtype=np.float32)
     T, ld = ids.shape
     tw = None if token_w is None else np.ascontiguousarray(token_w, dtype=np.float32)
+    bs = None if bias is None else np.ascontiguousarray(bias, dtype=np.int8)
     out_ids = np.zeros((T, k), dtype=np.int32)
     out_gates = np.zeros((T, k), dtype=np.float32)
     status = np.zeros((T, k), dtype=np.uint8)
     load = np.zeros(N, dtype=np.int64)
     cap = np.zeros(1, dtype=np.int64)
     _check(lib().orc_capacity(_p(ids), _p(gates), ld, T, N, k, R, _p(tw), float(gamma), _p(out_ids),
-                              _p(out_gates), _p(status), _p(load), _p(cap)), "capacity")
+                              _p(out_gates), _p(status), _p(load), _p(cap), _p(bs), float(r_v)), "capacity")
     return out_ids, out_gates, status, load, int(cap[0])
+
+
+def capacity_expert(S: int, k: int, gamma: float, N: int, m: int, r_v: float) -> int:
+    """Per-expert capacity (a reading of the truncated [MACS] 3.3):
+    floor(c * (1 + m (r_v - 1/2))) with c the unfloored static capacity."""
+    return int(lib().orc_capacity_expert(int(S), k, float(gamma), N, int(m), float(r_v)))
 
 
 def permute(ids: np.ndarray, gates: np.ndarray, N: int, k: int):

@@ -30,7 +30,11 @@
  *                      declarative property check, hand-worked golden cases.
  *   orc_capacity       pinned: w==1 reduces to Eq. (3) count capacity, huge
  *                      gamma reduces to plain dispatch, declarative brute force,
- *                      hand-worked golden case.
+ *                      hand-worked golden case.  Per-expert capacity (a
+ *                      reading of the truncated [MACS] 3.3): m = 0 or
+ *                      R_v = 1/2 reduce to the static case, unit weights give
+ *                      floor(gamma T k / N (1 + m (R_v - 1/2))) tokens (exact
+ *                      rationals), declarative brute force per expert.
  *   orc_permute        pinned: numpy lexsort on (expert, token).
  *   orc_ffn_combine    pinned: dense numpy float64 evaluation of Eq. (1).
  *   orc_token_weights  pinned: entropy against scipy's entropy of softmax,
@@ -308,12 +312,31 @@ int64_t orc_capacity_value(int64_t S, int k, float gamma, int N) {
     return (int64_t)floor(((double)S * (double)k) * (double)gamma / (double)N);
 }
 
+/* Per-expert capacity.  [MACS] 3.3 groups experts by modality (m_j = +1
+ * visual, -1 text, 0 shared) and scales their capacity with the batch's
+ * effective visual ratio R_v (Eq. 7); the page text stops before the
+ * scaling formula.  Reading: C_j = floor(c * (1 + m_j * (R_v - 1/2))) with
+ * c = ((double)S * k) * gamma / N the unfloored static capacity, so that
+ * m_j = 0 (or R_v = 1/2) gives the static C and a modality's experts get up
+ * to half as much again when the batch leans towards it.  Each operation
+ * is rounded on its own, in this order. */
+int64_t orc_capacity_expert(int64_t S, int k, float gamma, int N, int m, float r_v) {
+    const double c = ((double)S * (double)k) * (double)gamma / (double)N;
+    const double scale = 1.0 + (double)m * ((double)r_v - 0.5);
+    return (int64_t)floor(c * scale);
+}
+
 int orc_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, int k, int R,
                  const float* token_w, float gamma, int32_t* out_ids, float* out_gates,
-                 uint8_t* status, int64_t* load, int64_t* cap) {
+                 uint8_t* status, int64_t* load, int64_t* cap, const int8_t* bias, float r_v) {
     if (!ids || !gates || !out_ids || !out_gates || !status || !load || T < 0 || N <= 0 || k <= 0 ||
         R < k || ld < R || !(gamma > 0.0f))
         return ORC_EINVAL;
+    if (bias != NULL) {
+        if (!(r_v >= 0.0f && r_v <= 1.0f)) return ORC_EINVAL;
+        for (int e = 0; e < N; ++e)
+            if (bias[e] < -1 || bias[e] > 1) return ORC_EINVAL;
+    }
     int64_t* wq = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1));
     orc_pair* buf = (orc_pair*)malloc(sizeof(orc_pair) * (size_t)(T > 0 ? T : 1));
     int32_t* pend = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
@@ -327,6 +350,9 @@ int orc_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, i
     }
     int64_t C = orc_capacity_value(S, k, gamma, N);
     if (cap) *cap = C;
+    int64_t* Ce = (int64_t*)malloc(sizeof(int64_t) * (size_t)N);
+    if (!Ce) { free(wq); free(buf); free(pend); return ORC_ENOMEM; }
+    for (int e = 0; e < N; ++e) Ce[e] = bias ? orc_capacity_expert(S, k, gamma, N, bias[e], r_v) : C;
     const uint8_t PENDING = 255;
     for (int t = 0; t < T; ++t)
         for (int r = 0; r < k; ++r) {
@@ -350,7 +376,7 @@ int orc_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, i
         int open = 1;
         for (int i = 0; i < n; ++i) {
             int t = buf[i].token, r = buf[i].slot;
-            if (open && cum + wq[t] <= C) {
+            if (open && cum + wq[t] <= Ce[e]) {
                 cum += wq[t];
                 status[(size_t)t * k + r] = ORC_SLOT_KEPT;
             } else {
@@ -380,7 +406,7 @@ int orc_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, i
             int open = 1;
             for (int j = 0; j < n; ++j) {
                 int t = buf[j].token, r = buf[j].slot;
-                if (open && load[e] + cum + wq[t] <= C) {
+                if (open && load[e] + cum + wq[t] <= Ce[e]) {
                     cum += wq[t];
                     status[(size_t)t * k + r] = ORC_SLOT_REROUTED;
                     out_ids[(size_t)t * k + r] = e;
@@ -401,6 +427,7 @@ int orc_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, i
     free(wq);
     free(buf);
     free(pend);
+    free(Ce);
     return ORC_OK;
 }
 

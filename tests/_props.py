@@ -79,6 +79,7 @@ def capacity_check(ids, gates, token_w, k, R, gamma, N, out_ids, out_gates, stat
     pending slot to its rank-(k+i) expert, and each expert admits exactly the
     proposals whose cumulative weight on top of its load stays within C."""
     T = ids.shape[0]
+    Ce = (lambda e: int(C[e])) if np.ndim(C) > 0 else (lambda e: int(C))   # per-expert or static capacity
     wq = [fixed(float(token_w[t]) if token_w is not None else 1.0) for t in range(T)]
     # phase 1
     load_ref = np.zeros(N, dtype=np.int64)
@@ -88,7 +89,7 @@ def capacity_check(ids, gates, token_w, k, R, gamma, N, out_ids, out_gates, stat
         pairs.sort(key=lambda p: (-float(gates[p[0], p[1]]), p[0]))
         for j, (t, r) in enumerate(pairs):
             need = sum(wq[tt] for tt, _ in pairs[: j + 1])
-            if need <= C:
+            if need <= Ce(e):
                 assert status[t, r] == 0 and out_ids[t, r] == e, ("phase1 admit", t, r)
                 load_ref[e] += wq[t]
             else:
@@ -107,7 +108,7 @@ def capacity_check(ids, gates, token_w, k, R, gamma, N, out_ids, out_gates, stat
             adm = 0
             for j, (t, r) in enumerate(lst):
                 need = base + sum(wq[tt] for tt, _ in lst[: j + 1])
-                if need <= C:
+                if need <= Ce(e):
                     assert status[t, r] == 1 and out_ids[t, r] == e, ("round admit", i, t, r)
                     adm += wq[t]
                     pending[t].remove(r)

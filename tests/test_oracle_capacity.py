@@ -124,3 +124,92 @@ def test_invalid_arguments():
         oracle.capacity(ids, g, 4, 2, 3, None, 0.0)        # gamma must be > 0
     with pytest.raises(RuntimeError):
         oracle.capacity(ids, g, 4, 2, 3, np.array([1.0, -1.0], dtype=np.float32), 1.0)  # negative weight
+
+
+# ---- per-expert capacity: a reading of the truncated [MACS] 3.3 ----------------
+def test_expert_capacity_neutral_cases_equal_static():
+    """m_j = 0 for every expert, or R_v = 1/2, must give exactly the static dispatch."""
+    rng = np.random.default_rng(21)
+    for _ in range(40):
+        T, N = int(rng.integers(1, 30)), int(rng.integers(2, 10))
+        k = int(rng.integers(1, min(N, 3) + 1))
+        R = int(rng.integers(k, min(N, 8) + 1))
+        ids, gates = _random_case(rng, T, N, k, R)
+        w = rng.beta(2, 5, size=T).astype(np.float32)
+        g = float(rng.choice([0.5, 1.0, 1.25]))
+        ref = oracle.capacity(ids, gates, N, k, R, w, g)
+        zero = oracle.capacity(ids, gates, N, k, R, w, g, bias=np.zeros(N, np.int8), r_v=float(rng.random()))
+        half = oracle.capacity(ids, gates, N, k, R, w, g, bias=rng.integers(-1, 2, N).astype(np.int8), r_v=0.5)
+        for out in (zero, half):
+            for a, b in zip(ref, out):
+                assert np.array_equal(np.asarray(a), np.asarray(b))
+
+
+def test_expert_capacity_unit_weights_count_closed_form():
+    """With w = 1 each expert admits min(n_e, floor(gamma T k / N * (1 + m (R_v - 1/2)))) of its
+    (gate desc, token asc) candidates; the bound is evaluated in exact rationals at parameters
+    whose product is at least 1e-3 away from an integer."""
+    from fractions import Fraction
+    rng = np.random.default_rng(22)
+    checked = 0
+    while checked < 40:
+        T, N = int(rng.integers(4, 40)), int(rng.integers(2, 10))
+        k = int(rng.integers(1, min(N, 3) + 1))
+        g = float(np.float32(rng.choice([0.5, 0.75, 1.25])))
+        r_v = float(np.float32(rng.choice([0.125, 0.25, 0.625, 0.875])))
+        bias = rng.integers(-1, 2, N).astype(np.int8)
+        ids, gates = _random_case(rng, T, N, k, k, gate_levels=8)
+        caps = []
+        ok = True
+        for e in range(N):
+            c = Fraction(g) * T * k / N * (1 + int(bias[e]) * (Fraction(r_v) - Fraction(1, 2)))
+            if abs(c - round(c)) < Fraction(1, 1000):
+                ok = False
+            caps.append(math.floor(c))
+        if not ok:
+            continue
+        oi, og, st, load, C = oracle.capacity(ids, gates, N, k, k, None, g, bias=bias, r_v=r_v)
+        for e in range(N):
+            pairs = [(t, r) for t in range(T) for r in range(k) if ids[t, r] == e]
+            pairs.sort(key=lambda p: (-float(gates[p]), p[0]))
+            admitted = [p for p in pairs if st[p] == 0]
+            assert admitted == pairs[: min(len(pairs), caps[e])]
+            assert oracle.capacity_expert(T * Q, k, g, N, int(bias[e]), r_v) // Q == caps[e]
+        checked += 1
+
+
+def test_expert_capacity_monotone_in_r_v():
+    S, k, g, N = 4096 * Q, 8, 1.25, 128
+    vis = [oracle.capacity_expert(S, k, g, N, +1, r) for r in (0.0, 0.25, 0.5, 0.75, 1.0)]
+    txt = [oracle.capacity_expert(S, k, g, N, -1, r) for r in (0.0, 0.25, 0.5, 0.75, 1.0)]
+    base = oracle.capacity_value(S, k, g, N)
+    assert vis == sorted(vis) and txt == sorted(txt, reverse=True)
+    assert vis[2] == txt[2] == base
+    assert vis[4] == txt[0] and vis[0] == txt[4]
+
+
+def test_expert_capacity_declarative_rules():
+    rng = np.random.default_rng(23)
+    for it in range(150):
+        T, N = int(rng.integers(1, 16)), int(rng.integers(2, 9))
+        k = int(rng.integers(1, min(N, 3) + 1))
+        R = int(rng.integers(k, min(N, 10) + 1))
+        ids, gates = _random_case(rng, T, N, k, R, gate_levels=(6 if it % 3 == 0 else None))
+        w = rng.beta(2, 5, size=T).astype(np.float32)
+        w[rng.random(T) < 0.3] = 1.0
+        g = float(rng.choice([0.5, 0.8, 1.0, 1.25]))
+        bias = rng.integers(-1, 2, N).astype(np.int8)
+        r_v = float(np.float32(rng.random()))
+        oi, og, st, load, C = oracle.capacity(ids, gates, N, k, R, w, g, bias=bias, r_v=r_v)
+        S = sum(oracle.fixed_weight(float(v)) for v in w)
+        Ce = np.array([oracle.capacity_expert(S, k, g, N, int(bias[e]), r_v) for e in range(N)])
+        capacity_check(ids, gates, w, k, R, g, N, oi, og, st, load, Ce, oracle.fixed_weight)
+
+
+def test_expert_capacity_rejects_bad_bias_or_ratio():
+    ids = np.zeros((2, 3), dtype=np.int32)
+    g = np.zeros((2, 3), dtype=np.float32)
+    with pytest.raises(Exception):
+        oracle.capacity(ids, g, 4, 2, 3, None, 1.0, bias=np.array([0, 2, 0, 0], np.int8), r_v=0.5)
+    with pytest.raises(Exception):
+        oracle.capacity(ids, g, 4, 2, 3, None, 1.0, bias=np.zeros(4, np.int8), r_v=1.5)
