@@ -59,11 +59,11 @@ def load(path: str = LIB_PATH):
             L.moe_route.restype = i
             L.moe_reroute_sere.argtypes = [p, p, i, i, i, i, p, p, p]
             L.moe_reroute_sere.restype = i
-            L.moe_dispatch_capacity.argtypes = [p, p, i, i, i, i, i, p, f, p, p, p, p, p, p, p, p, p, p, p, p, sz,
-                                                p, p]
+            L.moe_dispatch_capacity.argtypes = [p, p, i, i, i, i, i, p, f, p, p, p, p, p, p, p, p, p, p, p, p, p,
+                                                p, sz, p, p]
             L.moe_dispatch_capacity.restype = i
             L.moe_dispatch_capacity_static.argtypes = [p, p, i, i, i, i, i, p, f, p, p, p, p, p, p, p, p, p, p,
-                                                       p, p, p]
+                                                       p, p, p, p, p]
             L.moe_dispatch_capacity_static.restype = i
             L.moe_ffn_grouped.argtypes = [p, i, p, p, p, i, i, i, i, i, p, p, p, p, u32, p, p, sz, p, p]
             L.moe_ffn_grouped.restype = i
@@ -155,11 +155,13 @@ def moe_reroute_sere(ids, gates, N: int, k: int, sere: SereParams, st=None, stre
 
 def moe_dispatch_capacity(ids, gates, N: int, k: int, R: int, counts, offsets, row_token, row_gate, active,
                           workspace, token_w=None, capacity_factor: float = 0.0, out_ids=None, out_gates=None,
-                          slot_row=None, slot_status=None, load_q=None, cap_q=None, st=None, stream=None):
+                          slot_row=None, slot_status=None, load_q=None, cap_q=None, st=None, stream=None,
+                          modality_bias=None, r_v=None):
     T, ld = ids.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load().moe_dispatch_capacity(_ptr(ids), _ptr(gates), ld, T, N, k, R, _ptr(token_w),
-                                      float(capacity_factor), _ptr(counts), _ptr(offsets), _ptr(row_token),
+                                      float(capacity_factor), _ptr(modality_bias), _ptr(r_v), _ptr(counts),
+                                      _ptr(offsets), _ptr(row_token),
                                       _ptr(row_gate), _ptr(active), _ptr(out_ids), _ptr(out_gates),
                                       _ptr(slot_row), _ptr(slot_status), _ptr(load_q), _ptr(cap_q),
                                       _ptr(workspace), ws_bytes, _ptr(st), _stream(stream))
@@ -168,12 +170,14 @@ def moe_dispatch_capacity(ids, gates, N: int, k: int, R: int, counts, offsets, r
 
 def moe_dispatch_capacity_static(ids, gates, N: int, k: int, R: int, counts, offsets, row_token, row_gate, active,
                                  token_w=None, capacity_factor: float = 0.0, out_ids=None, out_gates=None,
-                                 slot_row=None, slot_status=None, load_q=None, cap_q=None, st=None, stream=None):
+                                 slot_row=None, slot_status=None, load_q=None, cap_q=None, st=None, stream=None,
+                                 modality_bias=None, r_v=None):
     """moe_dispatch_capacity without a workspace: the library's own fixed
     device scratch is used (T <= 2048; calls on one device must not overlap)."""
     T, ld = ids.shape
     rc = load().moe_dispatch_capacity_static(_ptr(ids), _ptr(gates), ld, T, N, k, R, _ptr(token_w),
-                                             float(capacity_factor), _ptr(counts), _ptr(offsets), _ptr(row_token),
+                                             float(capacity_factor), _ptr(modality_bias), _ptr(r_v), _ptr(counts),
+                                             _ptr(offsets), _ptr(row_token),
                                              _ptr(row_gate), _ptr(active), _ptr(out_ids), _ptr(out_gates),
                                              _ptr(slot_row), _ptr(slot_status), _ptr(load_q), _ptr(cap_q), _ptr(st),
                                              _stream(stream))

@@ -73,7 +73,8 @@ size_t moe_workspace_size(int op, int T, int H, int I, int N, int k, int R, int 
 }
 
 moe_status_t moe_dispatch_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, int k, int R,
-                                   const float* token_w, float capacity_factor, int32_t* counts, int32_t* offsets,
+                                   const float* token_w, float capacity_factor, const int8_t* modality_bias,
+                                   const float* r_v, int32_t* counts, int32_t* offsets,
                                    int32_t* row_token, float* row_gate, int32_t* active, int32_t* out_ids,
                                    float* out_gates, int32_t* slot_row, uint8_t* slot_status, int64_t* load_q,
                                    int64_t* cap_q, void* workspace, size_t ws_bytes, moe_dev_status* st,
@@ -83,6 +84,7 @@ moe_status_t moe_dispatch_capacity(const int32_t* ids, const float* gates, int l
         ((ids == nullptr || gates == nullptr || row_token == nullptr || row_gate == nullptr) && T > 0))
         return MOE_ERR_INVALID_ARG;
     if (capacity_factor != capacity_factor) return MOE_ERR_INVALID_ARG;
+    if (modality_bias != nullptr && (r_v == nullptr || !(capacity_factor > 0.f))) return MOE_ERR_INVALID_ARG;
     const bool capped = capacity_factor > 0.f;
     if (capped) {
         if (R < k || R > MOE_MAX_RANKS || R > N || ld < R) return MOE_ERR_INVALID_ARG;
@@ -93,9 +95,9 @@ moe_status_t moe_dispatch_capacity(const int32_t* ids, const float* gates, int l
     const size_t need = moe::dispatch_workspace(T, N, k, R, capped);
     if (need > 0 && (workspace == nullptr || ws_bytes < need)) return MOE_ERR_WORKSPACE;
     if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
-    return from_cuda(moe::launch_dispatch(ids, gates, ld, T, N, k, R, token_w, capacity_factor, counts, offsets,
-                                          row_token, row_gate, active, out_ids, out_gates, slot_row, slot_status,
-                                          load_q, cap_q, workspace, st, as_stream(stream)));
+    return from_cuda(moe::launch_dispatch(ids, gates, ld, T, N, k, R, token_w, capacity_factor, modality_bias, r_v,
+                                          counts, offsets, row_token, row_gate, active, out_ids, out_gates, slot_row,
+                                          slot_status, load_q, cap_q, workspace, st, as_stream(stream)));
 }
 
 moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const void* w_up, const void* w_down,

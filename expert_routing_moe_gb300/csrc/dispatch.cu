@@ -39,6 +39,8 @@ struct DispatchWs {
     int32_t* wids;        // [T][k]
     float* wgates;        // [T][k]
     size_t zero_bytes;    // bytes from S to the end of cnt2 (cleared per call)
+    const int8_t* bias;   // [N] modality bias m_j, or null (static capacity)
+    const float* r_v;     // [1] effective visual ratio, with bias
 };
 
 static size_t carve(DispatchWs* w, void* base, int T, int N, int k, bool capped) {
@@ -192,6 +194,33 @@ __device__ __forceinline__ long long capacity_value(unsigned long long S, int k,
     return static_cast<long long>(floor(__ddiv_rn(b, static_cast<double>(N))));
 }
 
+// Capacity of expert e.  "MACS" sec. 3.3 scales each expert's capacity by its
+// modality (m_e = +1 visual, -1 text, 0 shared) and the batch's effective
+// visual ratio R_v; the page stops before the formula.  Reading:
+// C_e = floor(c * (1 + m_e * (R_v - 1/2))), c the unfloored static capacity,
+// each operation rounded on its own in this order.  An out-of-range bias or
+// ratio is reported and treated as m_e = 0.
+__device__ __forceinline__ long long capacity_of(const DispatchWs& w, int e, int k, float gamma, int N,
+                                                 moe_dev_status* st) {
+    const unsigned long long S = *w.S;
+    if (w.bias == nullptr) return capacity_value(S, k, gamma, N);
+    const int m = w.bias[e];
+    const float rv = *w.r_v;
+    if (m < -1 || m > 1) {
+        report(st, MOE_DEV_BAD_INDEX, m);
+        return capacity_value(S, k, gamma, N);
+    }
+    if (!(rv >= 0.f && rv <= 1.f)) {
+        report(st, MOE_DEV_NONFINITE, e);
+        return capacity_value(S, k, gamma, N);
+    }
+    const double c = __ddiv_rn(__dmul_rn(__dmul_rn(static_cast<double>(S), static_cast<double>(k)),
+                                         static_cast<double>(gamma)),
+                               static_cast<double>(N));
+    const double scale = __dadd_rn(1.0, __dmul_rn(static_cast<double>(m), __dsub_rn(static_cast<double>(rv), 0.5)));
+    return static_cast<long long>(floor(__dmul_rn(c, scale)));
+}
+
 // Phase-1 bucketing: fixed-point weights, total S, copies of the slots, and
 // each slot appended to its expert's bucket (order fixed later by the keys).
 // S is summed per block (one global atomic per block); a token's k slots are
@@ -294,7 +323,7 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
 
 __global__ void __launch_bounds__(1024) cap_admit_kernel(const float* __restrict__ gates, int ld, int T, int N,
                                                          int k, float gamma, const float* __restrict__ token_w,
-                                                         int round, DispatchWs w) {
+                                                         int round, DispatchWs w, moe_dev_status* st) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ unsigned long long keys[];       // [P2(T)] candidate keys, then [T] float weights
@@ -309,7 +338,7 @@ __global__ void __launch_bounds__(1024) cap_admit_kernel(const float* __restrict
     const int e = blockIdx.x;
     const int n = min((round < 0) ? w.cnt1[e] : w.cnt2[e], T);
     const uint32_t* bucket = ((round < 0) ? w.bucket1 : w.bucket2) + static_cast<size_t>(e) * T;
-    const long long C = capacity_value(*w.S, k, gamma, N);
+    const long long C = capacity_of(w, e, k, gamma, N, st);
     const long long base = (round < 0) ? 0ll : w.load[e];
     auto admit = [&](uint32_t tr) {
         const size_t so = static_cast<size_t>(tr >> 4) * k + (tr & 15u);
@@ -521,13 +550,16 @@ __global__ void cap_finalize_kernel(int T, int N, int k, DispatchWs w, uint8_t* 
 }
 
 cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int T, int N, int k, int R,
-                            const float* token_w, float capacity_factor, int32_t* counts, int32_t* offsets,
-                            int32_t* row_token, float* row_gate, int32_t* active, int32_t* out_ids,
-                            float* out_gates, int32_t* slot_row, uint8_t* slot_status, int64_t* load_q,
-                            int64_t* cap_q, void* ws, moe_dev_status* st, cudaStream_t s) {
+                            const float* token_w, float capacity_factor, const int8_t* modality_bias,
+                            const float* r_v, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                            float* row_gate, int32_t* active, int32_t* out_ids, float* out_gates,
+                            int32_t* slot_row, uint8_t* slot_status, int64_t* load_q, int64_t* cap_q, void* ws,
+                            moe_dev_status* st, cudaStream_t s) {
     const bool capped = capacity_factor > 0.f;
     DispatchWs w{};
     carve(&w, ws, T, N, k, capped);
+    w.bias = modality_bias;
+    w.r_v = r_v;
     if (!capped) {
         if (T == 0) {
             cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
@@ -552,14 +584,14 @@ cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int 
                                    static_cast<int>(smem));
         if (err != cudaSuccess) return err;
         err = launch_pdl(cap_admit_kernel, dim3(N), dim3(1024), smem, s, gates, ld, T, N, k, capacity_factor,
-                         token_w, -1, w);
+                         token_w, -1, w, st);
         if (err != cudaSuccess) return err;
         for (int i = 0; i + k < R; ++i) {
             cudaMemsetAsync(w.cnt2, 0, sizeof(int32_t) * N, s);
             err = launch_pdl(cap_offer_kernel, dim3((T + tb - 1) / tb), dim3(tb), 0, s, ids, ld, T, N, k, i, w);
             if (err != cudaSuccess) return err;
             err = launch_pdl(cap_admit_kernel, dim3(N), dim3(1024), smem, s, gates, ld, T, N, k, capacity_factor,
-                             token_w, i, w);
+                             token_w, i, w, st);
             if (err != cudaSuccess) return err;
         }
     }

@@ -37,6 +37,7 @@ moe_status_t scratch_for_current_device(void** out) {
 
 extern "C" moe_status_t moe_dispatch_capacity_static(const int32_t* ids, const float* gates, int ld, int T, int N,
                                                      int k, int R, const float* token_w, float capacity_factor,
+                                                     const int8_t* modality_bias, const float* r_v,
                                                      int32_t* counts, int32_t* offsets, int32_t* row_token,
                                                      float* row_gate, int32_t* active, int32_t* out_ids,
                                                      float* out_gates, int32_t* slot_row, uint8_t* slot_status,
@@ -52,7 +53,7 @@ extern "C" moe_status_t moe_dispatch_capacity_static(const int32_t* ids, const f
     if (s != MOE_OK) return s;
     // The rest of the checks, and the kernels, are those of moe_dispatch_capacity;
     // it clears the parts of the scratch that must start at zero on every call.
-    return moe_dispatch_capacity(ids, gates, ld, T, N, k, R, token_w, capacity_factor, counts, offsets, row_token,
-                                 row_gate, active, out_ids, out_gates, slot_row, slot_status, load_q, cap_q, scratch,
-                                 sizeof(g_dispatch_scratch), st, stream);
+    return moe_dispatch_capacity(ids, gates, ld, T, N, k, R, token_w, capacity_factor, modality_bias, r_v, counts,
+                                 offsets, row_token, row_gate, active, out_ids, out_gates, slot_row, slot_status,
+                                 load_q, cap_q, scratch, sizeof(g_dispatch_scratch), st, stream);
 }

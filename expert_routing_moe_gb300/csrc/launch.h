@@ -43,10 +43,11 @@ constexpr int kSereMaxT = 4096;
 // ---- dispatch (dispatch.cu) ----
 size_t dispatch_workspace(int T, int N, int k, int R, bool capped);
 cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int T, int N, int k, int R,
-                            const float* token_w, float capacity_factor, int32_t* counts, int32_t* offsets,
-                            int32_t* row_token, float* row_gate, int32_t* active, int32_t* out_ids,
-                            float* out_gates, int32_t* slot_row, uint8_t* slot_status, int64_t* load_q,
-                            int64_t* cap_q, void* ws, moe_dev_status* st, cudaStream_t s);
+                            const float* token_w, float capacity_factor, const int8_t* modality_bias,
+                            const float* r_v, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                            float* row_gate, int32_t* active, int32_t* out_ids, float* out_gates,
+                            int32_t* slot_row, uint8_t* slot_status, int64_t* load_q, int64_t* cap_q, void* ws,
+                            moe_dev_status* st, cudaStream_t s);
 constexpr int kCapacityMaxT = 16384;
 
 // ---- FFN (ffn_simt.cu, ffn_tc.cu) ----

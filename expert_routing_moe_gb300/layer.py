@@ -16,7 +16,8 @@ class MoELayer:
     def __init__(self, w_router: torch.Tensor, w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
                  k: int, max_tokens: int, sim: Optional[torch.Tensor] = None, protect: Optional[torch.Tensor] = None,
                  k_primary: int = 2, rho: float = 0.5, R: Optional[int] = None, capacity_factor: float = 0.0,
-                 renorm: bool = False):
+                 renorm: bool = False, modality_bias: Optional[torch.Tensor] = None,
+                 r_v: Optional[torch.Tensor] = None):
         dev = w_gate.device
         self.w_router, self.w_gate, self.w_up, self.w_down = w_router, w_gate, w_up, w_down
         self.N, self.I, self.H = w_gate.shape
@@ -26,6 +27,8 @@ class MoELayer:
         self.sim, self.protect = sim, protect
         self.k_primary, self.rho = k_primary, rho
         self.capacity_factor = capacity_factor
+        # per-expert capacity: m_j in {+1, -1, 0} [N] int8 and the batch's visual ratio [1] fp32
+        self.modality_bias, self.r_v = modality_bias, r_v
         self.flags = abi.MOE_ROUTE_RENORM_TOPK if renorm else 0
         T, N, R, H = max_tokens, self.N, self.R, self.H
         i32, f32 = torch.int32, torch.float32
@@ -68,7 +71,9 @@ class MoELayer:
                                   self.capacity_factor, self.out_ids[:T], self.out_gates[:T], None,
                                   self.slot_status[:T] if self.capacity_factor > 0 else None,
                                   self.load_q if self.capacity_factor > 0 else None,
-                                  self.cap_q if self.capacity_factor > 0 else None, self.status, stream)
+                                  self.cap_q if self.capacity_factor > 0 else None, self.status, stream,
+                                  modality_bias=self.modality_bias if self.capacity_factor > 0 else None,
+                                  r_v=self.r_v if self.capacity_factor > 0 else None)
 
     def ffn(self, x: torch.Tensor, stream=None, accumulate_into: Optional[torch.Tensor] = None):
         """y = sum_j G_j E_j(x) into the layer's buffer, or added to

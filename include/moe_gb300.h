@@ -153,7 +153,18 @@ moe_status_t moe_reroute_sere(int32_t* ids, float* gates, int ld, int T, int N, 
  * reroute locally, else drop).
  *
  *   ids, gates   [T][ld]  ranked routing (ld >= R when capped, >= k otherwise)
- *   token_w      [T] fp32 >= 0, or NULL (all 1); capped mode only
+ *   token_w      [T] fp32 >= 0, or NULL (all 1); capped mode only (e.g. the
+ *                      entropy weights of moe_token_weights)
+ *   modality_bias [N] int8, or NULL: per-expert capacity ("MACS" sec. 3.3:
+ *                      m_j = +1 visual, -1 text, 0 shared expert).  The page
+ *                      stops before its scaling formula; this library reads it
+ *                      as C_j = floor(c * (1 + m_j * (R_v - 1/2))) with
+ *                      c = ((double)S * k) * capacity_factor / N unfloored, so
+ *                      m_j = 0 or R_v = 1/2 keep the static C.  Capped mode only.
+ *   r_v          [1] fp32 device scalar in [0, 1] (the effective visual ratio of
+ *                      moe_token_weights); required with modality_bias.  A bias
+ *                      outside {-1, 0, 1} or a ratio outside [0, 1] is reported
+ *                      in st and that expert keeps the static C.
  *   counts       [N]      out: rows per expert
  *   offsets      [N+1]    out: exclusive prefix of counts
  *   row_token    [T*k]    out: token of each row, rows ordered by (expert, token)
@@ -164,12 +175,13 @@ moe_status_t moe_reroute_sere(int32_t* ids, float* gates, int ld, int T, int N, 
  *   slot_row     [T][k]   out (may be NULL): row index of each slot, -1 if none
  *   slot_status  [T][k]   out (may be NULL): MOE_SLOT_*; capped mode only
  *   load_q       [N]      out (may be NULL): final weighted load in 2^-24 units
- *   cap_q        [1]      out (may be NULL): C in 2^-24 units
+ *   cap_q        [1]      out (may be NULL): the static C in 2^-24 units
  *   workspace    device scratch of moe_workspace_size(MOE_OP_DISPATCH, ...) bytes
  * Limits: N <= 256, k <= R <= min(16, N); capped mode T <= 16384.
  */
 moe_status_t moe_dispatch_capacity(const int32_t* ids, const float* gates, int ld, int T, int N, int k,
-                                   int R, const float* token_w, float capacity_factor, int32_t* counts,
+                                   int R, const float* token_w, float capacity_factor,
+                                   const int8_t* modality_bias, const float* r_v, int32_t* counts,
                                    int32_t* offsets, int32_t* row_token, float* row_gate, int32_t* active,
                                    int32_t* out_ids, float* out_gates, int32_t* slot_row,
                                    uint8_t* slot_status, int64_t* load_q, int64_t* cap_q, void* workspace,
@@ -205,7 +217,8 @@ moe_status_t moe_dispatch_capacity(const int32_t* ids, const float* gates, int l
 #define MOE_STATIC_DISPATCH_MAX_T 2048
 #define MOE_STATIC_DISPATCH_SCRATCH_BYTES (4608u * 1024u)
 moe_status_t moe_dispatch_capacity_static(const int32_t* ids, const float* gates, int ld, int T, int N, int k,
-                                          int R, const float* token_w, float capacity_factor, int32_t* counts,
+                                          int R, const float* token_w, float capacity_factor,
+                                          const int8_t* modality_bias, const float* r_v, int32_t* counts,
                                           int32_t* offsets, int32_t* row_token, float* row_gate,
                                           int32_t* active, int32_t* out_ids, float* out_gates,
                                           int32_t* slot_row, uint8_t* slot_status, int64_t* load_q,

@@ -94,16 +94,19 @@ def test_sere_rejects_bad_params(lib):
 def test_dispatch_rejects(lib):
     d = lib.moe_dispatch_capacity
     # capped mode needs ld >= R and R >= k
-    assert d(FAKE, FAKE, 2, 4, 8, 2, 4, None, 1.25, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
+    assert d(FAKE, FAKE, 2, 4, 8, 2, 4, None, 1.25, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
              None, FAKE, 1 << 30, None, None) == -1
     # capped mode with T above the limit
-    assert d(FAKE, FAKE, 4, 20000, 8, 2, 4, None, 1.25, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
+    assert d(FAKE, FAKE, 4, 20000, 8, 2, 4, None, 1.25, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
              None, FAKE, 1 << 30, None, None) == -2
     # workspace too small
-    assert d(FAKE, FAKE, 4, 64, 8, 2, 4, None, 1.25, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
+    assert d(FAKE, FAKE, 4, 64, 8, 2, 4, None, 1.25, None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None, None,
              None, FAKE, 16, None, None) == -4
+    # a modality bias needs the visual ratio
+    assert d(FAKE, FAKE, 4, 64, 8, 2, 4, None, 1.25, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+             None, None, None, FAKE, 1 << 30, None, None) == -1
     # NaN capacity factor
-    assert d(FAKE, FAKE, 4, 64, 8, 2, 4, None, float("nan"), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None,
+    assert d(FAKE, FAKE, 4, 64, 8, 2, 4, None, float("nan"), None, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, None,
              None, None, FAKE, 1 << 30, None, None) == -1
 
 

@@ -97,3 +97,48 @@ def test_capacity_dispatch_with_entropy_weights(g):
     assert np.array_equal(d["out_ids"], ref[0])
     assert np.array_equal(d["status"], ref[2])
     assert np.array_equal(d["load"], ref[3])
+
+
+def test_per_expert_capacity_from_visual_ratio(g):
+    """Modality-scaled capacity: weights and R_v from the entropies on the
+    GPU, a seeded modality bias per expert; the dispatch is bit-exact against
+    the oracle's per-expert capacity on the same weights and ratio, and every
+    expert's load stays within its own capacity."""
+    import expert_routing_moe_gb300._abi as abi
+    L = syn.prefill(with_weights=False)
+    vis = L.is_visual.astype(np.uint8)
+    x_dev = g.dev(L.x_bf16, torch.bfloat16)
+    T = L.T
+    ent = torch.empty(T, dtype=torch.float32, device=g.DEV)
+    w = torch.empty(T, dtype=torch.float32, device=g.DEV)
+    rv = torch.empty(1, dtype=torch.float32, device=g.DEV)
+    st = g.status_tensor()
+    moe.moe_token_weights(x_dev, g.dev(vis), ent, w, rv, 1.0, 1e-6, st)
+    bias = np.random.default_rng(5).integers(-1, 2, L.N).astype(np.int8)
+    logits = oracle.router(L.x_bf16, L.w_r, oracle.DT_BF16)
+    ids, gates = oracle.route(logits, L.R)
+    k, R, N = L.k, L.R, L.N
+    i32 = dict(dtype=torch.int32, device=g.DEV)
+    ws = torch.empty(abi.workspace_size(abi.MOE_OP_DISPATCH, T, 1, 1, N, k, R, True, 0), dtype=torch.uint8,
+                     device=g.DEV)
+    counts, offsets, active = torch.empty(N, **i32), torch.empty(N + 1, **i32), torch.empty(N + 1, **i32)
+    row_token, row_gate = torch.empty(T * k, **i32), torch.empty(T * k, dtype=torch.float32, device=g.DEV)
+    out_ids, out_gates = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=g.DEV)
+    status = torch.empty(T, k, dtype=torch.uint8, device=g.DEV)
+    load_q, cap_q = torch.empty(N, dtype=torch.int64, device=g.DEV), torch.empty(1, dtype=torch.int64, device=g.DEV)
+    moe.moe_dispatch_capacity(g.dev(ids), g.dev(gates), N, k, R, counts, offsets, row_token, row_gate, active, ws,
+                              w, L.gamma, out_ids, out_gates, None, status, load_q, cap_q, st,
+                              modality_bias=g.dev(bias), r_v=rv)
+    torch.cuda.synchronize()
+    g.assert_status_ok(st)
+    w_h, r_h = g.host(w), float(rv.item())
+    ref = oracle.capacity(ids, gates, N, k, R, w_h, L.gamma, bias=bias, r_v=r_h)
+    assert np.array_equal(g.host(out_ids), ref[0])
+    assert np.array_equal(g.host(status), ref[2])
+    assert np.array_equal(g.host(load_q), ref[3])
+    assert int(cap_q.item()) == ref[4]
+    S = sum(oracle.fixed_weight(float(v)) for v in w_h)
+    Ce = np.array([oracle.capacity_expert(S, k, L.gamma, N, int(bias[e]), r_h) for e in range(N)])
+    assert (g.host(load_q) <= Ce).all()
+    # a visual-leaning batch (R_v > 1/2) gives visual experts more room than text experts
+    assert (r_h > 0.5) == (Ce[bias == 1].min() > Ce[bias == -1].max())
