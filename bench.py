@@ -528,6 +528,38 @@ def run_prefill(args):
     clocks = clk.stop()
     tf = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"] \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+    # MACS: entropy weights computed in the step, per-expert capacity from a modality grouping
+    vis = t(L.is_visual.astype(np.uint8))
+    ent = torch.empty(L.T, dtype=torch.float32, device=dev)
+    w_ent = torch.empty(L.T, dtype=torch.float32, device=dev)
+    rv = torch.empty(1, dtype=torch.float32, device=dev)
+    lay_m = moe.MoELayer(lay.w_router, lay.w_gate, lay.w_up, lay.w_down, k=L.k, max_tokens=L.T, R=L.R,
+                         capacity_factor=L.gamma, modality_bias=t(syn.modality_bias(N)), r_v=rv)
+
+    def macs_step():
+        moe.moe_token_weights(x, vis, ent, w_ent, rv, 1.0, 1e-6, lay_m.status)
+        lay_m.forward(x, token_w=w_ent)
+
+    with torch.cuda.stream(stream):
+        macs_step()
+        stream.synchronize()
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gm, stream=stream):
+            macs_step()
+        gw = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gw, stream=stream):
+            for _ in range(20):
+                moe.moe_token_weights(x, vis, ent, w_ent, rv, 1.0, 1e-6, lay_m.status)
+    code, detail = lay_m.device_status()
+    if code != 0:
+        raise RuntimeError("device status %d detail %d (MACS step)" % (code, detail))
+    rows_m = int(lay_m.offsets[lay_m.N].item())
+    t_m = _timed_steps(torch, stream, [gm], steps, args.warmup, ws)
+    t_w = _timed_steps(torch, stream, [gw], steps, args.warmup, ws) / 20
+    macs = {"ms_per_layer": t_m / steps, "tokens_per_s": L.T * steps / (t_m / 1e3), "rows_admitted": rows_m,
+            "r_v": float(rv.item()), "token_weights_us": t_w / steps * 1e3,
+            "token_weights_gbs": L.T * H * 2 / (t_w / steps / 1e3) / 1e9,
+            "modality_groups": "seeded: 32 visual, 32 text, 64 shared experts"}
     flops = 2.0 * 3 * H * I * rows[0]
     ffn_s = float(np.mean(ffn)) / 1e3
     if rank == 0:
@@ -537,7 +569,8 @@ def run_prefill(args):
                           "tokens_per_s": L.T * steps / (tot / 1e3), "ms_per_layer": tot / steps,
                           "ffn_ms": ffn_s * 1e3, "rows_admitted": rows[0], "active_experts": us[0],
                           "ffn_tflops": flops / ffn_s / 1e12, "peak_tflops": tf,
-                          "ffn_frac": flops / ffn_s / 1e12 / tf, "steps": steps, "clocks": clocks}), flush=True)
+                          "ffn_frac": flops / ffn_s / 1e12 / tf, "steps": steps, "clocks": clocks,
+                          "macs_entropy_weights_and_expert_capacity": macs}), flush=True)
     return 0
 
 

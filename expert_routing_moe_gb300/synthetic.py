@@ -268,3 +268,18 @@ def stack_weight_seed(layer: int) -> int:
     """Seed of the torch generator that draws a stack layer's expert weights
     (N(0, 0.02), fp32 then bf16) on the device, in the order gate, up, down."""
     return seed_for(CONFIG_STACK, layer, STREAM_WEIGHTS)
+
+
+STREAM_MODALITY = 6
+
+
+def modality_bias(N: int = 128, config: int = CONFIG_PREFILL, layer: int = 0) -> np.ndarray:
+    """Expert modality groups for the per-expert capacity: a seeded quarter of
+    the experts visual (+1), a quarter text (-1), the rest shared (0).  It
+    stands in for the grouping by activation frequency on a calibration set,
+    which needs a trained model."""
+    perm = rng_for(config, layer, STREAM_MODALITY).permutation(N)
+    m = np.zeros(N, dtype=np.int8)
+    m[perm[: N // 4]] = 1
+    m[perm[N // 4: N // 2]] = -1
+    return m
