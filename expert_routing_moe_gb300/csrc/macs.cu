@@ -12,7 +12,8 @@
 // m = max z and e_d = exp(z_d - m), fixed lane order and xor butterfly.
 // Kernel 2: one CTA; the statistics and R_v are summed in double in a fixed
 // order (per-thread strided sums, then a fixed tree), so results are
-// reproducible bit for bit.
+// reproducible bit for bit; each token's sigmoid is evaluated in fp32 (one
+// SM evaluating T double-precision exponentials would dominate the call).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -115,16 +116,19 @@ __global__ void __launch_bounds__(1024) token_weights_kernel(const float* __rest
         }
     var = block_sum_f64(var, red);
     const double sigma = nv > 0.0 ? sqrt(var / nv) : 0.0;
+    // the z-score's scale once in double; each token's sigmoid in fp32
+    const float inv = static_cast<float>(1.0 / (sigma + static_cast<double>(eps)));
+    const float muf = static_cast<float>(mu);
     double wv = 0.0, wall = 0.0;
     for (int t = threadIdx.x; t < T; t += blockDim.x) {
-        double w = 1.0;
+        float w = 1.0f;
         if (is_visual[t]) {
-            const double ht = (static_cast<double>(entropy[t]) - mu) / (sigma + static_cast<double>(eps));
-            w = 1.0 / (1.0 + exp(static_cast<double>(delta) * ht));
-            wv += w;
+            const float ht = (entropy[t] - muf) * inv;
+            w = 1.0f / (1.0f + expf(delta * ht));
+            wv += static_cast<double>(w);
         }
-        wall += w;
-        token_w[t] = static_cast<float>(w);
+        wall += static_cast<double>(w);
+        token_w[t] = w;
     }
     wv = block_sum_f64(wv, red);
     wall = block_sum_f64(wall, red);

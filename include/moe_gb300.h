@@ -275,8 +275,9 @@ moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const
  *              batch; 1 for text tokens
  *   r_v        [1] fp32 out (may be NULL): sum of visual weights / sum of all
  *              weights (0 when T == 0)
- * Entropies are computed in fp32 (one warp per token); the statistics, the
- * weights and R_v in double, in a fixed order, so results are reproducible.
+ * Entropies and weights are computed in fp32 (one warp per token for the
+ * entropy); the statistics and R_v are summed in double, in a fixed order,
+ * so results are reproducible.
  * A non-finite feature sets MOE_DEV_NONFINITE (detail = token) in st.
  */
 moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,

@@ -65,6 +65,7 @@ def lib():
                                           c_p, c_i, c_p]
             c_d = ctypes.c_double
             L.orc_token_weights.argtypes = [c_p, c_i, c_i, c_i, c_p, c_d, c_d, c_p, c_p, c_p]
+            L.orc_similarity.argtypes = [c_p, c_i, c_i, c_i, c_p, c_p, c_p, c_i, c_i, c_i, c_p]
             _lib = L
     return _lib
 
@@ -209,6 +210,18 @@ def token_weights(x: np.ndarray, is_visual: np.ndarray, delta: float = 1.0, eps:
     _check(lib().orc_token_weights(_p(x), x_dtype, T, H, _p(vis), float(delta), float(eps), _p(ent), _p(w),
                                    _p(rv)), "token_weights")
     return ent[:T], w[:T], float(rv[0])
+
+
+def similarity(x: np.ndarray, w_gate, w_up, w_down, x_dtype: int = DT_F32, w_dtype: int = DT_F32) -> np.ndarray:
+    """[SERE] 4.2: Frobenius similarity of the experts' outputs on the
+    calibration tokens x [n][H]; [N][N] float64."""
+    x = np.ascontiguousarray(x)
+    n, H = x.shape
+    N, I = w_gate.shape[0], w_gate.shape[1]
+    out = np.zeros((N, N), dtype=np.float64)
+    _check(lib().orc_similarity(_p(x), x_dtype, n, H, _p(np.ascontiguousarray(w_gate)), _p(np.ascontiguousarray(w_up)),
+                                _p(np.ascontiguousarray(w_down)), w_dtype, I, N, _p(out)), "similarity")
+    return out
 
 
 def layer(L, sere_on: bool, capacity_on: bool = False, tokens=None, renorm_k: int = 0, logits=None):

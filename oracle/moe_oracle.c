@@ -37,6 +37,10 @@
  *                      rationals), declarative brute force per expert.
  *   orc_permute        pinned: numpy lexsort on (expert, token).
  *   orc_ffn_combine    pinned: dense numpy float64 evaluation of Eq. (1).
+ *   orc_similarity     pinned: a duplicated expert -> 1, a negated down
+ *                      projection -> -1, a positively scaled one -> 1,
+ *                      experts writing disjoint coordinates -> 0, symmetry,
+ *                      unit diagonal, |sim| <= 1.
  *   orc_token_weights  pinned: entropy against scipy's entropy of softmax,
  *                      closed forms (uniform z -> ln D, one raised entry,
  *                      shift invariance), two-token z-score -> sigmoid(+-delta),
@@ -573,5 +577,63 @@ int orc_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* i
         wall += w[t];
     }
     if (r_v != NULL) *r_v = wall > 0.0 ? wv / wall : 0.0;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Expert similarity from calibration tokens.  [SERE] 4.2: the          */
+/* similarity matrix is computed offline as the Frobenius similarity    */
+/* of the experts' outputs on calibration data:                         */
+/*   sim[i][j] = <E_i(X), E_j(X)>_F / (||E_i(X)||_F ||E_j(X)||_F)        */
+/* with E_e(X) the [n][H] matrix of expert e's SwiGLU outputs on the n   */
+/* calibration tokens ([MACS] Eq. 1's E_j).  Everything in double.      */
+/* Reading: the diagonal is 1, and a pair involving an expert whose      */
+/* output is all zero has similarity 0.                                  */
+/* ------------------------------------------------------------------ */
+int orc_similarity(const void* x, int x_dtype, int n, int H, const void* w_gate, const void* w_up,
+                   const void* w_down, int w_dtype, int I, int N, double* sim) {
+    if (n < 1 || H < 1 || I < 1 || N < 1 || !x || !w_gate || !w_up || !w_down || !sim) return ORC_EINVAL;
+    double* E = (double*)malloc(sizeof(double) * (size_t)N * n * H);
+    double* xv = (double*)malloc(sizeof(double) * (size_t)H);
+    double* act = (double*)malloc(sizeof(double) * (size_t)I);
+    if (!E || !xv || !act) { free(E); free(xv); free(act); return ORC_ENOMEM; }
+    for (int e = 0; e < N; ++e)
+        for (int t = 0; t < n; ++t) {
+            for (int h = 0; h < H; ++h) xv[h] = ld_val(x, x_dtype, (size_t)t * H + h);
+            for (int i = 0; i < I; ++i) {
+                double a = 0.0, b = 0.0;
+                const size_t base = ((size_t)e * I + i) * H;
+                for (int h = 0; h < H; ++h) {
+                    a += ld_val(w_gate, w_dtype, base + h) * xv[h];
+                    b += ld_val(w_up, w_dtype, base + h) * xv[h];
+                }
+                act[i] = a / (1.0 + exp(-a)) * b;
+            }
+            double* eo = E + ((size_t)e * n + t) * H;
+            for (int h = 0; h < H; ++h) {
+                double acc = 0.0;
+                const size_t base = ((size_t)e * H + h) * I;
+                for (int i = 0; i < I; ++i) acc += ld_val(w_down, w_dtype, base + i) * act[i];
+                eo[h] = acc;
+            }
+        }
+    const size_t K = (size_t)n * H;
+    for (int i = 0; i < N; ++i)
+        for (int j = i; j < N; ++j) {
+            double gij = 0.0, gii = 0.0, gjj = 0.0;
+            const double* a = E + (size_t)i * K;
+            const double* b = E + (size_t)j * K;
+            for (size_t q = 0; q < K; ++q) {
+                gij += a[q] * b[q];
+                gii += a[q] * a[q];
+                gjj += b[q] * b[q];
+            }
+            double v = (i == j) ? 1.0 : ((gii > 0.0 && gjj > 0.0) ? gij / sqrt(gii * gjj) : 0.0);
+            sim[(size_t)i * N + j] = v;
+            sim[(size_t)j * N + i] = v;
+        }
+    free(E);
+    free(xv);
+    free(act);
     return ORC_OK;
 }
