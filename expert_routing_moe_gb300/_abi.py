@@ -24,7 +24,7 @@ MOE_OK = 0
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_ROUTE_FROM_LOGITS, MOE_ROUTE_RENORM_TOPK = 1, 2
 MOE_FFN_FUSE_COMBINE, MOE_FFN_ZERO_Y = 1, 2
-MOE_OP_DISPATCH, MOE_OP_FFN = 1, 2
+MOE_OP_DISPATCH, MOE_OP_FFN, MOE_OP_CALIBRATE = 1, 2, 3
 MOE_SLOT_KEPT, MOE_SLOT_REROUTED, MOE_SLOT_DROPPED = 0, 1, 2
 MOE_DEV_OK, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0, 1, 2, 3
 
@@ -42,7 +42,7 @@ class _SereParams(ctypes.Structure):
 
 
 EXPORTS = ["moe_route", "moe_reroute_sere", "moe_dispatch_capacity", "moe_ffn_grouped", "moe_combine",
-           "moe_token_weights", "moe_workspace_size", "moe_status_string"]
+           "moe_token_weights", "moe_similarity_calibrate", "moe_workspace_size", "moe_status_string"]
 
 
 def load(path: str = LIB_PATH):
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH):
             L.moe_combine.restype = i
             L.moe_token_weights.argtypes = [p, i, i, i, p, f, f, p, p, p, p, p]
             L.moe_token_weights.restype = i
+            L.moe_similarity_calibrate.argtypes = [p, i, p, p, p, i, i, i, p, p, sz, p, p]
+            L.moe_similarity_calibrate.restype = i
             L.moe_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
             L.moe_workspace_size.restype = sz
             L.moe_status_string.argtypes = [i, i]
@@ -210,3 +212,15 @@ def moe_token_weights(x, is_visual, entropy, token_w, r_v=None, delta: float = 1
     rc = load().moe_token_weights(_ptr(x), _dtype_code(x), T, H, _ptr(is_visual), float(delta), float(eps),
                                   _ptr(entropy), _ptr(token_w), _ptr(r_v), _ptr(st), _stream(stream))
     _check(rc, "moe_token_weights")
+
+
+def moe_similarity_calibrate(x, w_gate, w_up, w_down, sim, workspace, st=None, stream=None):
+    """SERE similarity matrix [N][N] fp32 from the experts' outputs on the
+    calibration tokens x [n][H] bf16 (workspace: workspace_size(MOE_OP_CALIBRATE, n, H, I, N, 1, 1, False,
+    MOE_DTYPE_BF16) bytes)."""
+    n, H = x.shape
+    N, I = w_gate.shape[0], w_gate.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().moe_similarity_calibrate(_ptr(x), n, _ptr(w_gate), _ptr(w_up), _ptr(w_down), H, I, N, _ptr(sim),
+                                         _ptr(workspace), ws_bytes, _ptr(st), _stream(stream))
+    _check(rc, "moe_similarity_calibrate")

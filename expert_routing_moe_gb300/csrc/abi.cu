@@ -69,6 +69,10 @@ size_t moe_workspace_size(int op, int T, int H, int I, int N, int k, int R, int 
         if (H < 1 || I < 1) return 0;
         return moe::ffn_workspace(T, H, I, N, k, dtype);
     }
+    if (op == MOE_OP_CALIBRATE) {
+        if (H < 1 || I < 1) return 0;
+        return moe::calib_workspace(T, H, I, N);
+    }
     return 0;
 }
 
@@ -131,6 +135,24 @@ moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const
     if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_ffn_bf16(x, w_gate, w_up, w_down, T, H, I, N, k, offsets, row_token, row_gate,
                                           active, flags, out, workspace, st, s));
+}
+
+moe_status_t moe_similarity_calibrate(const void* x, int n, const void* w_gate, const void* w_up, const void* w_down,
+                                      int H, int I, int N, float* sim, void* workspace, size_t ws_bytes,
+                                      moe_dev_status* st, void* stream) {
+    if (n < 1 || H < 1 || I < 1 || N < 2) return MOE_ERR_INVALID_ARG;
+    if (x == nullptr || w_gate == nullptr || w_up == nullptr || w_down == nullptr || sim == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(sim))
+        return MOE_ERR_INVALID_ARG;
+    if (N > 128 || H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<long long>(n) * N > 0x7fffffffLL || static_cast<long long>(n) * H > 0x7fffffffLL)
+        return MOE_ERR_UNSUPPORTED;
+    const size_t need = moe::calib_workspace(n, H, I, N);
+    if (workspace == nullptr || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_similarity(x, n, w_gate, w_up, w_down, H, I, N, sim, workspace, st,
+                                            as_stream(stream)));
 }
 
 moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,

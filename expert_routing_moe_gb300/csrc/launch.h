@@ -60,6 +60,11 @@ cudaError_t launch_ffn_bf16(const void* x, const void* wg, const void* wu, const
                             int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                             const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
                             cudaStream_t s);
+// ---- expert similarity from calibration tokens (calib.cu) ----
+size_t calib_workspace(int n, int H, int I, int N);
+cudaError_t launch_similarity(const void* x, int n, const void* wg, const void* wu, const void* wd, int H, int I,
+                              int N, float* sim, void* ws, moe_dev_status* st, cudaStream_t s);
+
 // ---- entropy-weighted token load (macs.cu) ----
 cudaError_t launch_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
                                  float eps, float* entropy, float* token_w, float* r_v, moe_dev_status* st,

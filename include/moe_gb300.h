@@ -18,6 +18,9 @@
  *               moe_token_weights
  *                                entropy-weighted token load for the capacity
  *                                dispatch, and the effective visual ratio
+ *               moe_similarity_calibrate
+ *                                the SERE similarity matrix from the experts'
+ *                                outputs on calibration tokens
  *
  * Conventions for every entry point
  *  - Pointers named "host" are host memory; every other pointer is device
@@ -259,6 +262,31 @@ moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const
                              moe_dev_status* st, void* stream);
 
 /*
+ * Expert similarity from calibration tokens (SERE article sec. 4.2: the
+ * similarity matrix is prepared offline as the Frobenius similarity of the
+ * experts' outputs on calibration data):
+ *
+ *   sim[i][j] = <E_i(X), E_j(X)>_F / (||E_i(X)||_F ||E_j(X)||_F)
+ *
+ * with E_e(X) the [n][H] SwiGLU outputs of expert e on the calibration
+ * tokens X.  The diagonal is 1; a pair with an expert whose output is all
+ * zero gets 0.  Every expert's output on every token comes from the grouped
+ * tcgen05 FFN; they are rounded to bf16 and the Gram matrix E E^T runs on the
+ * tensor cores split over the SMs, summed and normalised in double.  The
+ * result feeds moe_sere_params.sim (the matrix is exactly symmetric).
+ *
+ *   x          [n][H] bf16 calibration tokens
+ *   w_gate, w_up, w_down   bf16 expert weights as in moe_ffn_grouped
+ *   sim        [N][N] fp32 out
+ *   workspace  moe_workspace_size(MOE_OP_CALIBRATE, n, H, I, N, 1, 1, 0,
+ *              MOE_DTYPE_BF16) bytes, 256-byte aligned
+ * Limits: 2 <= N <= 128, H % 128 == 0, I % 128 == 0, n * N and n * H below 2^31.
+ */
+moe_status_t moe_similarity_calibrate(const void* x, int n, const void* w_gate, const void* w_up,
+                                      const void* w_down, int H, int I, int N, float* sim, void* workspace,
+                                      size_t ws_bytes, moe_dev_status* st, void* stream);
+
+/*
  * Entropy-weighted token load ("MACS" sec. 3.2 Eqs. (4)-(5) and sec. 3.3
  * Eq. (7)): the per-token load weights that moe_dispatch_capacity takes as
  * token_w, and the batch's effective visual ratio.
@@ -297,6 +325,7 @@ moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const f
 /* ---------------------------------------------------------------- */
 #define MOE_OP_DISPATCH 1
 #define MOE_OP_FFN 2
+#define MOE_OP_CALIBRATE 3   /* moe_similarity_calibrate: T = calibration tokens n */
 
 /* Bytes of device workspace that `op` needs for these sizes (0 if none).
  * capped != 0 asks for the capacity-mode size of MOE_OP_DISPATCH; dtype

@@ -145,3 +145,12 @@ def test_token_weights_rejects(lib):
     assert f(FAKE, 5, 4, 64, FAKE, 1.0, 1e-6, FAKE, FAKE, None, None, None) == -1    # dtype
     assert f(FAKE, 1, 4, 64, None, 1.0, 1e-6, FAKE, FAKE, None, None, None) == -1    # no is_visual
     assert f(None, 1, 0, 64, None, 1.0, 1e-6, None, None, None, None, None) == 0     # empty batch
+
+
+def test_similarity_calibrate_rejects(lib):
+    f = lib.moe_similarity_calibrate
+    assert f(FAKE, 16, FAKE, FAKE, FAKE, 256, 128, 200, FAKE, FAKE, 1 << 30, None, None) == -2   # N > 128
+    assert f(FAKE, 16, FAKE, FAKE, FAKE, 192, 128, 8, FAKE, FAKE, 1 << 30, None, None) == -2     # H % 128
+    assert f(FAKE, 0, FAKE, FAKE, FAKE, 256, 128, 8, FAKE, FAKE, 1 << 30, None, None) == -1      # no tokens
+    assert f(FAKE, 16, FAKE, FAKE, FAKE, 256, 128, 8, None, FAKE, 1 << 30, None, None) == -1     # no output
+    assert f(FAKE, 16, FAKE, FAKE, FAKE, 256, 128, 8, FAKE, FAKE, 16, None, None) == -4          # workspace
