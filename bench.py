@@ -533,11 +533,14 @@ def run_prefill(args):
     ent = torch.empty(L.T, dtype=torch.float32, device=dev)
     w_ent = torch.empty(L.T, dtype=torch.float32, device=dev)
     rv = torch.empty(1, dtype=torch.float32, device=dev)
+    from expert_routing_moe_gb300 import _abi as abi
+    ws_tw = torch.empty(max(abi.workspace_size(abi.MOE_OP_TOKEN_WEIGHTS, L.T, 1, 1, 1, 1, 1, False, 0), 256),
+                        dtype=torch.uint8, device=dev)
     lay_m = moe.MoELayer(lay.w_router, lay.w_gate, lay.w_up, lay.w_down, k=L.k, max_tokens=L.T, R=L.R,
                          capacity_factor=L.gamma, modality_bias=t(syn.modality_bias(N)), r_v=rv)
 
     def macs_step():
-        moe.moe_token_weights(x, vis, ent, w_ent, rv, 1.0, 1e-6, lay_m.status)
+        moe.moe_token_weights(x, vis, ent, w_ent, rv, 1.0, 1e-6, lay_m.status, workspace=ws_tw)
         lay_m.forward(x, token_w=w_ent)
 
     with torch.cuda.stream(stream):
@@ -549,7 +552,7 @@ def run_prefill(args):
         gw = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gw, stream=stream):
             for _ in range(20):
-                moe.moe_token_weights(x, vis, ent, w_ent, rv, 1.0, 1e-6, lay_m.status)
+                moe.moe_token_weights(x, vis, ent, w_ent, rv, 1.0, 1e-6, lay_m.status, workspace=ws_tw)
     code, detail = lay_m.device_status()
     if code != 0:
         raise RuntimeError("device status %d detail %d (MACS step)" % (code, detail))
@@ -571,6 +574,49 @@ def run_prefill(args):
                           "ffn_tflops": flops / ffn_s / 1e12, "peak_tflops": tf,
                           "ffn_frac": flops / ffn_s / 1e12 / tf, "steps": steps, "clocks": clocks,
                           "macs_entropy_weights_and_expert_capacity": macs}), flush=True)
+    return 0
+
+
+def run_calibrate(args):
+    """SERE similarity calibration: every expert's output on n = 64 synthetic
+    calibration tokens, then the normalised Gram matrix (offline step)."""
+    torch, moe, dev, ws, rank, local = _gpu_setup()
+    from expert_routing_moe_gb300 import synthetic as syn
+    from expert_routing_moe_gb300 import _abi as abi
+    L = syn.decode(32)
+    n = 64
+    t = lambda a, dt=None: (torch.from_numpy(a).view(dt) if dt else torch.from_numpy(a)).to(dev)
+    wg, wu, wd = t(L.w_gate, torch.bfloat16), t(L.w_up, torch.bfloat16), t(L.w_down, torch.bfloat16)
+    x = t(syn.f32_to_bf16_bits(np.random.default_rng(1000 * syn.CONFIG_DECODE + 7).standard_normal((n, H))
+                               .astype(np.float32)), torch.bfloat16)
+    wsz = abi.workspace_size(abi.MOE_OP_CALIBRATE, n, H, I, N, 1, 1, False, abi.MOE_DTYPE_BF16)
+    work = torch.empty(wsz, dtype=torch.uint8, device=dev)
+    sim = torch.empty(N, N, dtype=torch.float32, device=dev)
+    st = torch.zeros(2, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        moe.moe_similarity_calibrate(x, wg, wu, wd, sim, work, st)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            moe.moe_similarity_calibrate(x, wg, wu, wd, sim, work, st)
+    if int(st[0].item()) != 0:
+        raise RuntimeError("device status %s" % st.tolist())
+    steps = max(3, args.steps // 20)
+    tot = _timed_steps(torch, stream, [g], steps, args.warmup, ws)
+    ms = tot / steps
+    gram_flops = 2.0 * N * N * n * H
+    ffn_flops = 2.0 * 3 * H * I * n * N
+    s_h = sim.cpu().numpy()
+    off = s_h[~np.eye(N, dtype=bool)]
+    if rank == 0:
+        print(json.dumps({"workload": "SERE similarity calibration: 128 experts (hidden 2048, intermediate 768, bf16) "
+                                      "on 64 synthetic N(0,1) calibration tokens",
+                          "metric": "calibration time", "ms": ms, "steps": steps,
+                          "expert_weight_gbs": N * EXPERT_BYTES / (ms / 1e3) / 1e9,
+                          "tflops_total": (gram_flops + ffn_flops) / (ms / 1e3) / 1e12,
+                          "sim_offdiag": {"min": float(off.min()), "max": float(off.max()),
+                                          "mean": float(off.mean())}}), flush=True)
     return 0
 
 
@@ -672,7 +718,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=4, help="expert-weight copies rotated per step")
     ap.add_argument("--clock-soak", type=float, default=1.5, help="seconds of untimed load while sampling clocks")
-    ap.add_argument("--workload", choices=["decode", "sweep", "prefill", "stack"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "sweep", "prefill", "stack", "calibrate"], default="decode",
                     help="decode (the headline line) or one of the further workloads")
     ap.add_argument("--layers", type=int, default=48, help="layers of the stack workload")
     ap.add_argument("--traffic", type=float, default=None,
@@ -690,6 +736,8 @@ def main():
         return run_prefill(args)
     if args.workload == "stack":
         return run_stack(args)
+    if args.workload == "calibrate":
+        return run_calibrate(args)
     return run_ours(args)
 
 

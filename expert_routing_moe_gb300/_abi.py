@@ -24,7 +24,7 @@ MOE_OK = 0
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_ROUTE_FROM_LOGITS, MOE_ROUTE_RENORM_TOPK = 1, 2
 MOE_FFN_FUSE_COMBINE, MOE_FFN_ZERO_Y = 1, 2
-MOE_OP_DISPATCH, MOE_OP_FFN, MOE_OP_CALIBRATE = 1, 2, 3
+MOE_OP_DISPATCH, MOE_OP_FFN, MOE_OP_CALIBRATE, MOE_OP_TOKEN_WEIGHTS = 1, 2, 3, 4
 MOE_SLOT_KEPT, MOE_SLOT_REROUTED, MOE_SLOT_DROPPED = 0, 1, 2
 MOE_DEV_OK, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0, 1, 2, 3
 
@@ -69,7 +69,7 @@ def load(path: str = LIB_PATH):
             L.moe_ffn_grouped.restype = i
             L.moe_combine.argtypes = [p, p, p, i, i, i, p, p]
             L.moe_combine.restype = i
-            L.moe_token_weights.argtypes = [p, i, i, i, p, f, f, p, p, p, p, p]
+            L.moe_token_weights.argtypes = [p, i, i, i, p, f, f, p, p, p, p, sz, p, p]
             L.moe_token_weights.restype = i
             L.moe_similarity_calibrate.argtypes = [p, i, p, p, p, i, i, i, p, p, sz, p, p]
             L.moe_similarity_calibrate.restype = i
@@ -205,12 +205,19 @@ def moe_combine(rows_out, slot_row, slot_gate, y, stream=None):
 
 
 def moe_token_weights(x, is_visual, entropy, token_w, r_v=None, delta: float = 1.0, eps: float = 1e-6, st=None,
-                      stream=None):
+                      stream=None, workspace=None):
     """MACS entropy-weighted token load: entropy [T], token_w [T] and R_v [1]
-    (fp32 CUDA tensors) from the token features x [T][H] and is_visual [T] uint8."""
+    (fp32 CUDA tensors) from the token features x [T][H] and is_visual [T]
+    uint8.  workspace: workspace_size(MOE_OP_TOKEN_WEIGHTS, T, ...) bytes; when
+    omitted a buffer is allocated for this call (not graph-capturable)."""
     T, H = x.shape
+    if workspace is None:
+        workspace = torch.empty(max(workspace_size(MOE_OP_TOKEN_WEIGHTS, T, 1, 1, 1, 1, 1, False, 0), 256),
+                                dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
     rc = load().moe_token_weights(_ptr(x), _dtype_code(x), T, H, _ptr(is_visual), float(delta), float(eps),
-                                  _ptr(entropy), _ptr(token_w), _ptr(r_v), _ptr(st), _stream(stream))
+                                  _ptr(entropy), _ptr(token_w), _ptr(r_v), _ptr(workspace), ws_bytes, _ptr(st),
+                                  _stream(stream))
     _check(rc, "moe_token_weights")
 
 

@@ -69,6 +69,7 @@ size_t moe_workspace_size(int op, int T, int H, int I, int N, int k, int R, int 
         if (H < 1 || I < 1) return 0;
         return moe::ffn_workspace(T, H, I, N, k, dtype);
     }
+    if (op == MOE_OP_TOKEN_WEIGHTS) return moe::token_weights_workspace(T);
     if (op == MOE_OP_CALIBRATE) {
         if (H < 1 || I < 1) return 0;
         return moe::calib_workspace(T, H, I, N);
@@ -156,8 +157,8 @@ moe_status_t moe_similarity_calibrate(const void* x, int n, const void* w_gate, 
 }
 
 moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
-                               float eps, float* entropy, float* token_w, float* r_v, moe_dev_status* st,
-                               void* stream) {
+                               float eps, float* entropy, float* token_w, float* r_v, void* workspace,
+                               size_t ws_bytes, moe_dev_status* st, void* stream) {
     if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
     if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
     if (!(eps > 0.f) || !(delta == delta) || delta - delta != 0.f) return MOE_ERR_INVALID_ARG;   // eps > 0, delta finite
@@ -165,8 +166,10 @@ moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const u
     if (x == nullptr || is_visual == nullptr || entropy == nullptr || token_w == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x)) return MOE_ERR_INVALID_ARG;
     if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
-    return from_cuda(moe::launch_token_weights(x, x_dtype, T, H, is_visual, delta, eps, entropy, token_w, r_v, st,
-                                               as_stream(stream)));
+    if (workspace == nullptr || ws_bytes < moe::token_weights_workspace(T)) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_token_weights(x, x_dtype, T, H, is_visual, delta, eps, entropy, token_w, r_v,
+                                               workspace, st, as_stream(stream)));
 }
 
 moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const float* slot_gate, int T, int H, int k,

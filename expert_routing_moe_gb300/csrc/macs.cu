@@ -10,10 +10,12 @@
 //
 // Kernel 1: one warp per token, H = ln Z - (sum e_d (z_d - m)) / Z with
 // m = max z and e_d = exp(z_d - m), fixed lane order and xor butterfly.
-// Kernel 2: one CTA; the statistics and R_v are summed in double in a fixed
-// order (per-thread strided sums, then a fixed tree), so results are
-// reproducible bit for bit; each token's sigmoid is evaluated in fp32 (one
-// SM evaluating T double-precision exponentials would dominate the call).
+// Kernel 1 also leaves per-CTA partials (count, sum, sum of squares of the
+// visual entropies, in double, in a fixed order) in the workspace.
+// Kernel 2: one CTA reduces the partials in a fixed order (so results are
+// reproducible bit for bit), then evaluates each token's sigmoid in fp32 and
+// R_v.  (One SM doing the whole reduction in double costs about as much as
+// the entropies themselves: fp64 throughput per SM is small.)
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -36,117 +38,149 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// Per-CTA partial statistics of the visual tokens' entropies (count, sum,
+// sum of squares), in double, summed by thread 0 over its 8 tokens in order.
+struct EntPart {
+    double n, s, s2;
+};
+
 template <typename XT>
 __global__ void __launch_bounds__(256) token_entropy_kernel(const XT* __restrict__ x, int T, int H,
-                                                            float* __restrict__ entropy, moe_dev_status* st) {
+                                                            const uint8_t* __restrict__ is_visual,
+                                                            float* __restrict__ entropy, EntPart* __restrict__ parts,
+                                                            moe_dev_status* st) {
+    __shared__ float s_h[8];
     pdl_wait();
     pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= T) return;
-    const XT* row = x + static_cast<size_t>(t) * H;
-    float m = -INFINITY;
-    bool finite = true;
-    for (int h = lane * 8; h < H; h += 256) {
-        float v[8];
-        load8(row + h, v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * 8 + warp;
+    if (lane == 0) s_h[warp] = 0.f;
+    if (t < T) {   // warp-uniform
+        const XT* row = x + static_cast<size_t>(t) * H;
+        float m = -INFINITY;
+        bool finite = true;
+        for (int h = lane * 8; h < H; h += 256) {
+            float v[8];
+            load8(row + h, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            finite &= isfinite(v[j]);
-            m = fmaxf(m, v[j]);
+            for (int j = 0; j < 8; ++j) {
+                finite &= isfinite(v[j]);
+                m = fmaxf(m, v[j]);
+            }
+        }
+        for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+        float Z = 0.f, S1 = 0.f;
+        for (int h = lane * 8; h < H; h += 256) {
+            float v[8];
+            load8(row + h, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float d = v[j] - m;
+                const float e = expf(d);
+                Z += e;
+                S1 = fmaf(e, d, S1);
+            }
+        }
+        for (int off = 16; off >= 1; off >>= 1) {
+            Z += __shfl_xor_sync(kFull, Z, off);
+            S1 += __shfl_xor_sync(kFull, S1, off);
+        }
+        const bool all_finite = __all_sync(kFull, finite);
+        if (lane == 0) {
+            const float hv = logf(Z) - S1 / Z;
+            entropy[t] = hv;
+            s_h[warp] = hv;
+            if (!all_finite) report(st, MOE_DEV_NONFINITE, t);
         }
     }
-    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-    float Z = 0.f, S1 = 0.f;
-    for (int h = lane * 8; h < H; h += 256) {
-        float v[8];
-        load8(row + h, v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float d = v[j] - m;
-            const float e = expf(d);
-            Z += e;
-            S1 = fmaf(e, d, S1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        EntPart p{0.0, 0.0, 0.0};
+        for (int w = 0; w < 8; ++w) {
+            const int tw = blockIdx.x * 8 + w;
+            if (tw < T && is_visual[tw]) {
+                const double h = static_cast<double>(s_h[w]);
+                p.n += 1.0;
+                p.s += h;
+                p.s2 += h * h;
+            }
         }
-    }
-    for (int off = 16; off >= 1; off >>= 1) {
-        Z += __shfl_xor_sync(kFull, Z, off);
-        S1 += __shfl_xor_sync(kFull, S1, off);
-    }
-    const bool all_finite = __all_sync(kFull, finite);
-    if (lane == 0) {
-        entropy[t] = logf(Z) - S1 / Z;
-        if (!all_finite) report(st, MOE_DEV_NONFINITE, t);
+        parts[blockIdx.x] = p;
     }
 }
 
 // Sum over the block in double, fixed order: thread-strided partials, warp
-// butterfly, then warp 0 adds the 32 warp sums in order.
+// butterfly, then thread 0 adds the warp sums in order and broadcasts (one
+// thread doing the 32 adds: fp64 throughput on one SM is small).
 __device__ __forceinline__ double block_sum_f64(double v, double* red) {
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
     __syncthreads();
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    double s = 0.0;
-    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) s += red[i];
-    return s;
+    if (threadIdx.x == 0) {
+        double s = 0.0;
+        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) s += red[i];
+        red[32] = s;
+    }
+    __syncthreads();
+    return red[32];
 }
 
 __global__ void __launch_bounds__(1024) token_weights_kernel(const float* __restrict__ entropy,
                                                              const uint8_t* __restrict__ is_visual, int T,
+                                                             const EntPart* __restrict__ parts, int nparts,
                                                              float delta, float eps, float* __restrict__ token_w,
                                                              float* __restrict__ r_v) {
-    __shared__ double red[32];
+    __shared__ double red[33];
     pdl_wait();
     pdl_trigger();
-    double s = 0.0, nv = 0.0;
-    for (int t = threadIdx.x; t < T; t += blockDim.x)
-        if (is_visual[t]) {
-            s += static_cast<double>(entropy[t]);
-            nv += 1.0;
-        }
-    s = block_sum_f64(s, red);
+    double nv = 0.0, s = 0.0, s2 = 0.0;
+    for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
+        nv += parts[i].n;
+        s += parts[i].s;
+        s2 += parts[i].s2;
+    }
     nv = block_sum_f64(nv, red);
+    s = block_sum_f64(s, red);
+    s2 = block_sum_f64(s2, red);
+    // population statistics; the one-pass variance in double is exact to far
+    // below the fp32 entropies' own rounding at these magnitudes (|H| <= ln D)
     const double mu = nv > 0.0 ? s / nv : 0.0;
-    double var = 0.0;
-    for (int t = threadIdx.x; t < T; t += blockDim.x)
-        if (is_visual[t]) {
-            const double d = static_cast<double>(entropy[t]) - mu;
-            var += d * d;
-        }
-    var = block_sum_f64(var, red);
-    const double sigma = nv > 0.0 ? sqrt(var / nv) : 0.0;
+    const double sigma = nv > 0.0 ? sqrt(fmax(s2 / nv - mu * mu, 0.0)) : 0.0;
     // the z-score's scale once in double; each token's sigmoid in fp32
     const float inv = static_cast<float>(1.0 / (sigma + static_cast<double>(eps)));
     const float muf = static_cast<float>(mu);
-    double wv = 0.0, wall = 0.0;
+    float wv = 0.f, wall = 0.f;   // per thread at most ceil(T / 1024) terms
     for (int t = threadIdx.x; t < T; t += blockDim.x) {
         float w = 1.0f;
         if (is_visual[t]) {
             const float ht = (entropy[t] - muf) * inv;
             w = 1.0f / (1.0f + expf(delta * ht));
-            wv += static_cast<double>(w);
+            wv += w;
         }
-        wall += static_cast<double>(w);
+        wall += w;
         token_w[t] = w;
     }
-    wv = block_sum_f64(wv, red);
-    wall = block_sum_f64(wall, red);
-    if (threadIdx.x == 0 && r_v != nullptr) *r_v = static_cast<float>(wall > 0.0 ? wv / wall : 0.0);
+    const double wvs = block_sum_f64(static_cast<double>(wv), red);
+    const double walls = block_sum_f64(static_cast<double>(wall), red);
+    if (threadIdx.x == 0 && r_v != nullptr) *r_v = static_cast<float>(walls > 0.0 ? wvs / walls : 0.0);
 }
 
+size_t token_weights_workspace(int T) { return static_cast<size_t>((T + 7) / 8) * sizeof(EntPart); }
+
 cudaError_t launch_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
-                                 float eps, float* entropy, float* token_w, float* r_v, moe_dev_status* st,
+                                 float eps, float* entropy, float* token_w, float* r_v, void* ws, moe_dev_status* st,
                                  cudaStream_t s) {
-    const dim3 grid((T + 7) / 8);
+    const int nb = (T + 7) / 8;
+    EntPart* parts = static_cast<EntPart*>(ws);
     cudaError_t e = (x_dtype == MOE_DTYPE_BF16)
-                        ? launch_pdl(token_entropy_kernel<__nv_bfloat16>, grid, dim3(256), 0, s,
-                                     static_cast<const __nv_bfloat16*>(x), T, H, entropy, st)
-                        : launch_pdl(token_entropy_kernel<float>, grid, dim3(256), 0, s, static_cast<const float*>(x),
-                                     T, H, entropy, st);
+                        ? launch_pdl(token_entropy_kernel<__nv_bfloat16>, dim3(nb), dim3(256), 0, s,
+                                     static_cast<const __nv_bfloat16*>(x), T, H, is_visual, entropy, parts, st)
+                        : launch_pdl(token_entropy_kernel<float>, dim3(nb), dim3(256), 0, s,
+                                     static_cast<const float*>(x), T, H, is_visual, entropy, parts, st);
     if (e != cudaSuccess) return e;
     return launch_pdl(token_weights_kernel, dim3(1), dim3(1024), 0, s, static_cast<const float*>(entropy), is_visual,
-                      T, delta, eps, token_w, r_v);
+                      T, static_cast<const EntPart*>(parts), nb, delta, eps, token_w, r_v);
 }
 
 }  // namespace moe

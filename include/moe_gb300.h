@@ -303,14 +303,17 @@ moe_status_t moe_similarity_calibrate(const void* x, int n, const void* w_gate, 
  *              batch; 1 for text tokens
  *   r_v        [1] fp32 out (may be NULL): sum of visual weights / sum of all
  *              weights (0 when T == 0)
+ *   workspace  moe_workspace_size(MOE_OP_TOKEN_WEIGHTS, T, ...) bytes (24 bytes
+ *              per 8 tokens), 256-byte aligned
  * Entropies and weights are computed in fp32 (one warp per token for the
- * entropy); the statistics and R_v are summed in double, in a fixed order,
- * so results are reproducible.
+ * entropy); the statistics (count, sum and sum of squares of the visual
+ * entropies, population variance) and R_v are summed in double, in a fixed
+ * order, so results are reproducible.
  * A non-finite feature sets MOE_DEV_NONFINITE (detail = token) in st.
  */
 moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
-                               float eps, float* entropy, float* token_w, float* r_v, moe_dev_status* st,
-                               void* stream);
+                               float eps, float* entropy, float* token_w, float* r_v, void* workspace,
+                               size_t ws_bytes, moe_dev_status* st, void* stream);
 
 /*
  * Weighted combine ("MACS" Eq. (1)): y[t] = sum_r gate[t][r] * rows_out[slot_row[t][r]]
@@ -326,6 +329,7 @@ moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const f
 #define MOE_OP_DISPATCH 1
 #define MOE_OP_FFN 2
 #define MOE_OP_CALIBRATE 3   /* moe_similarity_calibrate: T = calibration tokens n */
+#define MOE_OP_TOKEN_WEIGHTS 4   /* moe_token_weights: depends on T only */
 
 /* Bytes of device workspace that `op` needs for these sizes (0 if none).
  * capped != 0 asks for the capacity-mode size of MOE_OP_DISPATCH; dtype

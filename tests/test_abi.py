@@ -138,13 +138,15 @@ def test_combine_rejects(lib):
 def test_token_weights_rejects(lib):
     f = lib.moe_token_weights
     odd = ctypes.c_void_p((1 << 20) + 8)
-    assert f(FAKE, 1, 4, 64, FAKE, 1.0, 0.0, FAKE, FAKE, None, None, None) == -1     # eps must be > 0
-    assert f(FAKE, 1, 4, 64, FAKE, float("nan"), 1e-6, FAKE, FAKE, None, None, None) == -1
-    assert f(FAKE, 1, 4, 60, FAKE, 1.0, 1e-6, FAKE, FAKE, None, None, None) == -2    # H % 8
-    assert f(odd, 1, 4, 64, FAKE, 1.0, 1e-6, FAKE, FAKE, None, None, None) == -1     # misaligned x
-    assert f(FAKE, 5, 4, 64, FAKE, 1.0, 1e-6, FAKE, FAKE, None, None, None) == -1    # dtype
-    assert f(FAKE, 1, 4, 64, None, 1.0, 1e-6, FAKE, FAKE, None, None, None) == -1    # no is_visual
-    assert f(None, 1, 0, 64, None, 1.0, 1e-6, None, None, None, None, None) == 0     # empty batch
+    W = (FAKE, 1 << 20)
+    assert f(FAKE, 1, 4, 64, FAKE, 1.0, 0.0, FAKE, FAKE, None, *W, None, None) == -1     # eps must be > 0
+    assert f(FAKE, 1, 4, 64, FAKE, float("nan"), 1e-6, FAKE, FAKE, None, *W, None, None) == -1
+    assert f(FAKE, 1, 4, 60, FAKE, 1.0, 1e-6, FAKE, FAKE, None, *W, None, None) == -2    # H % 8
+    assert f(odd, 1, 4, 64, FAKE, 1.0, 1e-6, FAKE, FAKE, None, *W, None, None) == -1     # misaligned x
+    assert f(FAKE, 5, 4, 64, FAKE, 1.0, 1e-6, FAKE, FAKE, None, *W, None, None) == -1    # dtype
+    assert f(FAKE, 1, 4, 64, None, 1.0, 1e-6, FAKE, FAKE, None, *W, None, None) == -1    # no is_visual
+    assert f(FAKE, 1, 4, 64, FAKE, 1.0, 1e-6, FAKE, FAKE, None, FAKE, 0, None, None) == -4   # no workspace
+    assert f(None, 1, 0, 64, None, 1.0, 1e-6, None, None, None, None, 0, None, None) == 0    # empty batch
 
 
 def test_similarity_calibrate_rejects(lib):
