@@ -225,8 +225,7 @@ def _capture(torch, stream, layers, xs, sere, token_w=None):
             stream.synchronize()
             g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
             with torch.cuda.graph(g1, stream=stream):
-                lay.route(x, sere)
-                lay.dispatch(T, token_w)
+                lay.route_and_dispatch(x, sere, token_w)
             with torch.cuda.graph(g2, stream=stream):
                 lay.ffn(x)
             graphs.append((g1, g2))
@@ -366,8 +365,9 @@ def run_ours(args):
     s_top8 = _capture_steps(torch, stream, layers, xs, False)
     g_sere = _capture(torch, stream, layers, xs, True)
     g_top8 = _capture(torch, stream, layers, xs, False)
-    # router, rank+SERE, permute, FFN counter clear, FFN tensor-core kernel
-    launches_per_step = 5
+    # routing + SERE + permutation in one launch, FFN counter clear, FFN tensor-core kernel
+    assert layers[0].fused_route_dispatch_ok(T)
+    launches_per_step = 3
 
     clk = ClockSampler(local if ws > 1 else 0)
     clk.start()
@@ -421,8 +421,8 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Dirichlet-skewed router logits, N(0,0.02) bf16 experts)",
         "config": workload_config({"parallelism": "replicas" if ws > 1 else "single GPU",
-                                   "cuda_graphs": "value: one graph per step (router, rank+SERE, permute, FFN "
-                                                  "counter clear, FFN); roofline: a second timed run of the same "
+                                   "cuda_graphs": "value: one graph per step (single-launch router + rank "
+                                                  "+ SERE + permutation, FFN counter clear, FFN); roofline: a second timed run of the same "
                                                   "steps as a routing graph and an FFN graph with CUDA events "
                                                   "around the FFN graph"}),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -653,8 +653,7 @@ def run_stack(args):
         xres.copy_(x0_f32)
         xb.copy_(x0_bf16)
         for lay in stack:
-            lay.route(xb, sere)
-            lay.dispatch(B)
+            lay.route_and_dispatch(xb, sere)
             lay.ffn(xb, accumulate_into=xres)
             xb.copy_(xres)
 

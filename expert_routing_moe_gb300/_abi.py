@@ -24,7 +24,8 @@ MOE_OK = 0
 MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
 MOE_ROUTE_FROM_LOGITS, MOE_ROUTE_RENORM_TOPK = 1, 2
 MOE_FFN_FUSE_COMBINE, MOE_FFN_ZERO_Y = 1, 2
-MOE_OP_DISPATCH, MOE_OP_FFN, MOE_OP_CALIBRATE, MOE_OP_TOKEN_WEIGHTS = 1, 2, 3, 4
+MOE_OP_DISPATCH, MOE_OP_FFN, MOE_OP_CALIBRATE, MOE_OP_TOKEN_WEIGHTS, MOE_OP_ROUTE_DISPATCH = 1, 2, 3, 4, 5
+ROUTE_DISPATCH_MAX_T, ROUTE_DISPATCH_MAX_SLOTS = 256, 2048
 MOE_SLOT_KEPT, MOE_SLOT_REROUTED, MOE_SLOT_DROPPED = 0, 1, 2
 MOE_DEV_OK, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0, 1, 2, 3
 
@@ -41,7 +42,7 @@ class _SereParams(ctypes.Structure):
                 ("protect", ctypes.c_void_p), ("union_bitmap", ctypes.c_void_p), ("stats", ctypes.c_void_p)]
 
 
-EXPORTS = ["moe_route", "moe_reroute_sere", "moe_dispatch_capacity", "moe_ffn_grouped", "moe_combine",
+EXPORTS = ["moe_route", "moe_route_dispatch", "moe_reroute_sere", "moe_dispatch_capacity", "moe_ffn_grouped", "moe_combine",
            "moe_token_weights", "moe_similarity_calibrate", "moe_workspace_size", "moe_status_string"]
 
 
@@ -57,6 +58,8 @@ def load(path: str = LIB_PATH):
             i, u32, f, p, sz = ctypes.c_int, ctypes.c_uint32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
             L.moe_route.argtypes = [p, i, p, i, i, i, i, i, u32, p, p, p, p, p, p]
             L.moe_route.restype = i
+            L.moe_route_dispatch.argtypes = [p, i, p, i, i, i, i, u32, p, p, p, p, p, p, p, p, p, p, sz, p, p]
+            L.moe_route_dispatch.restype = i
             L.moe_reroute_sere.argtypes = [p, p, i, i, i, i, p, p, p]
             L.moe_reroute_sere.restype = i
             L.moe_dispatch_capacity.argtypes = [p, p, i, i, i, i, i, p, f, p, p, p, p, p, p, p, p, p, p, p, p, p,
@@ -146,6 +149,24 @@ def moe_route(x, w_router, logits, ids, gates, k: int, flags: int = 0, sere: Opt
     rc = load().moe_route(_ptr(x), xd, _ptr(w_router), T, H, N, R, k, flags, _ptr(logits), _ptr(ids), _ptr(gates),
                           sp, _ptr(st), _stream(stream))
     _check(rc, "moe_route")
+
+
+def moe_route_dispatch(x, w_router, logits, ids, gates, counts, offsets, row_token, row_gate, active, workspace,
+                       flags: int = 0, sere: Optional[SereParams] = None, st=None, stream=None):
+    """Decode batches (T <= 256): moe_route with R = k (optionally with SERE)
+    and the uncapped dispatch in one launch.  ids/gates are [T][k]; workspace
+    is workspace_size(MOE_OP_ROUTE_DISPATCH, ...) bytes, zero-filled before
+    its first use (each call leaves it zeroed)."""
+    T, N = logits.shape
+    k = ids.shape[1]
+    H = x.shape[1]
+    sp = None if sere is None else ctypes.byref(sere._c())
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().moe_route_dispatch(_ptr(x), _dtype_code(x), _ptr(w_router), T, H, N, k, flags, _ptr(logits),
+                                   _ptr(ids), _ptr(gates), sp, _ptr(counts), _ptr(offsets), _ptr(row_token),
+                                   _ptr(row_gate), _ptr(active), _ptr(workspace), ws_bytes, _ptr(st),
+                                   _stream(stream))
+    _check(rc, "moe_route_dispatch")
 
 
 def moe_reroute_sere(ids, gates, N: int, k: int, sere: SereParams, st=None, stream=None):

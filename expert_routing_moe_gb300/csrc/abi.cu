@@ -51,6 +51,38 @@ moe_status_t moe_route(const void* x, int x_dtype, const float* w_router, int T,
     return from_cuda(moe::launch_rank(logits, T, N, R, k, renorm, ids, gates, st, s));
 }
 
+moe_status_t moe_route_dispatch(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int k,
+                                uint32_t flags, float* logits, int32_t* ids, float* gates,
+                                const moe_sere_params* sere, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                                float* row_gate, int32_t* active, void* workspace, size_t ws_bytes,
+                                moe_dev_status* st, void* stream) {
+    if (T < 0 || N < 1 || N > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_RANKS || k > N) return MOE_ERR_INVALID_ARG;
+    if (flags & ~MOE_ROUTE_RENORM_TOPK) return MOE_ERR_INVALID_ARG;
+    if (sere != nullptr && !sere_ok(sere, N, k)) return MOE_ERR_INVALID_ARG;
+    if (counts == nullptr || offsets == nullptr || active == nullptr) return MOE_ERR_INVALID_ARG;
+    if (T > moe::kRouteDispatchMaxT || T * k > moe::kRouteDispatchMaxSlots) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) {
+        cudaStream_t s = as_stream(stream);
+        cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
+        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
+        cudaMemsetAsync(active, 0, sizeof(int32_t) * (N + 1), s);
+        return from_cuda(cudaGetLastError());
+    }
+    if (x == nullptr || w_router == nullptr || H < 1 || logits == nullptr || ids == nullptr || gates == nullptr ||
+        row_token == nullptr || row_gate == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+    if (x_dtype == MOE_DTYPE_BF16 && (H % 8 != 0)) return MOE_ERR_UNSUPPORTED;
+    if (x_dtype == MOE_DTYPE_F32 && (H % 4 != 0)) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+    if (workspace == nullptr || ws_bytes < static_cast<size_t>(moe::kRouteDispatchWs)) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_route_dispatch(x, x_dtype, w_router, T, H, N, k,
+                                                (flags & MOE_ROUTE_RENORM_TOPK) != 0, logits, ids, gates, sere,
+                                                counts, offsets, row_token, row_gate, active, workspace, st,
+                                                as_stream(stream)));
+}
+
 moe_status_t moe_reroute_sere(int32_t* ids, float* gates, int ld, int T, int N, int k, const moe_sere_params* sere,
                               moe_dev_status* st, void* stream) {
     if (ids == nullptr || gates == nullptr || sere == nullptr) return MOE_ERR_INVALID_ARG;
@@ -70,6 +102,7 @@ size_t moe_workspace_size(int op, int T, int H, int I, int N, int k, int R, int 
         return moe::ffn_workspace(T, H, I, N, k, dtype);
     }
     if (op == MOE_OP_TOKEN_WEIGHTS) return moe::token_weights_workspace(T);
+    if (op == MOE_OP_ROUTE_DISPATCH) return static_cast<size_t>(moe::kRouteDispatchWs);
     if (op == MOE_OP_CALIBRATE) {
         if (H < 1 || I < 1) return 0;
         return moe::calib_workspace(T, H, I, N);

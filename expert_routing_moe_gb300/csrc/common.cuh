@@ -218,6 +218,16 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     return v;
 }
 
+// Ticket: fetch-and-add with acquire-release semantics at GPU scope.  Taken
+// by one thread after a CTA barrier, it publishes the CTA's earlier writes
+// and, for the CTA that draws the last ticket, makes every other CTA's
+// published writes visible to the reads after its next barrier.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

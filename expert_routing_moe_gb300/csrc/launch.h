@@ -40,6 +40,15 @@ cudaError_t launch_sere(int32_t* ids, float* gates, int ld, int T, int N, int k,
                         moe_dev_status* st, cudaStream_t s);
 constexpr int kSereMaxT = 4096;
 
+// ---- decode routing + dispatch in one launch (route_dispatch.cu) ----
+constexpr int kRouteDispatchMaxT = 256;
+constexpr int kRouteDispatchMaxSlots = 2048;   // T * k
+constexpr int kRouteDispatchWs = 512;
+cudaError_t launch_route_dispatch(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int k,
+                                  bool renorm, float* logits, int32_t* ids, float* gates, const moe_sere_params* sere,
+                                  int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,
+                                  int32_t* active, void* ws, moe_dev_status* st, cudaStream_t s);
+
 // ---- dispatch (dispatch.cu) ----
 size_t dispatch_workspace(int T, int N, int k, int R, bool capped);
 cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int T, int N, int k, int R,

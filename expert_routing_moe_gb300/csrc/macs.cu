@@ -9,13 +9,19 @@
 // ratio R_v = sum_vis w / sum_all w.
 //
 // Kernel 1: one warp per token, H = ln Z - (sum e_d (z_d - m)) / Z with
-// m = max z and e_d = exp(z_d - m), fixed lane order and xor butterfly.
-// Kernel 1 also leaves per-CTA partials (count, sum, sum of squares of the
-// visual entropies, in double, in a fixed order) in the workspace.
-// Kernel 2: one CTA reduces the partials in a fixed order (so results are
-// reproducible bit for bit), then evaluates each token's sigmoid in fp32 and
-// R_v.  (One SM doing the whole reduction in double costs about as much as
-// the entropies themselves: fp64 throughput per SM is small.)
+// m = max z and e_d = exp(z_d - m) (CUDA's fast exponential intrinsic: its
+// error is far below the entropy's fp32 summation error), fixed lane order and
+// xor butterfly.  Rows
+// of up to 2048 features are read once, into registers, and both passes run
+// from there.  Kernel 1 also leaves per-CTA partials (count, sum, sum of
+// squares of the visual entropies, in double, in a fixed order) in the
+// workspace.
+// Kernel 2: one thread per token over ceil(T / 256) CTAs.  Every CTA reduces
+// the kernel-1 partials itself, in the same fixed order, so all CTAs hold
+// bit-identical statistics; each evaluates its tokens' sigmoids in fp32 and
+// leaves its (visual, total) weight sums in double.  The last CTA to finish
+// (a ticket counter that kernel 1 clears) sums those in CTA order for R_v, so
+// the results are reproducible bit for bit.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -44,21 +50,53 @@ struct EntPart {
     double n, s, s2;
 };
 
-template <typename XT>
-__global__ void __launch_bounds__(256) token_entropy_kernel(const XT* __restrict__ x, int T, int H,
-                                                            const uint8_t* __restrict__ is_visual,
-                                                            float* __restrict__ entropy, EntPart* __restrict__ parts,
-                                                            moe_dev_status* st) {
-    __shared__ float s_h[8];
-    pdl_wait();
-    pdl_trigger();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t = blockIdx.x * 8 + warp;
-    if (lane == 0) s_h[warp] = 0.f;
-    if (t < T) {   // warp-uniform
-        const XT* row = x + static_cast<size_t>(t) * H;
-        float m = -INFINITY;
-        bool finite = true;
+// Chunks of 8 features per lane that a register-cached row holds (H <= 2048).
+constexpr int kEntRegChunks = 8;
+
+// Max, then sum of e and e * (z - m), over one lane's chunks of a row.
+template <typename XT, bool CACHED>
+__device__ __forceinline__ void entropy_lane_sums(const XT* row, int H, int lane, float& m, float& Z, float& S1,
+                                                  bool& finite) {
+    m = -INFINITY;
+    finite = true;
+    if constexpr (CACHED) {
+        float v[kEntRegChunks][8];
+#pragma unroll
+        for (int c = 0; c < kEntRegChunks; ++c) {
+            const int h = lane * 8 + c * 256;
+            if (h < H) {
+                load8(row + h, v[c]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[c][j] = -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kEntRegChunks; ++c) {
+            if (lane * 8 + c * 256 < H) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    finite &= isfinite(v[c][j]);
+                    m = fmaxf(m, v[c][j]);
+                }
+            }
+        }
+        for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+        Z = 0.f;
+        S1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < kEntRegChunks; ++c) {
+            if (lane * 8 + c * 256 < H) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float d = v[c][j] - m;
+                    const float e = __expf(d);
+                    Z += e;
+                    S1 = fmaf(e, d, S1);
+                }
+            }
+        }
+    } else {
         for (int h = lane * 8; h < H; h += 256) {
             float v[8];
             load8(row + h, v);
@@ -69,18 +107,44 @@ __global__ void __launch_bounds__(256) token_entropy_kernel(const XT* __restrict
             }
         }
         for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-        float Z = 0.f, S1 = 0.f;
+        Z = 0.f;
+        S1 = 0.f;
         for (int h = lane * 8; h < H; h += 256) {
             float v[8];
             load8(row + h, v);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float d = v[j] - m;
-                const float e = expf(d);
+                const float e = __expf(d);
                 Z += e;
                 S1 = fmaf(e, d, S1);
             }
         }
+    }
+}
+
+// Sums of the weights of one CTA of kernel 2 (visual, all), in double.
+struct WPart {
+    double wv, wall;
+};
+
+template <typename XT, bool CACHED>
+__global__ void __launch_bounds__(256) token_entropy_kernel(const XT* __restrict__ x, int T, int H,
+                                                            const uint8_t* __restrict__ is_visual,
+                                                            float* __restrict__ entropy, EntPart* __restrict__ parts,
+                                                            int* __restrict__ ticket, moe_dev_status* st) {
+    __shared__ float s_h[8];
+    pdl_wait();
+    pdl_trigger();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;   // kernel 2's ticket, cleared for this call
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * 8 + warp;
+    if (lane == 0) s_h[warp] = 0.f;
+    if (t < T) {   // warp-uniform
+        const XT* row = x + static_cast<size_t>(t) * H;
+        float m, Z, S1;
+        bool finite;
+        entropy_lane_sums<XT, CACHED>(row, H, lane, m, Z, S1, finite);
         for (int off = 16; off >= 1; off >>= 1) {
             Z += __shfl_xor_sync(kFull, Z, off);
             S1 += __shfl_xor_sync(kFull, S1, off);
@@ -109,78 +173,135 @@ __global__ void __launch_bounds__(256) token_entropy_kernel(const XT* __restrict
     }
 }
 
-// Sum over the block in double, fixed order: thread-strided partials, warp
-// butterfly, then thread 0 adds the warp sums in order and broadcasts (one
-// thread doing the 32 adds: fp64 throughput on one SM is small).
-__device__ __forceinline__ double block_sum_f64(double v, double* red) {
-    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+// Sums of NV values over the block in double, fixed order: warp butterfly,
+// then thread 0 adds the warp sums in order and broadcasts (one thread doing
+// the few adds: fp64 throughput on one SM is small).  red: [NV][33].
+template <int NV>
+__device__ __forceinline__ void block_sum_f64(double (&v)[NV], double (*red)[33]) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        for (int off = 16; off >= 1; off >>= 1) v[i] += __shfl_xor_sync(kFull, v[i], off);
     __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) red[i][threadIdx.x >> 5] = v[i];
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        double s = 0.0;
-        for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) s += red[i];
-        red[32] = s;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            double t = 0.0;
+            for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[i][w];
+            red[i][32] = t;
+        }
     }
     __syncthreads();
-    return red[32];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = red[i][32];
 }
 
-__global__ void __launch_bounds__(1024) token_weights_kernel(const float* __restrict__ entropy,
-                                                             const uint8_t* __restrict__ is_visual, int T,
-                                                             const EntPart* __restrict__ parts, int nparts,
-                                                             float delta, float eps, float* __restrict__ token_w,
-                                                             float* __restrict__ r_v) {
-    __shared__ double red[33];
+__global__ void __launch_bounds__(256) token_weights_kernel(const float* __restrict__ entropy,
+                                                            const uint8_t* __restrict__ is_visual, int T,
+                                                            const EntPart* __restrict__ parts, int nparts,
+                                                            float delta, float eps, float* __restrict__ token_w,
+                                                            WPart* __restrict__ wparts, int* __restrict__ ticket,
+                                                            float* __restrict__ r_v) {
+    __shared__ double red[3][33];
+    __shared__ bool s_last;
     pdl_wait();
     pdl_trigger();
-    double nv = 0.0, s = 0.0, s2 = 0.0;
+    // this thread's token, loaded before the statistics are reduced
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const bool vis_t = t < T && is_visual[t] != 0;
+    const float ent_t = vis_t ? entropy[t] : 0.f;
+    double st3[3] = {0.0, 0.0, 0.0};   // count, sum, sum of squares
     for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
-        nv += parts[i].n;
-        s += parts[i].s;
-        s2 += parts[i].s2;
+        const EntPart p = parts[i];
+        st3[0] += p.n;
+        st3[1] += p.s;
+        st3[2] += p.s2;
     }
-    nv = block_sum_f64(nv, red);
-    s = block_sum_f64(s, red);
-    s2 = block_sum_f64(s2, red);
-    // population statistics; the one-pass variance in double is exact to far
-    // below the fp32 entropies' own rounding at these magnitudes (|H| <= ln D)
-    const double mu = nv > 0.0 ? s / nv : 0.0;
-    const double sigma = nv > 0.0 ? sqrt(fmax(s2 / nv - mu * mu, 0.0)) : 0.0;
-    // the z-score's scale once in double; each token's sigmoid in fp32
-    const float inv = static_cast<float>(1.0 / (sigma + static_cast<double>(eps)));
-    const float muf = static_cast<float>(mu);
-    float wv = 0.f, wall = 0.f;   // per thread at most ceil(T / 1024) terms
-    for (int t = threadIdx.x; t < T; t += blockDim.x) {
-        float w = 1.0f;
-        if (is_visual[t]) {
-            const float ht = (entropy[t] - muf) * inv;
+    block_sum_f64<3>(st3, red);
+    // population statistics, by one thread (a double division or square
+    // root is tens of fp64 operations, and fp64 throughput per SM is small);
+    // the one-pass variance in double is exact to far below the fp32
+    // entropies' own rounding at these magnitudes (|H| <= ln D)
+    __shared__ float s_mu, s_inv;
+    if (threadIdx.x == 0) {
+        const double nv = st3[0], s = st3[1], s2 = st3[2];
+        const double mu = nv > 0.0 ? s / nv : 0.0;
+        const double sigma = nv > 0.0 ? sqrt(fmax(s2 / nv - mu * mu, 0.0)) : 0.0;
+        // the z-score's scale once in double; each token's sigmoid in fp32
+        s_inv = static_cast<float>(1.0 / (sigma + static_cast<double>(eps)));
+        s_mu = static_cast<float>(mu);
+    }
+    __syncthreads();
+    const float inv = s_inv, muf = s_mu;
+    float w = 0.f, wv = 0.f;
+    if (t < T) {
+        w = 1.0f;
+        if (vis_t) {
+            const float ht = (ent_t - muf) * inv;
             w = 1.0f / (1.0f + expf(delta * ht));
-            wv += w;
+            wv = w;
         }
-        wall += w;
         token_w[t] = w;
     }
-    const double wvs = block_sum_f64(static_cast<double>(wv), red);
-    const double walls = block_sum_f64(static_cast<double>(wall), red);
-    if (threadIdx.x == 0 && r_v != nullptr) *r_v = static_cast<float>(walls > 0.0 ? wvs / walls : 0.0);
+    if (r_v == nullptr) return;   // uniform over the grid
+    double ws2[2] = {static_cast<double>(wv), static_cast<double>(w)};
+    block_sum_f64<2>(ws2, red);
+    if (threadIdx.x == 0) {
+        wparts[blockIdx.x] = WPart{ws2[0], ws2[1]};
+        __threadfence();
+        s_last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;   // uniform over the block
+    __threadfence();
+    double tot[2] = {0.0, 0.0};
+    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x) {
+        tot[0] += __ldcg(&wparts[i].wv);
+        tot[1] += __ldcg(&wparts[i].wall);
+    }
+    block_sum_f64<2>(tot, red);
+    if (threadIdx.x == 0) {
+        const double av = tot[0], aa = tot[1];
+        *r_v = static_cast<float>(aa > 0.0 ? av / aa : 0.0);
+        *ticket = 0;
+    }
 }
 
-size_t token_weights_workspace(int T) { return static_cast<size_t>((T + 7) / 8) * sizeof(EntPart); }
+// Workspace: kernel-1 partials, kernel-2 partials, the ticket.
+static size_t ent_parts_bytes(int T) { return static_cast<size_t>((T + 7) / 8) * sizeof(EntPart); }
+static size_t w_parts_bytes(int T) { return static_cast<size_t>((T + 255) / 256) * sizeof(WPart); }
+
+size_t token_weights_workspace(int T) { return ent_parts_bytes(T) + w_parts_bytes(T) + 16; }
 
 cudaError_t launch_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
                                  float eps, float* entropy, float* token_w, float* r_v, void* ws, moe_dev_status* st,
                                  cudaStream_t s) {
     const int nb = (T + 7) / 8;
     EntPart* parts = static_cast<EntPart*>(ws);
-    cudaError_t e = (x_dtype == MOE_DTYPE_BF16)
-                        ? launch_pdl(token_entropy_kernel<__nv_bfloat16>, dim3(nb), dim3(256), 0, s,
-                                     static_cast<const __nv_bfloat16*>(x), T, H, is_visual, entropy, parts, st)
-                        : launch_pdl(token_entropy_kernel<float>, dim3(nb), dim3(256), 0, s,
-                                     static_cast<const float*>(x), T, H, is_visual, entropy, parts, st);
+    WPart* wparts = reinterpret_cast<WPart*>(static_cast<char*>(ws) + ent_parts_bytes(T));
+    int* ticket = reinterpret_cast<int*>(static_cast<char*>(ws) + ent_parts_bytes(T) + w_parts_bytes(T));
+    const bool cached = H <= kEntRegChunks * 256;
+    cudaError_t e;
+    if (x_dtype == MOE_DTYPE_BF16) {
+        const auto* xb = static_cast<const __nv_bfloat16*>(x);
+        e = cached ? launch_pdl(token_entropy_kernel<__nv_bfloat16, true>, dim3(nb), dim3(256), 0, s, xb, T, H,
+                                is_visual, entropy, parts, ticket, st)
+                   : launch_pdl(token_entropy_kernel<__nv_bfloat16, false>, dim3(nb), dim3(256), 0, s, xb, T, H,
+                                is_visual, entropy, parts, ticket, st);
+    } else {
+        const auto* xf = static_cast<const float*>(x);
+        e = cached ? launch_pdl(token_entropy_kernel<float, true>, dim3(nb), dim3(256), 0, s, xf, T, H, is_visual,
+                                entropy, parts, ticket, st)
+                   : launch_pdl(token_entropy_kernel<float, false>, dim3(nb), dim3(256), 0, s, xf, T, H, is_visual,
+                                entropy, parts, ticket, st);
+    }
     if (e != cudaSuccess) return e;
-    return launch_pdl(token_weights_kernel, dim3(1), dim3(1024), 0, s, static_cast<const float*>(entropy), is_visual,
-                      T, static_cast<const EntPart*>(parts), nb, delta, eps, token_w, r_v);
+    return launch_pdl(token_weights_kernel, dim3((T + 255) / 256), dim3(256), 0, s, static_cast<const float*>(entropy),
+                      is_visual, T, static_cast<const EntPart*>(parts), nb, delta, eps, token_w, wparts, ticket, r_v);
 }
 
 }  // namespace moe

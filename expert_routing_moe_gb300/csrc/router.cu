@@ -17,81 +17,16 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// Router GEMM, small batches: four warps per expert (one per quarter of H,
-// so that a warp issues all of its loads at once), four tokens per warp, the
-// lanes split the quarter (4 consecutive elements each, 16-byte weight
-// loads); a fixed xor-butterfly and a fixed-order sum of the quarters reduce
-// the partial sums.  Two experts per CTA: grid (ceil(N/2), ceil(T/4)).
+// Router GEMM, small batches: router_tile (routing.cuh) with two experts per
+// 256-thread CTA, grid (ceil(N/2), ceil(T/4)).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
-    float4 q = *reinterpret_cast<const float4*>(p);
-    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-}
-__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
-    uint2 q = *reinterpret_cast<const uint2*>(p);
-    v[0] = __uint_as_float(q.x << 16);
-    v[1] = __uint_as_float(q.x & 0xffff0000u);
-    v[2] = __uint_as_float(q.y << 16);
-    v[3] = __uint_as_float(q.y & 0xffff0000u);
-}
-
 template <typename XT>
 __global__ void __launch_bounds__(256) router_warp_kernel(const XT* __restrict__ x, const float* __restrict__ w,
                                                           int T, int H, int N, float* __restrict__ logits) {
-    constexpr int U = 4;  // 128-element strips per batch of loads (all issued before any FMA)
     __shared__ float part[8][4];
     pdl_wait();
     pdl_trigger();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int j = blockIdx.x * 2 + (warp >> 2);   // four warps per expert, one per quarter of H
-    const int t0 = blockIdx.y * 4;
-    const int hq = ((H >> 2) + 127) / 128 * 128;
-    const int hbeg = min((warp & 3) * hq, H), hend = min(hbeg + hq, H);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (j < N) {
-        const float* wr = w + static_cast<size_t>(j) * H;
-        for (int hb = hbeg + lane * 4; hb < hend; hb += 128 * U) {
-            float wv[U][4];
-            float xv[U][4][4];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int h = hb + 128 * u;
-                if (h < hend) {
-                    load4(wr + h, wv[u]);
-                } else {
-                    wv[u][0] = wv[u][1] = wv[u][2] = wv[u][3] = 0.f;
-                }
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt) {
-                    if (h < hend && t0 + tt < T) {
-                        load4(x + static_cast<size_t>(t0 + tt) * H + h, xv[u][tt]);
-                    } else {
-                        xv[u][tt][0] = xv[u][tt][1] = xv[u][tt][2] = xv[u][tt][3] = 0.f;
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[tt] = fmaf(xv[u][tt][q], wv[u][q], acc[tt]);
-        }
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) acc[tt] += __shfl_xor_sync(kFull, acc[tt], off);
-        }
-    }
-    if (lane < 4) part[warp][lane] = (lane == 0) ? acc[0] : (lane == 1) ? acc[1] : (lane == 2) ? acc[2] : acc[3];
-    __syncthreads();
-    if (threadIdx.x < 8) {
-        const int jl = threadIdx.x >> 2, tt = threadIdx.x & 3;
-        const int jj = blockIdx.x * 2 + jl;
-        if (jj < N && t0 + tt < T)
-            logits[static_cast<size_t>(t0 + tt) * N + jj] =
-                (part[4 * jl][tt] + part[4 * jl + 1][tt]) + (part[4 * jl + 2][tt] + part[4 * jl + 3][tt]);
-    }
+    router_tile<XT, 2>(x, w, T, H, N, blockIdx.x * 2, blockIdx.y * 4, logits, part);
 }
 
 // ---------------------------------------------------------------------------

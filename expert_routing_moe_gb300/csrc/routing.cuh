@@ -1,15 +1,118 @@
-// routing.cuh -- per-token ranking (fp32 softmax gate, top-R by logit) and the
-// SERE reroute of one token's secondary slots, each done by one warp.  Shared
-// by the routing kernels and the fused decode layer kernel.
+// routing.cuh -- the small-batch router tile, per-token ranking (fp32 softmax
+// gate, top-R by logit) and the SERE reroute of one token's secondary slots,
+// each done by one warp.  Shared by the routing kernels and the fused decode
+// routing + dispatch kernel, so that both give bit-identical results.
 //
 // Gate and ranking: "MACS: Modality-Aware Capacity Scaling for Efficient
 // Multimodal MoE Inference", sec. 3.1, Eq. (1).  SERE: Xiaohongshu
 // multi-image QA inference article, sec. 4.1-4.2.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace moe {
+
+// ---------------------------------------------------------------------------
+// Router logits of experts j0 .. j0+EPC-1 for tokens t0 .. t0+3 by a CTA of
+// 128 * EPC threads: four warps per expert (one per quarter of H), four
+// tokens per warp, the lanes split the quarter (4 consecutive elements each,
+// 16-byte weight loads); a fixed xor-butterfly and a fixed-order sum of the
+// quarters reduce the partial sums.  part: shared [4 * EPC][4].
+// U strips of 128 elements are loaded per batch (all loads of a batch issued
+// before any FMA; x is kept as loaded and widened at the FMA); U changes only
+// how many loads are in flight, never the order of the FMAs.  The router
+// weight is read with an L2 evict-last hint: it is read again every step and
+// stays resident while expert weights stream through the L2.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ float4 ld_f4_keep(const float* p, uint64_t pol) {
+    float4 v;
+    asm("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void prefetch_l2_keep(const void* p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
+template <typename XT>
+struct XRaw;
+template <>
+struct XRaw<float> {
+    using type = float4;
+    static __device__ __forceinline__ type load(const float* p) { return *reinterpret_cast<const float4*>(p); }
+    static __device__ __forceinline__ float at(const type& r, int q) {
+        return q == 0 ? r.x : q == 1 ? r.y : q == 2 ? r.z : r.w;
+    }
+    static __device__ __forceinline__ type zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+};
+template <>
+struct XRaw<__nv_bfloat16> {
+    using type = uint2;
+    static __device__ __forceinline__ type load(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
+    static __device__ __forceinline__ float at(const type& r, int q) {
+        const uint32_t u = (q < 2) ? r.x : r.y;
+        return __uint_as_float((q & 1) ? (u & 0xffff0000u) : (u << 16));
+    }
+    static __device__ __forceinline__ type zero() { return make_uint2(0u, 0u); }
+};
+
+template <typename XT, int EPC, int U = 4>
+__device__ __forceinline__ void router_tile(const XT* __restrict__ x, const float* __restrict__ w, int T, int H,
+                                            int N, int j0, int t0, float* __restrict__ logits, float (*part)[4]) {
+    using XR = XRaw<XT>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int j = j0 + (warp >> 2);
+    const int hq = ((H >> 2) + 127) / 128 * 128;
+    const int hbeg = min((warp & 3) * hq, H), hend = min(hbeg + hq, H);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (j < N) {
+        const uint64_t pol = l2_evict_last_policy();
+        const float* wr = w + static_cast<size_t>(j) * H;
+        for (int hb = hbeg + lane * 4; hb < hend; hb += 128 * U) {
+            float4 wv[U];
+            typename XR::type xv[U][4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int h = hb + 128 * u;
+                wv[u] = (h < hend) ? ld_f4_keep(wr + h, pol) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int tt = 0; tt < 4; ++tt)
+                    xv[u][tt] = (h < hend && t0 + tt < T) ? XR::load(x + static_cast<size_t>(t0 + tt) * H + h)
+                                                         : XR::zero();
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float wq[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+                for (int tt = 0; tt < 4; ++tt)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[tt] = fmaf(XR::at(xv[u][tt], q), wq[q], acc[tt]);
+            }
+        }
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) acc[tt] += __shfl_xor_sync(kFull, acc[tt], off);
+        }
+    }
+    if (lane < 4) part[warp][lane] = (lane == 0) ? acc[0] : (lane == 1) ? acc[1] : (lane == 2) ? acc[2] : acc[3];
+    __syncthreads();
+    if (threadIdx.x < 4 * EPC) {
+        const int jl = threadIdx.x >> 2, tt = threadIdx.x & 3;
+        const int jj = j0 + jl;
+        if (jj < N && t0 + tt < T)
+            logits[static_cast<size_t>(t0 + tt) * N + jj] =
+                (part[4 * jl][tt] + part[4 * jl + 1][tt]) + (part[4 * jl + 2][tt] + part[4 * jl + 3][tt]);
+    }
+}
 
 // ---------------------------------------------------------------------------
 // Ranking of one token by one warp.  Lane l holds experts j = l + 32 i for
@@ -32,7 +135,9 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
-template <int PL>
+// kCoherent: read the logits with L1-bypassing loads (logits written by other
+// CTAs of the same grid).
+template <int PL, bool kCoherent = false>
 __device__ __forceinline__ bool rank_token(const float* __restrict__ lrow, int N, int R, int k, bool renorm,
                                            int& my_id, float& my_gate) {
     const int lane = threadIdx.x & 31;
@@ -43,7 +148,7 @@ __device__ __forceinline__ bool rank_token(const float* __restrict__ lrow, int N
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
         const int j = lane + 32 * i;
-        lv[i] = (j < N) ? lrow[j] : 0.f;
+        lv[i] = (j < N) ? (kCoherent ? __ldcg(lrow + j) : lrow[j]) : 0.f;
         if (j < N && !isfinite(lv[i])) finite = false;
         kv[i] = (j < N) ? order_key(lv[i]) : 0u;   // every finite logit has a key > 0
         lmax = max(lmax, kv[i]);

@@ -1,8 +1,9 @@
 """A resident MoE layer: device weights, preallocated buffers and the C-ABI
 calls of one forward pass in order (router + rank (+ SERE) -> dispatch
-(+ capacity) -> grouped FFN with the combine fused in).  Buffers are sized
-once for a maximum batch, so a forward pass allocates nothing and can be
-captured in a CUDA graph."""
+(+ capacity) -> grouped FFN with the combine fused in).  Uncapped batches of
+up to 256 tokens take the single-launch routing + dispatch entry point.
+Buffers are sized once for a maximum batch, so a forward pass allocates
+nothing and can be captured in a CUDA graph."""
 from __future__ import annotations
 
 from typing import Optional
@@ -54,6 +55,9 @@ class MoELayer:
         wsf = abi.workspace_size(abi.MOE_OP_FFN, T, H, self.I, N, k, self.R, capped, dt)
         self.ws_dispatch = torch.empty(max(wsd, 256), dtype=torch.uint8, device=dev)
         self.ws_ffn = torch.empty(max(wsf, 256), dtype=torch.uint8, device=dev)
+        # the single-launch routing + dispatch keeps a counter here (zero between calls)
+        wsr = abi.workspace_size(abi.MOE_OP_ROUTE_DISPATCH, T, H, self.I, N, k, self.R, False, dt)
+        self.ws_route = torch.zeros(max(wsr, 256), dtype=torch.uint8, device=dev)
         self.y = torch.empty(T, H, dtype=f32, device=dev)
 
     def sere_params(self) -> abi.SereParams:
@@ -64,6 +68,30 @@ class MoELayer:
         sp = self.sere_params() if sere else None
         abi.moe_route(x, self.w_router, self.logits[:T], self.ids[:T], self.gates[:T], self.k, self.flags, sp,
                       self.status, stream)
+
+    def fused_route_dispatch_ok(self, T: int) -> bool:
+        return (self.capacity_factor <= 0 and self.R == self.k and T <= abi.ROUTE_DISPATCH_MAX_T
+                and T * self.k <= abi.ROUTE_DISPATCH_MAX_SLOTS)
+
+    def route_dispatch(self, x: torch.Tensor, sere: bool, stream=None):
+        """Routing and the uncapped dispatch in one launch (decode batches)."""
+        T = x.shape[0]
+        sp = self.sere_params() if sere else None
+        abi.moe_route_dispatch(x, self.w_router, self.logits[:T], self.ids[:T], self.gates[:T], self.counts,
+                               self.offsets, self.row_token, self.row_gate, self.active, self.ws_route, self.flags,
+                               sp, self.status, stream)
+
+    def route_and_dispatch(self, x: torch.Tensor, sere: bool, token_w: Optional[torch.Tensor] = None, stream=None):
+        """Routing (+ SERE when a similarity matrix is set) and dispatch: one
+        launch for uncapped batches of up to 256 tokens, separate calls
+        otherwise."""
+        T = x.shape[0]
+        sere = sere and self.sim is not None
+        if self.fused_route_dispatch_ok(T):
+            self.route_dispatch(x, sere, stream)
+        else:
+            self.route(x, sere, stream)
+            self.dispatch(T, token_w, stream)
 
     def dispatch(self, T: int, token_w: Optional[torch.Tensor] = None, stream=None):
         abi.moe_dispatch_capacity(self.ids[:T], self.gates[:T], self.N, self.k, self.R, self.counts, self.offsets,
@@ -89,8 +117,7 @@ class MoELayer:
         T = x.shape[0]
         if T > self.max_T:
             raise abi.MoeError("batch %d exceeds the layer's max_tokens %d" % (T, self.max_T))
-        self.route(x, sere and self.sim is not None, stream)
-        self.dispatch(T, token_w, stream)
+        self.route_and_dispatch(x, sere, token_w, stream)
         self.ffn(x, stream)
         return self.y[:T]
 

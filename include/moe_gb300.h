@@ -10,6 +10,9 @@
  * computed as   moe_route        router GEMM + fp32 softmax + top-R ranking,
  *                                optionally fused with the SERE batch reroute
  *               moe_reroute_sere the SERE reroute on its own
+ *               moe_route_dispatch
+ *                                decode batches: moe_route (optionally with
+ *                                SERE) and the uncapped dispatch in one launch
  *               moe_dispatch_capacity
  *                                expert-sorted permutation, optionally under a
  *                                weighted capacity with overflow reroute / drop
@@ -119,6 +122,34 @@ typedef struct moe_sere_params {
 moe_status_t moe_route(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int R,
                        int k, uint32_t flags, float* logits, int32_t* ids, float* gates,
                        const moe_sere_params* sere, moe_dev_status* st, void* stream);
+
+/*
+ * Decode routing and dispatch in one launch: the results of moe_route with
+ * R = k (and `sere`, if given) followed by the uncapped
+ * moe_dispatch_capacity, bit for bit, for batches of up to 256 tokens.
+ * "SERE" article sec. 4.2: the reroute feeds the fused MoE with no host round
+ * trip; at decode sizes the ranking, reroute and permutation touch a few KB,
+ * so they run in the last CTA of the router launch instead of in launches of
+ * their own.
+ *
+ *   x, x_dtype, w_router, T, H, N, k, logits, ids, gates, sere
+ *              as for moe_route with R = k (logits is a required output;
+ *              flags: MOE_ROUTE_RENORM_TOPK only)
+ *   counts, offsets, row_token, row_gate, active
+ *              as for moe_dispatch_capacity with capacity_factor <= 0 and
+ *              ld = k: rows ordered by (expert, token)
+ *   workspace  moe_workspace_size(MOE_OP_ROUTE_DISPATCH, ...) bytes, 256-byte
+ *              aligned, ZERO-FILLED before its first use (it holds a counter
+ *              that every call leaves at zero); two calls must not use one
+ *              workspace concurrently
+ * Limits: 0 <= T <= 256, T * k <= 2048, 1 <= k <= min(16, N), N <= 256;
+ * H % 8 == 0 for BF16 x, H % 4 == 0 for F32 x.
+ */
+moe_status_t moe_route_dispatch(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int k,
+                                uint32_t flags, float* logits, int32_t* ids, float* gates,
+                                const moe_sere_params* sere, int32_t* counts, int32_t* offsets,
+                                int32_t* row_token, float* row_gate, int32_t* active, void* workspace,
+                                size_t ws_bytes, moe_dev_status* st, void* stream);
 
 /*
  * SERE batch reroute on given routing ("SERE" article, sec. 4.1: the union P
@@ -304,11 +335,13 @@ moe_status_t moe_similarity_calibrate(const void* x, int n, const void* w_gate, 
  *   r_v        [1] fp32 out (may be NULL): sum of visual weights / sum of all
  *              weights (0 when T == 0)
  *   workspace  moe_workspace_size(MOE_OP_TOKEN_WEIGHTS, T, ...) bytes (24 bytes
- *              per 8 tokens), 256-byte aligned
+ *              per 8 tokens + 16 per 256 tokens + 16), 256-byte aligned; no
+ *              initial contents needed
  * Entropies and weights are computed in fp32 (one warp per token for the
  * entropy); the statistics (count, sum and sum of squares of the visual
  * entropies, population variance) and R_v are summed in double, in a fixed
- * order, so results are reproducible.
+ * order, so results are reproducible bit for bit.  Two calls must not share
+ * a workspace concurrently (it holds a completion counter).
  * A non-finite feature sets MOE_DEV_NONFINITE (detail = token) in st.
  */
 moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
@@ -330,6 +363,7 @@ moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const f
 #define MOE_OP_FFN 2
 #define MOE_OP_CALIBRATE 3   /* moe_similarity_calibrate: T = calibration tokens n */
 #define MOE_OP_TOKEN_WEIGHTS 4   /* moe_token_weights: depends on T only */
+#define MOE_OP_ROUTE_DISPATCH 5  /* moe_route_dispatch: a fixed 512 bytes */
 
 /* Bytes of device workspace that `op` needs for these sizes (0 if none).
  * capped != 0 asks for the capacity-mode size of MOE_OP_DISPATCH; dtype

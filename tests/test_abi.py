@@ -78,6 +78,23 @@ def test_route_rejects_misaligned_and_unsupported(lib):
     assert lib.moe_route(None, 0, None, 4, 64, 8, 2, 2, 0, FAKE, FAKE, FAKE, None, None, None) == -1  # no x
 
 
+def test_route_dispatch_rejects(lib):
+    f = lib.moe_route_dispatch
+    B = (FAKE, FAKE, FAKE, FAKE, FAKE)           # counts, offsets, row_token, row_gate, active
+    W = (FAKE, 1 << 20)
+    args = lambda T=32, H=64, N=8, k=2, flags=0, sp=None, ws=W: (FAKE, 1, FAKE, T, H, N, k, flags, FAKE, FAKE, FAKE,
+                                                                    sp, *B, *ws, None, None)
+    assert f(*args(T=257)) == -2                                # above the single-launch batch limit
+    assert f(*args(flags=abi.MOE_ROUTE_FROM_LOGITS)) == -1      # logits are always computed here
+    assert f(*args(k=9)) == -1                                  # k > N
+    assert f(*args(H=60)) == -2                                 # H % 8 for bf16
+    assert f(*args(ws=(None, 0))) == -4                         # no workspace
+    assert f(*args(ws=(ctypes.c_void_p((1 << 20) + 16), 1 << 20))) == -1   # misaligned workspace
+    sp = abi._SereParams(3, 0.5, FAKE, None, None, None)        # K' > k
+    assert f(*args(sp=ctypes.byref(sp))) == -1
+    assert abi.workspace_size(abi.MOE_OP_ROUTE_DISPATCH, 32, 2048, 768, 128, 8, 8, False, 1) == 512
+
+
 def test_sere_rejects_bad_params(lib):
     sp = abi._SereParams(0, 0.5, FAKE, None, None, None)          # K' = 0
     assert lib.moe_reroute_sere(FAKE, FAKE, 4, 4, 8, 4, ctypes.byref(sp), None, None) == -1

@@ -43,7 +43,7 @@ def _run(g, L, sere, capped=False, tokens=None, max_mismatch=0):
     xabs = np.abs(L.x.astype(np.float64)) @ np.abs(L.w_r.astype(np.float64)).T
     assert np.all(np.abs(gl - ref["logits"]) <= L.H * 2.0 ** -24 * xabs + 1e-30)
     ok = _gap(ref["logits"], (L.R if capped else L.k)) >= 1e-5
-    ids = g.host(layer.out_ids[:L.T])
+    ids = g.host((layer.out_ids if capped else layer.ids)[:L.T])
     same = np.all(ids == ref["ids"], axis=1)
     # tokens whose routing differs must be near-ties of the fp32 router; with
     # capacity coupling a near-tie can move a few other tokens as well

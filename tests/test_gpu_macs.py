@@ -64,6 +64,27 @@ def test_token_weights_match_oracle(g, T, H, dtype, delta):
     assert abs(rv - rv_r) <= tol_w
 
 
+def test_token_weights_reproducible_and_without_rv(g):
+    """Bit-identical results on a repeat (fixed-order sums; the last-CTA
+    reduction of R_v does not depend on which CTA finishes last), and the
+    same weights when R_v is not requested."""
+    rng = np.random.default_rng(7)
+    T, H = 2000, 512
+    x = (rng.standard_normal((T, H)) * rng.uniform(0.2, 4.0, size=(T, 1))).astype(np.float32)
+    vis = (rng.random(T) < 0.6).astype(np.uint8)
+    x_dev = g.dev(syn.f32_to_bf16_bits(x), torch.bfloat16)
+    runs = [_gpu_weights(g, x_dev, vis, 1.5) for _ in range(3)]
+    for ent, w, rv in runs[1:]:
+        assert np.array_equal(ent, runs[0][0]) and np.array_equal(w, runs[0][1]) and rv == runs[0][2]
+    ent = torch.empty(T, dtype=torch.float32, device=g.DEV)
+    w = torch.empty(T, dtype=torch.float32, device=g.DEV)
+    st = g.status_tensor()
+    moe.moe_token_weights(x_dev, g.dev(vis), ent, w, None, 1.5, 1e-6, st)
+    torch.cuda.synchronize()
+    g.assert_status_ok(st)
+    assert np.array_equal(g.host(w), runs[0][1])
+
+
 def test_token_weights_closed_forms_on_gpu(g):
     D = 512
     x = np.zeros((4, D), np.float32)
