@@ -254,6 +254,9 @@ cudaError_t launch_similarity(const void* x, int n, const void* wg, const void* 
                                row_gate, reinterpret_cast<float4*>(rows));
     if (e != cudaSuccess) return e;
     // E_e(x_t) for every expert and token: the grouped FFN with k = N, rows_out mode
+    // (its counters start from zero; this workspace has no initial contents)
+    e = cudaMemsetAsync(b + L.ffn, 0, ffn_workspace_zero_bytes(n, H, N, N, MOE_DTYPE_BF16), s);
+    if (e != cudaSuccess) return e;
     e = launch_ffn_bf16(x, wg, wu, wd, n, H, I, N, N, offsets, row_token, row_gate, active, 0u, rows, b + L.ffn, st,
                         s);
     if (e != cudaSuccess) return e;

@@ -42,6 +42,14 @@ static long long ffn_max_items(int T, int N, int k, int nt) {
 
 static size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
+// The weight-major kernel's counters sit at the start of every bf16 FFN
+// workspace, in a region of fixed size that nothing else writes, so that a
+// workspace stays valid across calls of any batch size and either path.
+// Items of the weight-major path: min(N, T k) + ceil(T k / nt) <= 256 + 256
+// (T < 1024, k <= 16, nt = 64 above 32 tokens).
+constexpr long long kMaxStreamItems = 512;
+constexpr size_t kStreamCtrBytes = ((kMaxStreamItems + 4) * 4 + 255) & ~static_cast<size_t>(255);
+
 // Token-major workspace (byte offsets): the work counter and per-item
 // counters followed by the per-token row counts (one zeroed range), the
 // token -> rows map [T][k], A [T*k][I] bf16, the rows' activations in expert
@@ -56,8 +64,9 @@ static TmLayout tm_layout(int T, int H, int I, int N, int k) {
     const size_t M = static_cast<size_t>(T) * k;
     L.items = ffn_max_items(T, N, k, kTmRows);
     L.n_zero = L.items + 1 + T;
-    L.tok_cnt = static_cast<size_t>(L.items + 1) * 4;
-    L.tok_rows = align256(static_cast<size_t>(L.n_zero) * 4);
+    // its counters start after the weight-major kernel's region
+    L.tok_cnt = kStreamCtrBytes + static_cast<size_t>(L.items + 1) * 4;
+    L.tok_rows = kStreamCtrBytes + align256(static_cast<size_t>(L.n_zero) * 4);
     L.act = L.tok_rows + align256(M * 4);
     L.xp = L.act + align256(M * I * 2);
     L.rows = L.xp + align256(M * H * 2);
@@ -65,13 +74,23 @@ static TmLayout tm_layout(int T, int H, int I, int N, int k) {
     return L;
 }
 
-// bf16 workspace.  Weight-major: the work counter and per-item counters
-// (int32), then A [T*k][I] bf16 (row = dispatch row).  Token-major: tm_layout.
+// bf16 workspace.  Weight-major: the counters, then A [T*k][I] bf16 (row =
+// dispatch row).  Token-major: tm_layout.
 size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype) {
     if (dtype != MOE_DTYPE_BF16 || T <= 0) return 0;
     if (token_major(T, H)) return tm_layout(T, H, I, N, k).total;
-    const long long items = ffn_max_items(T, N, k, ffn_nt(T));
-    return align256(static_cast<size_t>(items + 1) * 4) + static_cast<size_t>(T) * k * I * 2;
+    return kStreamCtrBytes + static_cast<size_t>(T) * k * I * 2;
+}
+
+// Bytes at the start of the workspace that must be zero before the first
+// call (the weight-major kernel's counters; the token-major kernels clear
+// their own, which follow).
+size_t ffn_workspace_zero_bytes(int T, int H, int N, int k, int dtype) {
+    (void)H;
+    (void)N;
+    (void)k;
+    if (dtype != MOE_DTYPE_BF16 || T <= 0) return 0;
+    return kStreamCtrBytes;
 }
 
 // Items: for every active expert a, ceil(rows/NT) token chunks.  The table
@@ -99,8 +118,9 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 //   phase 1, S = I/128 units:  A[rows][slice] = silu(W_gate[slice] X^T) *
 //            (W_up[slice] X^T), the full K = H, rounded to bf16 and stored
 //            in a row-major activation buffer in the workspace;
-//   phase 2, H/128 units:      D[h-tile] = W_down[h-tile][:] A^T over the
-//            full K = I, added as gate * D into y.
+//   phase 2, H/128 units (two per H-tile, each over half of K, when a small
+//            batch would leave SMs idle): D[h-tile] = W_down[h-tile][:] A^T
+//            over K = I, added as gate * D into y.
 // A phase-2 unit starts once the S phase-1 units of its item have
 // published their part of A (a per-item counter, release/acquire).  Units
 // are handed out by a global work counter, all phase-1 units first and
@@ -127,8 +147,8 @@ struct StCfg {
     static constexpr int CW = NT / 2;               // token columns per epilogue warp
     static constexpr int QN = 4;                    // unit ids in flight between the warp roles
     static constexpr int NBAR = 2 * NSTAGE + 5 + 2 * QN;
-    static constexpr int MISC_INTS = 8 + 64;        // tmem slot, abort flag, table size, unit ring, token list
-    static constexpr int TABLE_INTS = 4 * MOE_MAX_EXPERTS + 4;
+    static constexpr int MISC_INTS = 8 + 64 + 8;    // tmem slot, abort flag, table size, unit ring, token list, exit flag
+    static constexpr int TABLE_INTS = 6 * MOE_MAX_EXPERTS + 8;   // item table + staged active[] and offsets[]
     static constexpr int SMEM =
         1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + TABLE_INTS * 4 + EPI_WARPS * 32 * 8;
     static constexpr uint32_t TMEM_COLS = 4 * NT;   // two accumulator slots of 2 x NT columns
@@ -157,7 +177,8 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                       const __grid_constant__ CUtensorMap tm_act, const int32_t* __restrict__ offsets,
                       const int32_t* __restrict__ active, const int32_t* __restrict__ row_token,
                       const float* __restrict__ row_gate, __nv_bfloat16* __restrict__ act_g, int* counters,
-                      float* __restrict__ out, int H, int I, int N, int fuse_combine, moe_dev_status* st) {
+                      int n_ctr, float* __restrict__ out, float* __restrict__ y_zero, long long y_elems, int H, int I,
+                      int N, int fuse_combine, moe_dev_status* st) {
     using C = StCfg<NT>;
     constexpr int CW = C::CW;
     extern __shared__ uint8_t smem_raw[];
@@ -174,6 +195,8 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
     int* etok_all = table + C::TABLE_INTS;           // [EPI_WARPS][32] tokens of each epilogue warp
     float* egt_all = reinterpret_cast<float*>(etok_all + C::EPI_WARPS * 32);   // [EPI_WARPS][32] their gates
     UnitTable tb{table, table + MOE_MAX_EXPERTS, table + 2 * MOE_MAX_EXPERTS, table + 3 * MOE_MAX_EXPERTS, 0};
+    int* s_act = table + 4 * MOE_MAX_EXPERTS + 4;   // [N + 1] staged copy of active[]
+    int* s_off = s_act + MOE_MAX_EXPERTS + 1;        // [N + 1] staged copy of offsets[]
 
     const uint32_t ring_a = smem_u32(ring);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
@@ -206,19 +229,47 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
         tma_prefetch_desc(&tm_act);
     }
     const int S = I / C::BI, MT = H / C::BH;
+    const int KT2 = I / (2 * C::BK);
+    int* const work_head = counters;           // next unit to hand out
+    int* const item_done = counters + 1;       // phase-1 units finished, per item
+    int* const zero_claim = counters + n_ctr;  // 4 KiB chunks of y handed out for zeroing
+    int* const zero_done = zero_claim + 1;     // chunks of y zeroed
+    int* const exit_cnt = zero_done + 1;       // CTAs that have finished
+    constexpr int kZeroChunk = 1024;           // floats per chunk of y
+    const int n_zchunks = (y_zero != nullptr) ? static_cast<int>((y_elems + kZeroChunk - 1) / kZeroChunk) : 0;
     pdl_wait();
     pdl_trigger();
+    // the producer's first unit id is fetched while the table is built
+    int first_unit = 0;
+    if (warp == 0 && lane == 0) first_unit = atomicAdd(work_head, 1);
+    // active[] and offsets[] in one round trip (independent loads), then the
+    // item table: prefix over active experts of their chunk counts
+    for (int i = threadIdx.x; i <= N; i += blockDim.x) {
+        s_act[i] = active[i];
+        s_off[i] = offsets[i];
+    }
+    __syncthreads();
+    // the last CTA to finish returns the counters to zero for the next call
+    // (every CTA passes here exactly once, whatever happened before)
+    int* const s_last = misc + 72;
+    auto finish = [&]() {
+        __syncthreads();
+        if (threadIdx.x == 0) *s_last = atom_add_acq_rel_gpu(exit_cnt, 1) == static_cast<int>(gridDim.x) - 1;
+        __syncthreads();
+        if (*s_last)
+            for (int i = threadIdx.x; i < n_ctr + 3; i += blockDim.x) counters[i] = 0;
+    };
     if (warp == 2) {
-        // item table: prefix over active experts of their chunk counts
-        const int na = min(active[0], N);
+        const int na = min(s_act[0], N);
         int run = 0;
         for (int base = 0; base < na; base += 32) {
             const int a = base + lane;
             int e = 0, r0 = 0, cnt = 0, ch = 0;
             if (a < na) {
-                e = active[1 + a];
-                r0 = offsets[e];
-                cnt = offsets[e + 1] - r0;
+                e = s_act[1 + a];
+                if (e < 0 || e >= N) e = 0;   // a corrupt list cannot index past offsets
+                r0 = s_off[e];
+                cnt = s_off[e + 1] - r0;
                 ch = (cnt + NT - 1) / NT;
             }
             int inc = ch;
@@ -243,11 +294,33 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
     }
     __syncthreads();
     tb.na = s_items[0];
-    // units: phase 1 = [0, n1) as item * S + slice, phase 2 = [n1, n1 + n2) as n1 + item * MT + h-tile
-    const int n1 = s_items[1] * S, n_total = n1 + s_items[1] * MT;
-    if (n_total == 0) return;
-    int* const work_head = counters;           // next unit to hand out
-    int* const item_done = counters + 1;       // phase-1 units finished, per item
+    // With fewer than two phase-2 units per CTA (small batches) a phase-2 unit
+    // covers half of K = I when the stages split evenly: its partial product
+    // is added into y like a whole one, and twice the units keep more SMs
+    // streaming.  (At larger batches the extra reductions into y cost more
+    // than the shorter units save.)
+    const int KP2 = (KT2 % 2 == 0 && s_items[1] * MT < 2 * static_cast<int>(gridDim.x)) ? 2 : 1;
+    const int KT2P = KT2 / KP2;
+    // units: phase 1 = [0, n1) as item * S + slice, phase 2 = [n1, n1 + n2) as
+    // n1 + (item * MT + h-tile) * KP2 + K part
+    const int n1 = s_items[1] * S, n_total = n1 + s_items[1] * MT * KP2;
+    if (n_total == 0) {
+        finish();
+        return;
+    }
+    auto decode = [&](int u, int& item, int& sub, int& part) {
+        if (u < n1) {
+            item = u / S;
+            sub = u - item * S;
+            part = 0;
+        } else {
+            const int v = u - n1;
+            item = v / (MT * KP2);
+            const int r = v - item * MT * KP2;
+            sub = r / KP2;
+            part = r - sub * KP2;
+        }
+    };
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
@@ -255,7 +328,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int KT1 = H / C::BK, KT2 = I / (2 * C::BK);
+    const int KT1 = H / C::BK;
 
     if (warp == 0) {
         // ---------------- TMA producer (lane 0 issues; the warp loads token lists) ----------------
@@ -263,8 +336,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
         int stage = 0;
         uint32_t phase = 0, pend = 0, pend_par = 0;
         bool ok = true;
-        int cur = (lane == 0) ? atomicAdd(work_head, 1) : 0;
-        cur = __shfl_sync(kFull, cur, 0);
+        int cur = __shfl_sync(kFull, first_unit, 0);
         for (int j = 0;; ++j) {
             const bool done = cur >= n_total;
             if (lane == 0) {
@@ -282,9 +354,8 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
             int nxt = 0;
             if (lane == 0) nxt = atomicAdd(work_head, 1);
             const bool p1 = cur < n1;
-            const int v = p1 ? cur : cur - n1;
-            const int item = p1 ? v / S : v / MT;
-            const int sub = p1 ? v - item * S : v - item * MT;   // I-slice or H-tile
+            int item, sub, part;   // sub: I-slice or H-tile
+            decode(cur, item, sub, part);
             int e, row0, nrows;
             item_info(tb, item, NT, e, row0, nrows);
             if (p1) {
@@ -296,7 +367,8 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                 if (!p1) {
                     // A of this item: all S phase-1 units must have published their slices
                     const unsigned long long t0 = global_ns();
-                    while (ld_acquire_gpu(item_done + item) < S) {
+                    while (ld_acquire_gpu(item_done + item) < S ||
+                           (n_zchunks > 0 && ld_acquire_gpu(zero_done) < n_zchunks)) {
                         if (*abort_flag) {
                             ok = false;
                             break;
@@ -313,7 +385,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                 }
                 const int n_g4 = (nrows + 3) / 4;
                 const int n16 = (min(NT, max(16, (nrows + 15) & ~15))) / 16;
-                const int nk = p1 ? KT1 : KT2;
+                const int nk = p1 ? KT1 : KT2P;
                 for (int kt = 0; kt < nk && ok; ++kt) {
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
@@ -331,13 +403,14 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                                         ptok[4 * g + 2], ptok[4 * g + 3], fb, pol_x);
                     } else {
                         const int wrow = e * H + sub * C::BH;
+                        const int kc = (part * KT2P + kt) * 2 * C::BK;   // first K column of this stage
                         mbar_arrive_expect_tx(fb, C::W_BYTES + 2 * n16 * 2048);
-                        tma_load_2d(dst, &tm_wd, kt * 2 * C::BK, wrow, fb, pol_w);
-                        tma_load_2d(dst + C::W_BOX, &tm_wd, kt * 2 * C::BK + C::BK, wrow, fb, pol_w);
+                        tma_load_2d(dst, &tm_wd, kc, wrow, fb, pol_w);
+                        tma_load_2d(dst + C::W_BOX, &tm_wd, kc + C::BK, wrow, fb, pol_w);
                         for (int a = 0; a < 2; ++a)
                             for (int g = 0; g < n16; ++g)
                                 tma_load_2d(dst + C::W_BYTES + a * C::X_ATOM + g * 2048, &tm_act,
-                                            kt * 2 * C::BK + a * C::BK, row0 + 16 * g, fb, pol_x);
+                                            kc + a * C::BK, row0 + 16 * g, fb, pol_x);
                     }
                     pend |= 1u << stage;
                     pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -370,8 +443,8 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                 mbar_arrive(bar(B_QEMPTY + qs));
                 if (un < 0) break;
                 const bool p1 = un < n1;
-                const int v = p1 ? un : un - n1;
-                const int item = p1 ? v / S : v / MT;
+                int item, sub, part;
+                decode(un, item, sub, part);
                 int e, row0, nrows;
                 item_info(tb, item, NT, e, row0, nrows);
                 // the MMA's N is the item's row count rounded up to 16
@@ -380,7 +453,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                 const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
                 if (!mbar_wait(bar(B_ACCE + b), ((j >> 1) & 1) ^ 1, abort_flag, st, kSiteMmaTmemFree)) break;
                 tc_fence_after();
-                const int nk = p1 ? KT1 : KT2;
+                const int nk = p1 ? KT1 : KT2P;
                 for (int kt = 0; kt < nk; ++kt) {
                     if (!mbar_wait(bar(B_FULL + stage), phase, abort_flag, st, kSiteMmaFull)) {
                         ok = false;
@@ -427,6 +500,20 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         int* etok = etok_all + (warp - 2) * 32;
         float* egt = egt_all + (warp - 2) * 32;
+        // zero y (MOE_FFN_ZERO_Y) in chunks that running warps claim, before
+        // the first accumulator is ready; phase-2 units wait for all chunks
+        // (zero_done), so only running CTAs ever hold a piece of y
+        while (n_zchunks > 0) {   // warp-uniform
+            int c = (lane == 0) ? atomicAdd(zero_claim, 1) : 0;
+            c = __shfl_sync(kFull, c, 0);
+            if (c >= n_zchunks) break;
+            const long long beg = static_cast<long long>(c) * kZeroChunk;
+            const long long end = min(beg + kZeroChunk, y_elems);
+            for (long long i = beg + lane * 4; i < end; i += 128)
+                *reinterpret_cast<float4*>(y_zero + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+            __syncwarp();
+            if (lane == 0) red_release_gpu_add(zero_done, 1);
+        }
         for (int j = 0;; ++j) {
             const int qs = j % C::QN;
             // every lane polls; the warp proceeds only if all lanes saw the phase complete
@@ -435,9 +522,8 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
             if (!named_sync_and(C::EPI_THREADS, okw)) break;
             if (un < 0) break;   // the same value in every epilogue thread
             const bool p1 = un < n1;
-            const int v = p1 ? un : un - n1;
-            const int item = p1 ? v / S : v / MT;
-            const int sub = p1 ? v - item * S : v - item * MT;
+            int item, sub, part;
+            decode(un, item, sub, part);
             int e, row0, nrows;
             item_info(tb, item, NT, e, row0, nrows);
             const int b = j & 1;
@@ -524,6 +610,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
+    finish();
 }
 
 // ---------------------------------------------------------------------------
@@ -989,11 +1076,12 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
     const bool fuse = (flags & MOE_FFN_FUSE_COMBINE) != 0;
     const long long M = static_cast<long long>(T) * k;
     const long long items = ffn_max_items(T, N, k, NT);
+    // counters: work head, per-item counters, then zero_claim, zero_done and
+    // exit_cnt; zero before the first call, and returned to zero by every call
+    if (items > kMaxStreamItems) return cudaErrorInvalidValue;
     int* counters = static_cast<int*>(ws);
-    __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + align256((items + 1) * 4));
-    cudaError_t e = launch_zero(out, (fuse && (flags & MOE_FFN_ZERO_Y)) ? static_cast<long long>(T) * H : 0, s,
-                                counters, static_cast<int>(items + 1));
-    if (e != cudaSuccess) return e;
+    __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + kStreamCtrBytes);
+    float* y_zero = (fuse && (flags & MOE_FFN_ZERO_Y)) ? out : nullptr;
     CUtensorMap tm_wg, tm_wu, tm_wd, tm_x, tm_act;
     if (!make_tmap(&tm_wg, wg, H, static_cast<uint64_t>(N) * I, 64, 128) ||
         !make_tmap(&tm_wu, wu, H, static_cast<uint64_t>(N) * I, 64, 128) ||
@@ -1016,7 +1104,8 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
     int grid = sm_count();
     if (max_units < grid) grid = static_cast<int>(max_units > 0 ? max_units : 1);
     return launch_pdl(ffn_stream_kernel<NT>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wd, tm_x,
-                      tm_act, offsets, active, row_token, row_gate, act, counters, out, H, I, N, fuse ? 1 : 0, st);
+                      tm_act, offsets, active, row_token, row_gate, act, counters, static_cast<int>(items + 1), out,
+                      y_zero, static_cast<long long>(T) * H, H, I, N, fuse ? 1 : 0, st);
 }
 
 static cudaError_t run_tokmajor(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
@@ -1028,7 +1117,7 @@ static cudaError_t run_tokmajor(const void* x, const void* wg, const void* wu, c
     const long long M = static_cast<long long>(T) * k;
     const TmLayout Lw = tm_layout(T, H, I, N, k);
     uint8_t* base = static_cast<uint8_t*>(ws);
-    int* counters = reinterpret_cast<int*>(base);
+    int* counters = reinterpret_cast<int*>(base + kStreamCtrBytes);   // tok_cnt follows the item counters
     int* tok_cnt = reinterpret_cast<int*>(base + Lw.tok_cnt);
     int* tok_rows = reinterpret_cast<int*>(base + Lw.tok_rows);
     __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(base + Lw.act);

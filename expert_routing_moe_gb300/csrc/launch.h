@@ -61,6 +61,7 @@ constexpr int kCapacityMaxT = 16384;
 
 // ---- FFN (ffn_simt.cu, ffn_tc.cu) ----
 size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype);
+size_t ffn_workspace_zero_bytes(int T, int H, int N, int k, int dtype);
 cudaError_t launch_ffn_f32(const float* x, const float* wg, const float* wu, const float* wd, int T, int H, int I,
                            int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                            const int32_t* active, uint32_t flags, float* out, moe_dev_status* st,

@@ -54,7 +54,8 @@ class MoELayer:
         wsd = abi.workspace_size(abi.MOE_OP_DISPATCH, T, H, self.I, N, k, self.R, capped, dt)
         wsf = abi.workspace_size(abi.MOE_OP_FFN, T, H, self.I, N, k, self.R, capped, dt)
         self.ws_dispatch = torch.empty(max(wsd, 256), dtype=torch.uint8, device=dev)
-        self.ws_ffn = torch.empty(max(wsf, 256), dtype=torch.uint8, device=dev)
+        # the FFN keeps counters at the start of its workspace: zero before the first call
+        self.ws_ffn = torch.zeros(max(wsf, 256), dtype=torch.uint8, device=dev)
         # the single-launch routing + dispatch keeps a counter here (zero between calls)
         wsr = abi.workspace_size(abi.MOE_OP_ROUTE_DISPATCH, T, H, self.I, N, k, self.R, False, dt)
         self.ws_route = torch.zeros(max(wsr, 256), dtype=torch.uint8, device=dev)

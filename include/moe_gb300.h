@@ -276,10 +276,15 @@ moe_status_t moe_dispatch_capacity_static(const int32_t* ids, const float* gates
  *           rows_out [T*k][H] fp32, row r = E_e(x_token(r)) without the gate
  *   workspace  device scratch of moe_workspace_size(MOE_OP_FFN, ...) bytes,
  *           256-byte aligned.  BF16 needs it: a work counter, one counter
- *           per (expert, token chunk) and the bf16 SwiGLU activations of
- *           every row (T*k*I*2 bytes plus a few KiB); F32 needs none.  Each
- *           call clears what must start at zero.  Two calls in flight at
- *           once must not share a workspace.
+ *           per (expert, token chunk), three more counters and the bf16
+ *           SwiGLU activations of every row (T*k*I*2 bytes plus a few KiB);
+ *           F32 needs none.  ZERO-FILL it once before its first use: the
+ *           counters must start at zero, and every call (including one that
+ *           reports an error in st) leaves them at zero again, so nothing
+ *           needs clearing between calls.  Two calls in flight at once must
+ *           not share a workspace.
+ *   flags   MOE_FFN_ZERO_Y: y is zeroed inside the same launch (in chunks,
+ *           all of them before any row is added into it).
  * BF16 runs on the tensor cores (tcgen05, TMA-fed) with fp32 accumulation;
  * the SwiGLU activation is rounded to bf16 before the down projection.
  * F32 runs a CUDA-core kernel in fp32.

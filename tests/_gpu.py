@@ -102,12 +102,18 @@ def gpu_dispatch(ids, gates, N, k, R, token_w=None, gamma=0.0):
     return out
 
 
-def gpu_ffn(x, w_gate, w_up, w_down, k, disp_dev, T, fuse=True):
+def ffn_workspace(x, w_gate, k, T):
     H = x.shape[1]
     N, I = w_gate.shape[0], w_gate.shape[1]
     dt = abi.MOE_DTYPE_BF16 if x.dtype == torch.bfloat16 else abi.MOE_DTYPE_F32
     ws_n = abi.workspace_size(abi.MOE_OP_FFN, T, H, I, N, k, k, False, dt)
-    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=DEV)
+    return torch.zeros(max(ws_n, 256), dtype=torch.uint8, device=DEV)   # zero before the first call
+
+
+def gpu_ffn(x, w_gate, w_up, w_down, k, disp_dev, T, fuse=True, ws=None):
+    H = x.shape[1]
+    if ws is None:
+        ws = ffn_workspace(x, w_gate, k, T)
     st = status_tensor()
     if fuse:
         y = torch.full((T, H), float("nan"), dtype=torch.float32, device=DEV)

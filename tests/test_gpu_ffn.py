@@ -110,6 +110,25 @@ def test_repeat_calls_are_stable(g, qwen):
     assert np.max(np.abs(ys[0] - ys[1])) <= 1e-4 * np.sqrt(np.mean(yref ** 2))
 
 
+def test_one_workspace_across_calls(g, qwen):
+    """The weight-major kernel leaves its counters at zero: calls that share
+    one workspace (zeroed once) agree with the oracle, across batch sizes
+    that use different unit splits, and the counter words are zero after
+    every call."""
+    L, D = qwen
+    ws = g.ffn_workspace(D.x, D.w_gate, L.k, L.T)
+    for T in (L.T, 1, 5, L.T, 3):
+        ids, gates = _route(L, L.x_bf16[:T], T)
+        d = g.gpu_dispatch(g.dev(ids), g.dev(gates), L.N, L.k, L.k)
+        for fuse in (True, False):
+            y = g.gpu_ffn(D.x[:T], D.w_gate, D.w_up, D.w_down, L.k, d["dev"], T, fuse=fuse, ws=ws)
+            yref = oracle.ffn_combine(L.x_bf16[:T], L.w_gate, L.w_up, L.w_down, ids, gates, L.k, None,
+                                      oracle.DT_BF16, oracle.DT_BF16)
+            g.assert_y_close(y, yref, "shared workspace T=%d fuse=%d" % (T, fuse))
+            # the counter region: a fixed 2304 bytes at the start of the workspace
+            assert int(ws[:2304].view(torch.int32).abs().sum().item()) == 0
+
+
 def _skewed_ids(rng, T, N, k, hot=0, hole_frac=0.1):
     """Every token routes to expert `hot` plus k-1 others: `hot` gets T rows
     (many 128-row chunks and a ragged tail), the rest a few dozen each."""
