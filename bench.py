@@ -64,6 +64,18 @@ def dist_env():
     return ws, rank, local
 
 
+def replica_inputs(rank, config_seed, n_batches):
+    """A replica's own inputs: the seed of its device-drawn weight copies and
+    the token-stream offsets of its batches.  Ranks never share a batch, so
+    N replicas process N times the tokens (weak scaling)."""
+    return config_seed + 10 * (rank + 1), [b + 97 * rank for b in range(n_batches)]
+
+
+def job_throughput(ws, tokens_per_rank_step, steps, max_ms):
+    """Whole-job tokens/s: the tokens of every rank over the slowest rank's time."""
+    return ws * tokens_per_rank_step * steps / (max_ms / 1e3)
+
+
 class ClockSampler:
     """nvidia-smi clock and throttle-reason samples while running."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -350,10 +362,11 @@ def run_ours(args):
     L = syn.decode(T)
     w_r = torch.from_numpy(L.w_r).to(dev)
     sim = torch.from_numpy(L.sim).to(dev)
-    copies = _device_copies(torch, dev, L, N_COPIES, 1000 * syn.CONFIG_DECODE + 10 * (rank + 1))
+    copy_seed, offsets = replica_inputs(rank, 1000 * syn.CONFIG_DECODE, N_BATCHES)
+    copies = _device_copies(torch, dev, L, N_COPIES, copy_seed)
     xs = []
     for bidx in range(N_BATCHES):
-        Lb = syn.decode(T, with_weights=False, token_stream_offset=bidx + 97 * rank)
+        Lb = syn.decode(T, with_weights=False, token_stream_offset=offsets[bidx])
         xs.append(torch.from_numpy(Lb.x_bf16).view(torch.bfloat16).to(dev))
     layers = [moe.MoELayer(w_r, *copies[c], k=K_TOP, max_tokens=T, sim=sim, k_primary=K_PRIMARY, rho=RHO)
               for c in range(N_COPIES)]
@@ -417,7 +430,7 @@ def run_ours(args):
     peak, peak_src = load_peaks()
     achieved = sum(ffn_bytes) / (sum(ffn_ms) / 1e3) / 1e9
     line = {
-        "metric": METRIC, "value": ws * T * args.steps / (total_ms / 1e3), "unit": UNIT, "n_gpus": ws,
+        "metric": METRIC, "value": job_throughput(ws, T, args.steps, total_ms), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Dirichlet-skewed router logits, N(0,0.02) bf16 experts)",
@@ -439,7 +452,7 @@ def run_ours(args):
         "top8": {"value": ws * T * args.steps / (t8_ms / 1e3), "ms_per_step": t8_ms / args.steps,
                  "ffn_ms_mean": float(np.mean(t8_ffn_ms)),
                  "ffn_gbs": sum(t8_bytes) / (sum(t8_ffn_ms) / 1e3) / 1e9},
-        "e2e": {"value": ws * T * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
+        "e2e": {"value": job_throughput(ws, T, args.steps, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 4},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
