@@ -43,8 +43,11 @@ struct DispatchWs {
     const float* r_v;     // [1] effective visual ratio, with bias
 };
 
+// Tokens per block of the multi-block permutation (below).
+constexpr int kMbBlk = 256;
+
 static size_t carve(DispatchWs* w, void* base, int T, int N, int k, bool capped) {
-    const int nblk = (T + kBlk - 1) / kBlk;
+    const int nblk = (T + kMbBlk - 1) / kMbBlk;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
@@ -109,16 +112,44 @@ __global__ void __launch_bounds__(kBlk) permute_single_kernel(const int32_t* __r
     write_rows(ids, gates, ld, T, N, k, 0, nw, bits, start, row_token, row_gate, out_ids, out_gates, slot_row);
 }
 
-// Multi-block permutation, pass 1: per-block expert counts.
-__global__ void __launch_bounds__(kBlk) permute_count_kernel(const int32_t* __restrict__ ids, int ld, int T, int N,
-                                                             int k, int32_t* __restrict__ blk_cnt,
-                                                             moe_dev_status* st) {
+// Multi-block permutation over blocks of kMbBlk tokens (more, smaller
+// blocks keep more SMs busy at prefill sizes).  The presence bitmap of a
+// block has kMbWords words per expert, stored with a stride of kMbWords + 1
+// so that lanes reading different experts' words rarely share a bank.
+constexpr int kMbWords = kMbBlk / 32;
+constexpr int kMbStride = kMbWords + 1;
+
+// Marks bit (t mod 32) of word (t / 32) of expert e for every slot of token t
+// of block b holding e.
+__device__ __forceinline__ void mb_presence(const int32_t* __restrict__ ids, int ld, int T, int N, int k, int b,
+                                            uint32_t* bits, moe_dev_status* st) {
+    for (int i = threadIdx.x; i < N * kMbStride; i += blockDim.x) bits[i] = 0u;
+    __syncthreads();
+    const int t = b * kMbBlk + threadIdx.x;
+    if (t < T) {
+        for (int r = 0; r < k; ++r) {
+            const int e = ids[static_cast<size_t>(t) * ld + r];
+            if (e >= N && st != nullptr) report(st, MOE_DEV_BAD_INDEX, e);
+            if (e >= 0 && e < N) atomicOr(&bits[e * kMbStride + (threadIdx.x >> 5)], 1u << (threadIdx.x & 31));
+        }
+    }
+    __syncthreads();
+}
+
+// Pass 1: per-block expert counts.
+__global__ void __launch_bounds__(kMbBlk) permute_count_kernel(const int32_t* __restrict__ ids, int ld, int T, int N,
+                                                               int k, int32_t* __restrict__ blk_cnt,
+                                                               moe_dev_status* st) {
     pdl_wait();
     pdl_trigger();
-    __shared__ uint32_t bits[MOE_MAX_EXPERTS * kWordsPerBlk];
-    presence_bits(ids, ld, T, N, k, blockIdx.x, kWordsPerBlk, bits, st);
-    for (int e = threadIdx.x; e < N; e += blockDim.x)
-        blk_cnt[static_cast<size_t>(blockIdx.x) * N + e] = block_count(bits, e, kWordsPerBlk);
+    __shared__ uint32_t bits[MOE_MAX_EXPERTS * kMbStride];
+    mb_presence(ids, ld, T, N, k, blockIdx.x, bits, st);
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kMbWords; ++w) c += __popc(bits[e * kMbStride + w]);
+        blk_cnt[static_cast<size_t>(blockIdx.x) * N + e] = c;
+    }
 }
 
 // Pass 2 (one CTA): totals, offsets, active list; blk_cnt becomes the
@@ -145,21 +176,49 @@ __global__ void __launch_bounds__(256) permute_scan_kernel(int nblk, int N, int3
         for (int b = 0; b < nblk; ++b) blk_cnt[static_cast<size_t>(b) * N + e] += start[e];
 }
 
-// Pass 3: rows of each block.
-__global__ void __launch_bounds__(kBlk) permute_rows_kernel(const int32_t* __restrict__ ids,
-                                                            const float* __restrict__ gates, int ld, int T, int N,
-                                                            int k, const int32_t* __restrict__ blk_start,
-                                                            int32_t* row_token, float* row_gate, int32_t* out_ids,
-                                                            float* out_gates, int32_t* slot_row,
-                                                            moe_dev_status* st) {
+// Pass 3: rows of each block.  pre[e][w] = start of expert e in this block
+// plus the set bits of its words before w, so a slot's row is pre[e][w] plus
+// the set bits below its token in word w: (expert, token) order, as in the
+// single-block kernel.
+__global__ void __launch_bounds__(kMbBlk) permute_rows_kernel(const int32_t* __restrict__ ids,
+                                                              const float* __restrict__ gates, int ld, int T, int N,
+                                                              int k, const int32_t* __restrict__ blk_start,
+                                                              int32_t* row_token, float* row_gate, int32_t* out_ids,
+                                                              float* out_gates, int32_t* slot_row,
+                                                              moe_dev_status* st) {
     pdl_wait();
     pdl_trigger();
-    __shared__ uint32_t bits[MOE_MAX_EXPERTS * kWordsPerBlk];
-    __shared__ int start[MOE_MAX_EXPERTS];
-    for (int e = threadIdx.x; e < N; e += blockDim.x) start[e] = blk_start[static_cast<size_t>(blockIdx.x) * N + e];
-    presence_bits(ids, ld, T, N, k, blockIdx.x, kWordsPerBlk, bits, nullptr);
-    write_rows(ids, gates, ld, T, N, k, blockIdx.x, kWordsPerBlk, bits, start, row_token, row_gate, out_ids,
-               out_gates, slot_row);
+    __shared__ uint32_t bits[MOE_MAX_EXPERTS * kMbStride];
+    __shared__ int pre[MOE_MAX_EXPERTS * kMbStride];
+    mb_presence(ids, ld, T, N, k, blockIdx.x, bits, nullptr);
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int run = blk_start[static_cast<size_t>(blockIdx.x) * N + e];
+#pragma unroll
+        for (int w = 0; w < kMbWords; ++w) {
+            pre[e * kMbStride + w] = run;
+            run += __popc(bits[e * kMbStride + w]);
+        }
+    }
+    __syncthreads();
+    const int t = blockIdx.x * kMbBlk + threadIdx.x;
+    if (t >= T) return;
+    const int w0 = threadIdx.x >> 5;
+    const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
+    for (int r = 0; r < k; ++r) {
+        const size_t si = static_cast<size_t>(t) * ld + r;
+        const size_t so = static_cast<size_t>(t) * k + r;
+        const int e = ids[si];
+        const float g = gates[si];
+        int row = -1;
+        if (e >= 0 && e < N) {
+            row = pre[e * kMbStride + w0] + __popc(bits[e * kMbStride + w0] & below);
+            row_token[row] = t;
+            row_gate[row] = g;
+        }
+        if (slot_row) slot_row[so] = row;
+        if (out_ids) out_ids[so] = (row >= 0) ? e : -1;
+        if (out_gates) out_gates[so] = (row >= 0) ? g : 0.f;
+    }
     (void)st;
 }
 
@@ -167,17 +226,17 @@ static cudaError_t launch_permute(const int32_t* ids, const float* gates, int ld
                                   int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,
                                   int32_t* active, int32_t* out_ids, float* out_gates, int32_t* slot_row,
                                   int32_t* blk_start, moe_dev_status* st, cudaStream_t s) {
-    const int nblk = (T + kBlk - 1) / kBlk;
-    if (nblk <= 1) {
+    if (T <= kBlk) {
         const int threads = T <= 128 ? 128 : (T + 31) / 32 * 32;
         return launch_pdl(permute_single_kernel, dim3(1), dim3(threads), 0, s, ids, gates, ld, T, N, k, counts,
                           offsets, row_token, row_gate, active, out_ids, out_gates, slot_row, st);
     }
-    cudaError_t e = launch_pdl(permute_count_kernel, dim3(nblk), dim3(kBlk), 0, s, ids, ld, T, N, k, blk_start, st);
+    const int nblk = (T + kMbBlk - 1) / kMbBlk;
+    cudaError_t e = launch_pdl(permute_count_kernel, dim3(nblk), dim3(kMbBlk), 0, s, ids, ld, T, N, k, blk_start, st);
     if (e != cudaSuccess) return e;
     e = launch_pdl(permute_scan_kernel, dim3(1), dim3(256), 0, s, nblk, N, blk_start, counts, offsets, active);
     if (e != cudaSuccess) return e;
-    return launch_pdl(permute_rows_kernel, dim3(nblk), dim3(kBlk), 0, s, ids, gates, ld, T, N, k,
+    return launch_pdl(permute_rows_kernel, dim3(nblk), dim3(kMbBlk), 0, s, ids, gates, ld, T, N, k,
                       static_cast<const int32_t*>(blk_start), row_token, row_gate, out_ids, out_gates, slot_row, st);
 }
 
