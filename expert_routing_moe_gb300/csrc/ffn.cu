@@ -1003,55 +1003,91 @@ __global__ void __launch_bounds__(256) ffn_tm_prep_kernel(const uint4* __restric
     const int M = offsets[N];
     const int v = H / 8;
     const int lane = threadIdx.x & 31;
+    // one warp per row, a row's 16-byte loads issued 8 at a time before the stores
     for (int r = gtid >> 5; r < M; r += nthr >> 5) {
         const uint4* src = x + static_cast<size_t>(row_token[r]) * v;
         uint4* d = xp + static_cast<size_t>(r) * v;
-        for (int c = lane; c < v; c += 32) d[c] = src[c];
+        for (int c0 = lane; c0 < v; c0 += 32 * 8) {
+            uint4 q[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int c = c0 + 32 * m;
+                q[m] = (c < v) ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int c = c0 + 32 * m;
+                if (c < v) d[c] = q[m];
+            }
+        }
     }
 }
 
 // Token-major path, after the FFN kernel: y[t] = (y[t] or 0) + sum over the
-// token's rows, in ascending row order, of gate * E_e(x_t).
+// token's rows, in ascending row order, of gate * E_e(x_t).  Per token, warp
+// 0 reads the row list in one round trip and ranks the rows with shuffles
+// (a token's rows are distinct), then every thread issues all of its row
+// loads before adding them up in that order.
+template <int KMAX>
 __global__ void __launch_bounds__(256) ffn_tm_combine_kernel(const float* __restrict__ rows,
                                                              const int* __restrict__ tok_cnt,
                                                              const int* __restrict__ tok_rows,
                                                              const float* __restrict__ row_gate, int T, int H,
                                                              int k, int zero_y, float* __restrict__ y) {
-    __shared__ int srow[MOE_MAX_RANKS];
-    __shared__ float sg[MOE_MAX_RANKS];
+    __shared__ int srow[KMAX];
+    __shared__ float sg[KMAX];
     __shared__ int sn;
     pdl_wait();
     pdl_trigger();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H4 = H / 4;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        if (threadIdx.x == 0) {
+        if (warp == 0) {
             const int n = min(tok_cnt[t], k);
-            for (int i = 0; i < n; ++i) {
-                const int v = tok_rows[static_cast<size_t>(t) * k + i];
-                int j = i;
-                while (j > 0 && srow[j - 1] > v) {
-                    srow[j] = srow[j - 1];
-                    --j;
-                }
-                srow[j] = v;
+            const int v = (lane < k) ? tok_rows[static_cast<size_t>(t) * k + lane] : 0;
+            int rank = 0;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                const int vj = __shfl_sync(kFull, v, j);
+                if (j < n && vj < v) ++rank;
             }
-            for (int i = 0; i < n; ++i) sg[i] = row_gate[srow[i]];
-            sn = n;
+            if (lane < n) {
+                srow[rank] = v;
+                sg[rank] = row_gate[v];
+            }
+            if (lane == 0) sn = n;
         }
         __syncthreads();
         const int n = sn;
         float4* yt = reinterpret_cast<float4*>(y + static_cast<size_t>(t) * H);
-        for (int h4 = threadIdx.x; h4 < H / 4; h4 += 256) {
-            float4 a = zero_y ? make_float4(0.f, 0.f, 0.f, 0.f) : yt[h4];
-            for (int i = 0; i < n; ++i) {
-                const float4 v = reinterpret_cast<const float4*>(rows + static_cast<size_t>(srow[i]) * H)[h4];
-                a.x = fmaf(sg[i], v.x, a.x);
-                a.y = fmaf(sg[i], v.y, a.y);
-                a.z = fmaf(sg[i], v.z, a.z);
-                a.w = fmaf(sg[i], v.w, a.w);
+        for (int hb = threadIdx.x; hb < H4; hb += 2 * 256) {
+            float4 v[KMAX][2];
+#pragma unroll
+            for (int i = 0; i < KMAX; ++i)
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int h4 = hb + 256 * m;
+                    v[i][m] = (i < n && h4 < H4) ? reinterpret_cast<const float4*>(rows + static_cast<size_t>(srow[i]) * H)[h4]
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int h4 = hb + 256 * m;
+                if (h4 >= H4) break;
+                float4 acc = zero_y ? make_float4(0.f, 0.f, 0.f, 0.f) : yt[h4];
+#pragma unroll
+                for (int i = 0; i < KMAX; ++i) {
+                    if (i < n) {
+                        acc.x = fmaf(sg[i], v[i][m].x, acc.x);
+                        acc.y = fmaf(sg[i], v[i][m].y, acc.y);
+                        acc.z = fmaf(sg[i], v[i][m].z, acc.z);
+                        acc.w = fmaf(sg[i], v[i][m].w, acc.w);
+                    }
+                }
+                yt[h4] = acc;
             }
-            yt[h4] = a;
         }
-        __syncthreads();
+        __syncthreads();   // the row list is read by every thread before the next token's
     }
 }
 
@@ -1152,9 +1188,13 @@ static cudaError_t run_tokmajor(const void* x, const void* wg, const void* wu, c
                    fuse ? rows : out, fuse ? 0 : 1, H, I, N, k, st);
     if (e != cudaSuccess || !fuse) return e;
     const int cgrid = T < 8 * sms ? T : 8 * sms;
-    return launch_pdl(ffn_tm_combine_kernel, dim3(cgrid), dim3(256), 0, s, static_cast<const float*>(rows),
-                      static_cast<const int*>(tok_cnt), static_cast<const int*>(tok_rows), row_gate, T, H, k,
-                      (flags & MOE_FFN_ZERO_Y) ? 1 : 0, out);
+    if (k <= 8)
+        return launch_pdl(ffn_tm_combine_kernel<8>, dim3(cgrid), dim3(256), 0, s, static_cast<const float*>(rows),
+                          static_cast<const int*>(tok_cnt), static_cast<const int*>(tok_rows), row_gate, T, H, k,
+                          (flags & MOE_FFN_ZERO_Y) ? 1 : 0, out);
+    return launch_pdl(ffn_tm_combine_kernel<MOE_MAX_RANKS>, dim3(cgrid), dim3(256), 0, s,
+                      static_cast<const float*>(rows), static_cast<const int*>(tok_cnt),
+                      static_cast<const int*>(tok_rows), row_gate, T, H, k, (flags & MOE_FFN_ZERO_Y) ? 1 : 0, out);
 }
 
 cudaError_t launch_ffn_bf16(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
