@@ -152,28 +152,37 @@ __global__ void __launch_bounds__(kMbBlk) permute_count_kernel(const int32_t* __
     }
 }
 
-// Pass 2 (one CTA): totals, offsets, active list; blk_cnt becomes the
-// absolute start row of each (block, expert).
-__global__ void __launch_bounds__(256) permute_scan_kernel(int nblk, int N, int32_t* __restrict__ blk_cnt,
-                                                           int32_t* counts, int32_t* offsets, int32_t* active) {
+// Pass 2 (one CTA of 1024 threads): totals, offsets, active list; blk_cnt
+// becomes the absolute start row of each (block, expert).  One warp per
+// expert scans its block counts, 32 blocks per lane pass (all loads issued
+// first); integer sums, so the order of the adds does not matter.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int nblk, int N, int32_t* __restrict__ blk_cnt,
+                                                            int32_t* counts, int32_t* offsets, int32_t* active) {
     pdl_wait();
     pdl_trigger();
     __shared__ int tot[MOE_MAX_EXPERTS];
     __shared__ int start[MOE_MAX_EXPERTS];
-    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int e = warp; e < N; e += nwarps) {
         int run = 0;
-        for (int b = 0; b < nblk; ++b) {
-            const int c = blk_cnt[static_cast<size_t>(b) * N + e];
-            blk_cnt[static_cast<size_t>(b) * N + e] = run;
-            run += c;
+        for (int b0 = 0; b0 < nblk; b0 += 32) {
+            const int b = b0 + lane;
+            const int c = (b < nblk) ? blk_cnt[static_cast<size_t>(b) * N + e] : 0;
+            int inc = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(kFull, inc, off);
+                if (lane >= off) inc += o;
+            }
+            if (b < nblk) blk_cnt[static_cast<size_t>(b) * N + e] = run + inc - c;
+            run += __shfl_sync(kFull, inc, 31);
         }
-        tot[e] = run;
+        if (lane == 0) tot[e] = run;
     }
     __syncthreads();
     scan_experts(tot, N, counts, offsets, active, start);
     __syncthreads();
-    for (int e = threadIdx.x; e < N; e += blockDim.x)
-        for (int b = 0; b < nblk; ++b) blk_cnt[static_cast<size_t>(b) * N + e] += start[e];
+    for (int i = threadIdx.x; i < nblk * N; i += blockDim.x) blk_cnt[i] += start[i % N];
 }
 
 // Pass 3: rows of each block.  pre[e][w] = start of expert e in this block
@@ -234,7 +243,7 @@ static cudaError_t launch_permute(const int32_t* ids, const float* gates, int ld
     const int nblk = (T + kMbBlk - 1) / kMbBlk;
     cudaError_t e = launch_pdl(permute_count_kernel, dim3(nblk), dim3(kMbBlk), 0, s, ids, ld, T, N, k, blk_start, st);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(256), 0, s, nblk, N, blk_start, counts, offsets, active);
+    e = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, s, nblk, N, blk_start, counts, offsets, active);
     if (e != cudaSuccess) return e;
     return launch_pdl(permute_rows_kernel, dim3(nblk), dim3(kMbBlk), 0, s, ids, gates, ld, T, N, k,
                       static_cast<const int32_t*>(blk_start), row_token, row_gate, out_ids, out_gates, slot_row, st);
@@ -522,14 +531,18 @@ __global__ void __launch_bounds__(1024) cap_admit_kernel(const float* __restrict
             __syncthreads();
         }
     }
-    // running weight through b* in sorted order (m is small: one thread walks it when m <= 64)
+    // running weight through b* in sorted order (m is small: one thread walks it when m <= 64,
+    // the weights fetched into shared memory first in one parallel round trip; wts[] is free now)
     if (m <= 64) {
+        if (threadIdx.x < m)
+            wts[threadIdx.x] = cap_weight(token_w, static_cast<int>((keys[threadIdx.x] & 0xffffffffull) >> 4));
+        __syncthreads();
         if (threadIdx.x == 0) {
             long long cum = base + excl;
             unsigned long long adm = 0ull;
             for (int i = 0; i < m; ++i) {
                 const uint32_t tr = static_cast<uint32_t>(keys[i] & 0xffffffffull);
-                cum += fixed_weight(cap_weight(token_w, static_cast<int>(tr >> 4)));
+                cum += fixed_weight(wts[i]);
                 if (cum > C) break;
                 admit(tr);
                 adm = static_cast<unsigned long long>(cum - base - excl);
