@@ -104,23 +104,29 @@ class MoELayer:
                                   modality_bias=self.modality_bias if self.capacity_factor > 0 else None,
                                   r_v=self.r_v if self.capacity_factor > 0 else None)
 
-    def ffn(self, x: torch.Tensor, stream=None, accumulate_into: Optional[torch.Tensor] = None):
-        """y = sum_j G_j E_j(x) into the layer's buffer, or added to
-        `accumulate_into` ([T][H] fp32, e.g. a residual stream)."""
+    def ffn(self, x: torch.Tensor, stream=None, accumulate_into: Optional[torch.Tensor] = None,
+            out: Optional[torch.Tensor] = None):
+        """y = sum_j G_j E_j(x) into `out` ([T][H] fp32) or the layer's buffer,
+        or added to `accumulate_into` ([T][H] fp32, e.g. a residual stream)."""
         T = x.shape[0]
-        out = self.y[:T] if accumulate_into is None else accumulate_into
-        flags = abi.MOE_FFN_FUSE_COMBINE | (abi.MOE_FFN_ZERO_Y if accumulate_into is None else 0)
+        if accumulate_into is not None:
+            out, flags = accumulate_into, abi.MOE_FFN_FUSE_COMBINE
+        else:
+            out = self.y[:T] if out is None else out
+            flags = abi.MOE_FFN_FUSE_COMBINE | abi.MOE_FFN_ZERO_Y
         abi.moe_ffn_grouped(x, self.w_gate, self.w_up, self.w_down, self.k, self.offsets, self.row_token,
                             self.row_gate, self.active, out, self.ws_ffn, flags, self.status, stream)
 
-    def forward(self, x: torch.Tensor, sere: bool = False, token_w: Optional[torch.Tensor] = None, stream=None):
-        """y[T][H] fp32 (a view of the layer's output buffer)."""
+    def forward(self, x: torch.Tensor, sere: bool = False, token_w: Optional[torch.Tensor] = None, stream=None,
+                out: Optional[torch.Tensor] = None):
+        """y[T][H] fp32: written into `out` if given, else into (a view of)
+        the layer's output buffer."""
         T = x.shape[0]
         if T > self.max_T:
             raise abi.MoeError("batch %d exceeds the layer's max_tokens %d" % (T, self.max_T))
         self.route_and_dispatch(x, sere, token_w, stream)
-        self.ffn(x, stream)
-        return self.y[:T]
+        self.ffn(x, stream, out=out)
+        return self.y[:T] if out is None else out
 
     def device_status(self):
         code, detail = (int(v) for v in self.status.tolist())

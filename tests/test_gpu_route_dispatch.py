@@ -193,3 +193,32 @@ def test_layer_forward_uses_single_launch_path(g):
     assert np.array_equal(rows1, rows2)
     assert torch.equal(y1, lay.y[:L.T]) or float((y1 - lay.y[:L.T]).abs().max()) <= 1e-6 * float(
         y1.abs().max())
+    # the same layer into a caller's buffer (zeroed inside the FFN launch)
+    buf = torch.full((L.T, L.H), float("nan"), dtype=torch.float32, device="cuda:0")
+    y3 = lay.forward(D.x, sere=True, out=buf)
+    torch.cuda.synchronize()
+    assert y3.data_ptr() == buf.data_ptr()
+    assert float((y3 - y1).abs().max()) <= 1e-6 * float(y1.abs().max())
+
+
+@pytest.mark.parametrize("T,N,k,H", [(128, 256, 16, 256), (100, 200, 12, 192), (256, 96, 8, 128)])
+def test_limits_and_ragged_tiles(g, ws, T, N, k, H):
+    """The largest slot count (T k = 2048) with N = 256 and k = 16, an expert
+    count that is not a multiple of 32 (partial last lane word) and of the
+    router tile of 8, and bf16 x: bit-identical to the separate calls and
+    to the oracle given the kernel's logits, with and without SERE."""
+    rng = np.random.default_rng(T + N + k)
+    x = syn.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    w_r = (rng.standard_normal((N, H)) / np.sqrt(H)).astype(np.float32)
+    sim = rng.uniform(0, 1, (N, N)).astype(np.float32)
+    sim = ((sim + sim.T) / 2).astype(np.float32)
+    np.fill_diagonal(sim, 1.0)
+    prot = (rng.random(N) < 0.1).astype(np.uint8)
+    x_dev, w_dev = g.dev(x, torch.bfloat16), g.dev(w_r)
+    for sere in (False, True):
+        kw = dict(sim=g.dev(sim), kp=3, rho=0.45, protect=g.dev(prot)) if sere else {}
+        f = _fused(g, x_dev, w_dev, k, ws, **kw)
+        s = _separate(g, x_dev, w_dev, k, **kw)
+        for name in f:
+            _same_bits(f[name], s[name], name)
+        _check_oracle(f, k, N, **(dict(sim=sim, kp=3, rho=0.45, protect=prot) if sere else {}))
