@@ -5,6 +5,8 @@ import pytest
 import torch
 
 import oracle
+import expert_routing_moe_gb300 as moe
+from expert_routing_moe_gb300 import _abi as abi
 from expert_routing_moe_gb300 import synthetic as syn
 
 pytestmark = pytest.mark.gpu
@@ -168,3 +170,36 @@ def test_token_major_prefill_shape_sampled(g, qwen):
     ids, gates = _route(L, Lt.x_bf16, Lt.T)
     tokens = np.arange(0, Lt.T, 337, dtype=np.int32)
     _ffn_case(g, L, D, Lt.x_bf16, x_dev, ids, gates, tokens)
+
+
+def test_dependency_wait_times_out_cleanly(g, qwen):
+    """Failure detection without a fault: the work counter is preset past the
+    phase-1 units, so every CTA draws only phase-2 units whose activations
+    nothing will publish (a flag that nothing sets).  The bounded wait runs
+    out, the launch reports MOE_DEV_TIMEOUT at the dependency site and
+    returns; the last CTA still returns the counters to zero, so the same
+    workspace then serves a normal call."""
+    L, D = qwen
+    ids, gates = _route(L, L.x_bf16, L.T)
+    d = g.gpu_dispatch(g.dev(ids), g.dev(gates), L.N, L.k, L.k)
+    ws = g.ffn_workspace(D.x, D.w_gate, L.k, L.T)
+    # batch 32: one 32-row chunk per active expert, S = I / 128 phase-1 units each
+    n1 = int(d["active"][0]) * (L.I // 128)
+    ws[:4].view(torch.int32)[0] = n1
+    y = torch.full((L.T, L.H), float("nan"), dtype=torch.float32, device=g.DEV)
+    st = g.status_tensor()
+    moe.moe_ffn_grouped(D.x, D.w_gate, D.w_up, D.w_down, L.k, d["dev"]["offsets"], d["dev"]["row_token"],
+                        d["dev"]["row_gate"], d["dev"]["active"], y, ws, abi.MOE_FFN_FUSE_COMBINE | abi.MOE_FFN_ZERO_Y,
+                        st)
+    torch.cuda.synchronize()
+    code, detail = (int(v) for v in st.tolist())
+    assert code == abi.MOE_DEV_TIMEOUT, (code, detail)
+    # the dependency wait, or a wait of another warp role on the same missing data
+    # (the first one to give up reports its site)
+    assert 1 <= detail <= 10, detail
+    assert int(ws[:2304].view(torch.int32).abs().sum().item()) == 0
+    # the context and the workspace are usable again
+    y2 = g.gpu_ffn(D.x, D.w_gate, D.w_up, D.w_down, L.k, d["dev"], L.T, ws=ws)
+    yref = oracle.ffn_combine(L.x_bf16, L.w_gate, L.w_up, L.w_down, ids, gates, L.k, None, oracle.DT_BF16,
+                              oracle.DT_BF16)
+    g.assert_y_close(y2, yref, "after a timed-out call")
