@@ -297,6 +297,50 @@ def _timed_steps(torch, stream, graphs, steps, warmup, ws, group=1):
     return e0.elapsed_time(e1), reps * group
 
 
+def _ffn_inline(torch, stream, layers, xs, sere, rounds=3, group=STEP_GROUP):
+    """Each FFN call's own duration inside graphs of `group` layer steps:
+    timing events captured right before and after every FFN call (external
+    event-record nodes), each graph replayed and its events read back, over
+    `rounds` passes of every graph.  Returns the durations (ms) and the batch
+    index of each, or None where this PyTorch cannot record events in a
+    graph."""
+    nb = len(xs)
+    try:
+        graphs, evs = [], []
+        with torch.cuda.stream(stream):
+            for b0 in range(nb):
+                pairs = [(torch.cuda.Event(enable_timing=True, external=True),
+                          torch.cuda.Event(enable_timing=True, external=True)) for _ in range(group)]
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(group):
+                        b = (b0 + i) % nb
+                        lay = layers[b % len(layers)]
+                        lay.route_and_dispatch(xs[b], sere)
+                        pairs[i][0].record(stream)
+                        lay.ffn(xs[b])
+                        pairs[i][1].record(stream)
+                graphs.append(g)
+                evs.append(pairs)
+        torch.cuda.synchronize()
+        ms, bidx = [], []
+        with torch.cuda.stream(stream):
+            for g in graphs:   # warm-up pass
+                g.replay()
+            torch.cuda.synchronize()
+            for _ in range(rounds):
+                for b0, g in enumerate(graphs):
+                    g.replay()
+                    stream.synchronize()
+                    for i, (a, e) in enumerate(evs[b0]):
+                        ms.append(a.elapsed_time(e))
+                        bidx.append((b0 + i) % nb)
+        del graphs
+        return ms, bidx
+    except (TypeError, RuntimeError):
+        return None
+
+
 def _active_counts(torch, moe, stream, layers, xs, sere, token_w=None):
     us, rows = [], []
     for bidx, x in enumerate(xs):
@@ -401,14 +445,27 @@ def run_ours(args):
     # the headline: whole layer steps, STEP_GROUP per graph
     total_ms, steps_t = _timed_steps(torch, stream, s_sere, args.steps, args.warmup, ws, group=STEP_GROUP)
     total_ms = _max_over_ranks(torch, dev, ws, total_ms)
-    # the FFN's own duration: the same steps as a routing graph and an FFN graph with events between
-    _, ffn_ms = _timed(torch, stream, g_sere, args.steps, args.warmup, ws)
+    # the FFN's own duration: events around every FFN call inside the step graphs (else,
+    # where events cannot be captured, a routing graph and an FFN graph with events between)
+    inline = _ffn_inline(torch, stream, layers, xs, True)
+    if inline is not None:
+        ffn_ms, ffn_b = inline
+        ffn_how = "events captured around every FFN call inside graphs of %d steps" % STEP_GROUP
+    else:
+        _, ffn_ms = _timed(torch, stream, g_sere, args.steps, args.warmup, ws)
+        ffn_b = [i % N_BATCHES for i in range(args.steps)]
+        ffn_how = "events between a routing graph and an FFN graph per step"
     clocks = clk.stop()
-    ffn_bytes = [us_sere[i % N_BATCHES] * EXPERT_BYTES + T * H * 2 + T * H * 4 for i in range(args.steps)]
+    ffn_bytes = [us_sere[b] * EXPERT_BYTES + T * H * 2 + T * H * 4 for b in ffn_b]
     t8_ms, t8_steps = _timed_steps(torch, stream, s_top8, args.steps, args.warmup, ws, group=STEP_GROUP)
     t8_ms = _max_over_ranks(torch, dev, ws, t8_ms)
-    _, t8_ffn_ms = _timed(torch, stream, g_top8, args.steps, args.warmup, ws)
-    t8_bytes = [us_top8[i % N_BATCHES] * EXPERT_BYTES + T * H * 2 + T * H * 4 for i in range(args.steps)]
+    inline8 = _ffn_inline(torch, stream, layers, xs, False)
+    if inline8 is not None:
+        t8_ffn_ms, t8_b = inline8
+    else:
+        _, t8_ffn_ms = _timed(torch, stream, g_top8, args.steps, args.warmup, ws)
+        t8_b = [i % N_BATCHES for i in range(args.steps)]
+    t8_bytes = [us_top8[b] * EXPERT_BYTES + T * H * 2 + T * H * 4 for b in t8_b]
 
     # ---- end to end through the public API: pinned host x in, host y out, every step ----
     # The copies run on their own stream, overlapped with the layer: step i+1's
@@ -491,9 +548,8 @@ def run_ours(args):
         "config": workload_config({"parallelism": "replicas" if ws > 1 else "single GPU",
                                    "cuda_graphs": "value: graphs of 16 layer steps, each step the single-launch "
                                                   "router + rank + SERE + permutation and then the FFN, on "
-                                                  "its own batch and weight copy; roofline: a second timed run of the same "
-                                                  "steps as a routing graph and an FFN graph with CUDA events "
-                                                  "around the FFN graph; e2e: groups of 16 steps, each step "
+                                                  "its own batch and weight copy; roofline: " + ffn_how +
+                                                  "; e2e: groups of 16 steps, each step "
                                                   "uploading its x from pinned host memory and reading its y "
                                                   "back on a copy stream overlapped with the layer, captured "
                                                   "as one graph and replayed"}),
