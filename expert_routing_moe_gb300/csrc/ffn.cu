@@ -130,7 +130,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 // phase-1 units already taken, so the waits end whatever the residency of
 // the grid; a wait that outlasts kWaitLimitNs reports MOE_DEV_TIMEOUT.
 // ---------------------------------------------------------------------------
-template <int NT>
+template <int NT, bool STK = false>
 struct StCfg {
     static constexpr int BI = 128;                  // I-slice of a phase-1 unit (MMA M)
     static constexpr int BH = 128;                  // H-tile of a phase-2 unit (MMA M)
@@ -140,7 +140,7 @@ struct StCfg {
     static constexpr int X_ATOM = NT * 128;         // NT rows of one 64-column swizzle atom
     static constexpr int X_BYTES = 2 * X_ATOM;      // phase 2 stages 128 columns of A
     static constexpr int STAGE = W_BYTES + X_BYTES;
-    static constexpr int NSTAGE = NT <= 16 ? 6 : (NT <= 32 ? 5 : 4);
+    static constexpr int NSTAGE = NT <= 16 ? (STK ? 5 : 6) : (NT <= 32 ? 5 : 4);
     static constexpr int EPI_WARPS = 8;             // two warps per TMEM lane quadrant
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
@@ -149,8 +149,9 @@ struct StCfg {
     static constexpr int NBAR = 2 * NSTAGE + 5 + 2 * QN;
     static constexpr int MISC_INTS = 8 + 64 + 8;    // tmem slot, abort flag, table size, unit ring, token list, exit flag
     static constexpr int TABLE_INTS = 6 * MOE_MAX_EXPERTS + 8;   // item table + staged active[] and offsets[]
+    static constexpr int XCH_BYTES = STK ? 64 * NT * 4 : 0;   // up values of a stacked phase-1 unit
     static constexpr int SMEM =
-        1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + TABLE_INTS * 4 + EPI_WARPS * 32 * 8;
+        1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + TABLE_INTS * 4 + EPI_WARPS * 32 * 8 + XCH_BYTES;
     static constexpr uint32_t TMEM_COLS = 4 * NT;   // two accumulator slots of 2 x NT columns
     static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
     static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256, "TMEM allocation");
@@ -170,16 +171,17 @@ __device__ __forceinline__ void item_info(const UnitTable& tb, int item, int NT,
     nrows = min(NT, tb.cnt[lo] - c * NT);
 }
 
-template <int NT>
-__global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
+template <int NT, bool STK>
+__global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
     ffn_stream_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
+                      const __grid_constant__ CUtensorMap tm_wg64, const __grid_constant__ CUtensorMap tm_wu64,
                       const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_act, const int32_t* __restrict__ offsets,
                       const int32_t* __restrict__ active, const int32_t* __restrict__ row_token,
                       const float* __restrict__ row_gate, __nv_bfloat16* __restrict__ act_g, int* counters,
                       int n_ctr, float* __restrict__ out, float* __restrict__ y_zero, long long y_elems, int H, int I,
                       int N, int fuse_combine, moe_dev_status* st) {
-    using C = StCfg<NT>;
+    using C = StCfg<NT, STK>;
     constexpr int CW = C::CW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
     int* table = misc + C::MISC_INTS;
     int* etok_all = table + C::TABLE_INTS;           // [EPI_WARPS][32] tokens of each epilogue warp
     float* egt_all = reinterpret_cast<float*>(etok_all + C::EPI_WARPS * 32);   // [EPI_WARPS][32] their gates
+    float* xch = egt_all + C::EPI_WARPS * 32;        // [NT][64] up values of a stacked unit
     UnitTable tb{table, table + MOE_MAX_EXPERTS, table + 2 * MOE_MAX_EXPERTS, table + 3 * MOE_MAX_EXPERTS, 0};
     int* s_act = table + 4 * MOE_MAX_EXPERTS + 4;   // [N + 1] staged copy of active[]
     int* s_off = s_act + MOE_MAX_EXPERTS + 1;        // [N + 1] staged copy of offsets[]
@@ -228,7 +231,8 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_act);
     }
-    const int S = I / C::BI, MT = H / C::BH;
+    int S = I / C::BI;   // phase-1 units per item (I / 64 for stacked units, set below)
+    const int MT = H / C::BH;
     const int KT2 = I / (2 * C::BK);
     int* const work_head = counters;           // next unit to hand out
     int* const item_done = counters + 1;       // phase-1 units finished, per item
@@ -300,6 +304,12 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
     // streaming.  (At larger batches the extra reductions into y cost more
     // than the shorter units save.)
     const int KP2 = (KT2 % 2 == 0 && s_items[1] * MT < 2 * static_cast<int>(gridDim.x)) ? 2 : 1;
+    // Stacked units (STK, chosen on the host for batches whose phase 1 cannot
+    // give every SM a whole 128-row I-slice): a phase-1 unit covers 64 I rows,
+    // their 64 gate and 64 up rows stacked as one 128-row operand, so twice
+    // the units stream.
+    constexpr bool stk = STK;
+    if (stk) S = I / 64;
     const int KT2P = KT2 / KP2;
     // units: phase 1 = [0, n1) as item * S + slice, phase 2 = [n1, n1 + n2) as
     // n1 + (item * MT + h-tile) * KP2 + K part
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                 }
                 const int n_g4 = (nrows + 3) / 4;
                 const int n16 = (min(NT, max(16, (nrows + 15) & ~15))) / 16;
-                const int nk = p1 ? KT1 : KT2P;
+                const int nk = p1 ? (stk ? KT1 / 2 : KT1) : KT2P;
                 for (int kt = 0; kt < nk && ok; ++kt) {
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
@@ -393,7 +403,19 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                     }
                     const uint32_t dst = ring_a + stage * C::STAGE;
                     const uint32_t fb = bar(B_FULL + stage);
-                    if (p1) {
+                    if (p1 && stk) {
+                        // two 64-column K chunks; each is [64 gate rows; the same 64 up rows]
+                        const int wrow = e * I + sub * 64;
+                        mbar_arrive_expect_tx(fb, C::W_BYTES + 2 * n_g4 * 512);
+                        for (int c = 0; c < 2; ++c) {
+                            const int kc = kt * 2 * C::BK + c * C::BK;
+                            tma_load_2d(dst + c * C::W_BOX, &tm_wg64, kc, wrow, fb, pol_w);
+                            tma_load_2d(dst + c * C::W_BOX + C::W_BOX / 2, &tm_wu64, kc, wrow, fb, pol_w);
+                            for (int g = 0; g < n_g4; ++g)
+                                tma_gather4(dst + C::W_BYTES + c * C::X_ATOM + g * 512, &tm_x, kc, ptok[4 * g],
+                                            ptok[4 * g + 1], ptok[4 * g + 2], ptok[4 * g + 3], fb, pol_x);
+                        }
+                    } else if (p1) {
                         const int wrow = e * I + sub * C::BI;
                         mbar_arrive_expect_tx(fb, C::W_BYTES + n_g4 * 512);
                         tma_load_2d(dst, &tm_wg, kt * C::BK, wrow, fb, pol_w);
@@ -453,7 +475,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                 const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
                 if (!mbar_wait(bar(B_ACCE + b), ((j >> 1) & 1) ^ 1, abort_flag, st, kSiteMmaTmemFree)) break;
                 tc_fence_after();
-                const int nk = p1 ? KT1 : KT2P;
+                const int nk = p1 ? (stk ? KT1 / 2 : KT1) : KT2P;
                 for (int kt = 0; kt < nk; ++kt) {
                     if (!mbar_wait(bar(B_FULL + stage), phase, abort_flag, st, kSiteMmaFull)) {
                         ok = false;
@@ -461,7 +483,7 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t a = ring_a + stage * C::STAGE;
-                    if (p1) {
+                    if (p1 && !stk) {
 #pragma unroll
                         for (int kk = 0; kk < C::BK / 16; ++kk) {
                             const uint64_t dx = sw128_desc(a + C::W_BYTES + kk * 32);
@@ -529,7 +551,50 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
             const int b = j & 1;
             const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
             okw = __all_sync(kFull, mbar_wait(bar(B_ACCF + b), (j >> 1) & 1, abort_flag, st, kSiteEpiG1Done));
-            if (okw) {
+            if (p1 && stk) {
+                // accumulator lanes 0-63: gate rows, 64-127: the same up rows.  The
+                // up warps stage their values in shared memory; after a barrier of
+                // all epilogue warps (taken by every warp) the gate warps form the
+                // SwiGLU for the 64 I rows of the unit.
+                if (okw && q >= 2) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c8 = 0; c8 < CW / 8; ++c8) {
+                        if (c_lo + c8 * 8 >= nrows) break;   // warp-uniform
+                        uint32_t u[8];
+                        tmem_ld8(acc0 + lane_off + c_lo + c8 * 8, u);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj)
+                            xch[(c_lo + c8 * 8 + jj) * 64 + (q - 2) * 32 + lane] = __uint_as_float(u[jj]);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(bar(B_ACCE + b));
+                }
+                okw = named_sync_and(C::EPI_THREADS, okw);
+                if (okw && q < 2) {
+                    tc_fence_after();
+                    __nv_bfloat16* dst = act_g + static_cast<size_t>(row0) * I + sub * 64 + row;
+#pragma unroll
+                    for (int c8 = 0; c8 < CW / 8; ++c8) {
+                        if (c_lo + c8 * 8 >= nrows) break;   // warp-uniform
+                        uint32_t g[8];
+                        tmem_ld8(acc0 + lane_off + c_lo + c8 * 8, g);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int t = c_lo + c8 * 8 + jj;
+                            if (t < nrows)
+                                dst[static_cast<size_t>(t) * I] =
+                                    __float2bfloat16_rn(silu_mul(__uint_as_float(g[jj]), xch[t * 64 + row]));
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(bar(B_ACCE + b));
+                    fence_proxy_async_global();
+                    __threadfence();
+                }
+            } else if (okw) {
                 tc_fence_after();
                 if (p1) {
                     // SwiGLU of this thread's I row for the warp's token columns -> A (bf16, row-major)
@@ -1103,12 +1168,12 @@ static cudaError_t launch_zero(float* p, long long n, cudaStream_t s, int* c = n
     return launch_pdl(zero_kernel, dim3(grid), dim3(256), 0, s, p, n, c, nc);
 }
 
-template <int NT>
+template <int NT, bool STK>
 static cudaError_t run_stream(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
                               int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                               const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
                               cudaStream_t s) {
-    using C = StCfg<NT>;
+    using C = StCfg<NT, STK>;
     const bool fuse = (flags & MOE_FFN_FUSE_COMBINE) != 0;
     const long long M = static_cast<long long>(T) * k;
     const long long items = ffn_max_items(T, N, k, NT);
@@ -1118,9 +1183,11 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
     int* counters = static_cast<int*>(ws);
     __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + kStreamCtrBytes);
     float* y_zero = (fuse && (flags & MOE_FFN_ZERO_Y)) ? out : nullptr;
-    CUtensorMap tm_wg, tm_wu, tm_wd, tm_x, tm_act;
+    CUtensorMap tm_wg, tm_wu, tm_wg64, tm_wu64, tm_wd, tm_x, tm_act;
     if (!make_tmap(&tm_wg, wg, H, static_cast<uint64_t>(N) * I, 64, 128) ||
         !make_tmap(&tm_wu, wu, H, static_cast<uint64_t>(N) * I, 64, 128) ||
+        !make_tmap(&tm_wg64, wg, H, static_cast<uint64_t>(N) * I, 64, 64) ||
+        !make_tmap(&tm_wu64, wu, H, static_cast<uint64_t>(N) * I, 64, 64) ||
         !make_tmap(&tm_wd, wd, I, static_cast<uint64_t>(N) * H, 64, 128) ||
         !make_tmap(&tm_x, x, H, static_cast<uint64_t>(T), 64, 1) ||
         !make_tmap(&tm_act, act, I, static_cast<uint64_t>(M), 64, 16))
@@ -1132,14 +1199,15 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
     if (devi < 0 || devi >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[devi]) {
         cudaError_t ae =
-            cudaFuncSetAttribute(ffn_stream_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+            cudaFuncSetAttribute(ffn_stream_kernel<NT, STK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (ae != cudaSuccess) return ae;
         attr_set[devi] = true;
     }
     const long long max_units = items * (I / C::BI + H / C::BH);
     int grid = sm_count();
     if (max_units < grid) grid = static_cast<int>(max_units > 0 ? max_units : 1);
-    return launch_pdl(ffn_stream_kernel<NT>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wd, tm_x,
+    return launch_pdl(ffn_stream_kernel<NT, STK>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wg64, tm_wu64,
+                      tm_wd, tm_x,
                       tm_act, offsets, active, row_token, row_gate, act, counters, static_cast<int>(items + 1), out,
                       y_zero, static_cast<long long>(T) * H, H, I, N, fuse ? 1 : 0, st);
 }
@@ -1206,14 +1274,19 @@ cudaError_t launch_ffn_bf16(const void* x, const void* wg, const void* wu, const
         return run_tokmajor(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws, st, s);
     switch (ffn_nt(T)) {
         case 16:
-            return run_stream<16>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws,
-                                  st, s);
+            // stacked phase-1 units when even min(N, T*k) active experts give
+            // fewer whole 128-row I-slices than SMs
+            if (static_cast<long long>(N < T * k ? N : T * k) * (I / 128) < sm_count())
+                return run_stream<16, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags,
+                                            out, ws, st, s);
+            return run_stream<16, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags,
+                                         out, ws, st, s);
         case 32:
-            return run_stream<32>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws,
-                                  st, s);
+            return run_stream<32, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags,
+                                         out, ws, st, s);
         default:
-            return run_stream<64>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws,
-                                  st, s);
+            return run_stream<64, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags,
+                                         out, ws, st, s);
     }
 }
 
