@@ -72,7 +72,7 @@ typedef struct moe_dev_status {
 #define MOE_DTYPE_F32 0
 #define MOE_DTYPE_BF16 1
 
-/* Limits of this build. */
+/* Compile-time limits of the library. */
 #define MOE_MAX_EXPERTS 256        /* N */
 #define MOE_MAX_RANKS 16           /* R (and k <= R) */
 

@@ -161,6 +161,27 @@ def test_token_major_odd_tiles(g):
     _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
 
 
+@pytest.mark.parametrize("fuse", [True, False])
+def test_token_major_many_ranks(g, fuse):
+    """k = 12 > 8 in the token-major kernel: the combine's instance for up to
+    16 rows per token (fused), or the rows added into the caller's buffer."""
+    L = syn.qwen_layer(1024, H=256, N=32, k=12, I=128)
+    D = g.DevLayer(L)
+    ids, gates = _route(L, L.x_bf16, 1024)
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=fuse)
+
+
+def test_weight_major_max_experts(g):
+    """N = 256 experts (the library's maximum) with k = 16 at a batch of 40:
+    up to 256 active experts in the weight-major kernel's item table, 64-row
+    token chunks."""
+    L = syn.qwen_layer(40, H=256, N=256, k=16, I=128)
+    D = g.DevLayer(L)
+    ids, gates = _route(L, L.x_bf16, 40)
+    assert len(np.unique(ids[ids >= 0])) > 128
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
+
+
 def test_token_major_prefill_shape_sampled(g, qwen):
     """The prefill shape (T = 8192, H = 2048, I = 768, 128 experts, top-8) on
     plain top-8 routing; sampled tokens against the oracle."""
