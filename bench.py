@@ -783,7 +783,7 @@ def run_stack(args):
         for lay in stack:
             lay.route_and_dispatch(xb, sere)
             lay.ffn(xb, accumulate_into=xres)
-            xb.copy_(xres)
+            moe.moe_residual_to_bf16(xres, xb)
 
     res = {}
     for mode, stack, sere in (("top8", layers, False), ("sere_k2", layers, True), ("sere_k1", layers_k1, True),
@@ -830,7 +830,7 @@ def run_stack(args):
                                       "rho=0.5 with per-layer similarity and 16 protected experts, plain top-8, "
                                       "plain top-2" % (nl, B, nl * N * EXPERT_BYTES / 1e9),
                           "metric": "decode step tokens/s (one CUDA graph per step)", "peak_gbs": peak,
-                          "peak_source": peak_src, "residual": "x_{l+1} = x_l + y_l in fp32, cast to bf16 per layer",
+                          "peak_source": peak_src, "residual": "x_{l+1} = x_l + y_l in fp32 (the FFN accumulates into it), rounded to bf16 per layer by moe_residual_to_bf16",
                           **res}), flush=True)
     return 0
 

@@ -43,7 +43,7 @@ class _SereParams(ctypes.Structure):
 
 
 EXPORTS = ["moe_route", "moe_route_dispatch", "moe_reroute_sere", "moe_dispatch_capacity", "moe_ffn_grouped", "moe_combine",
-           "moe_token_weights", "moe_similarity_calibrate", "moe_workspace_size", "moe_status_string"]
+           "moe_residual_to_bf16", "moe_token_weights", "moe_similarity_calibrate", "moe_workspace_size", "moe_status_string"]
 
 
 def load(path: str = LIB_PATH):
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH):
             L.moe_ffn_grouped.restype = i
             L.moe_combine.argtypes = [p, p, p, i, i, i, p, p]
             L.moe_combine.restype = i
+            L.moe_residual_to_bf16.argtypes = [p, p, ctypes.c_longlong, p]
+            L.moe_residual_to_bf16.restype = i
             L.moe_token_weights.argtypes = [p, i, i, i, p, f, f, p, p, p, p, sz, p, p]
             L.moe_token_weights.restype = i
             L.moe_similarity_calibrate.argtypes = [p, i, p, p, p, i, i, i, p, p, sz, p, p]
@@ -223,6 +225,15 @@ def moe_combine(rows_out, slot_row, slot_gate, y, stream=None):
     H = y.shape[1]
     rc = load().moe_combine(_ptr(rows_out), _ptr(slot_row), _ptr(slot_gate), T, H, k, _ptr(y), _stream(stream))
     _check(rc, "moe_combine")
+
+
+def moe_residual_to_bf16(x, y, stream=None):
+    """y = bf16(x), round to nearest even: x fp32 and y bf16 CUDA tensors of
+    the same number of elements (a multiple of 8)."""
+    if x.numel() != y.numel():
+        raise MoeError("moe_residual_to_bf16: %d elements in, %d out" % (x.numel(), y.numel()))
+    rc = load().moe_residual_to_bf16(_ptr(x), _ptr(y), x.numel(), _stream(stream))
+    _check(rc, "moe_residual_to_bf16")
 
 
 def moe_token_weights(x, is_visual, entropy, token_w, r_v=None, delta: float = 1.0, eps: float = 1e-6, st=None,

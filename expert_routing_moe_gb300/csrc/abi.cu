@@ -214,6 +214,13 @@ moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const f
     return from_cuda(moe::launch_combine(rows_out, slot_row, slot_gate, T, H, k, y, as_stream(stream)));
 }
 
+moe_status_t moe_residual_to_bf16(const float* x, void* y, long long n, void* stream) {
+    if (n < 0 || n % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (x == nullptr || y == nullptr || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_residual_to_bf16(x, y, n, as_stream(stream)));
+}
+
 const char* moe_status_string(int code, int device) {
     if (device) {
         switch (code) {

@@ -80,6 +80,8 @@ size_t token_weights_workspace(int T);
 cudaError_t launch_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
                                  float eps, float* entropy, float* token_w, float* r_v, void* ws, moe_dev_status* st,
                                  cudaStream_t s);
+cudaError_t launch_residual_to_bf16(const float* x, void* y, long long n, cudaStream_t s);
+
 cudaError_t launch_combine(const float* rows_out, const int32_t* slot_row, const float* slot_gate, int T, int H,
                            int k, float* y, cudaStream_t s);
 

@@ -361,6 +361,19 @@ moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const u
 moe_status_t moe_combine(const float* rows_out, const int32_t* slot_row, const float* slot_gate, int T,
                          int H, int k, float* y, void* stream);
 
+/*
+ * Residual rounding between stacked layers: y[i] = bf16(x[i]), round to
+ * nearest, ties to even, for i < n.  In a stack of layers the FFN adds
+ * sum_j G_j E_j(x) ("MACS" Eq. (1)) into the fp32 residual (moe_ffn_grouped
+ * with MOE_FFN_FUSE_COMBINE and without MOE_FFN_ZERO_Y), and the next
+ * layer's routing and FFN read bf16 tokens; this is that rounding, as a
+ * launch that overlaps its neighbours (programmatic dependent launch).
+ *   x [n] fp32 in, y [n] bf16 out (device, 16-byte aligned, caller-owned);
+ *   n a multiple of 8.  Bad sizes or alignment return MOE_ERR_INVALID_ARG
+ *   with no launch; n = 0 is a no-op.
+ */
+moe_status_t moe_residual_to_bf16(const float* x, void* y, long long n, void* stream);
+
 /* ---------------------------------------------------------------- */
 /* Workspace sizes and status strings                                 */
 /* ---------------------------------------------------------------- */

@@ -152,6 +152,17 @@ def test_combine_rejects(lib):
     assert lib.moe_combine(FAKE, None, FAKE, 4, 64, 2, FAKE, None) == -1
 
 
+def test_residual_to_bf16_rejects(lib):
+    f = lib.moe_residual_to_bf16
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert f(FAKE, FAKE, 12, None) == -1      # n % 8
+    assert f(FAKE, FAKE, -8, None) == -1      # negative n
+    assert f(odd, FAKE, 16, None) == -1       # misaligned x
+    assert f(FAKE, odd, 16, None) == -1       # misaligned y
+    assert f(None, FAKE, 16, None) == -1      # no input
+    assert f(None, None, 0, None) == 0        # n = 0: nothing to do
+
+
 def test_token_weights_rejects(lib):
     f = lib.moe_token_weights
     odd = ctypes.c_void_p((1 << 20) + 8)

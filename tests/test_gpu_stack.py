@@ -61,4 +61,4 @@ def test_stack_layers_chained(sere):
         assert int(lay.active[0].item()) == ref["perm"]["active"][0] or not ok.all()
         sel = (ok & same)[toks]
         g.assert_y_close(y[toks][sel], ref["y"][sel], "stack layer %d" % l)
-        xb.copy_(xres)
+        moe.moe_residual_to_bf16(xres, xb)
