@@ -85,3 +85,42 @@ def test_prefill_capacity_layer_sampled(g):
     assert (load <= ref["cap"]).all()
     st = g.host(layer.slot_status[:L.T])
     assert (st == 1).sum() > 0
+
+
+def test_decode_steps_replayed_from_one_graph(g):
+    """The bench's launch configuration: several SERE decode steps (routing
+    and dispatch in one launch, then the FFN, chained by programmatic
+    dependent launch) captured in one CUDA graph, each on its own batch and
+    into its own output, then replayed three times.  Every step's output
+    matches the oracle layer, so the kernels' counters and workspaces are
+    left ready for the next step inside the graph."""
+    import dataclasses
+    L = syn.decode(32)
+    D = g.DevLayer(L)
+    layer = _layer(g, L, D)
+    nb = 4
+    Ls = [L] + [dataclasses.replace(L, x=Lb.x, x_bf16=Lb.x_bf16) for Lb in
+                (syn.decode(32, with_weights=False, token_stream_offset=b) for b in range(1, nb))]
+    xs = [g.dev(Lb.x_bf16, torch.bfloat16) for Lb in Ls]
+    ys = [torch.empty(L.T, L.H, dtype=torch.float32, device=g.DEV) for _ in range(nb)]
+    stream = torch.cuda.Stream(device=g.DEV)
+    with torch.cuda.stream(stream):
+        for b in range(nb):
+            layer.forward(xs[b], sere=True, out=ys[b])
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for rep in range(2):
+                for b in range(nb):
+                    layer.forward(xs[b], sere=True, out=ys[b])
+        for y in ys:
+            y.fill_(float("nan"))
+        for _ in range(3):
+            graph.replay()
+        stream.synchronize()
+    code, detail = layer.device_status()
+    assert code == 0, (code, detail)
+    for b, Lb in enumerate(Ls):
+        ref = oracle.layer(Lb, sere_on=True)
+        ok = _gap(ref["logits"], L.k) >= 1e-5
+        g.assert_y_close(g.host(ys[b])[ok], ref["y"][ok], "graph step %d" % b)

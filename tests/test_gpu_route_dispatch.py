@@ -151,8 +151,9 @@ def test_ragged_expert_count(g, ws):
 
 
 def test_repeated_calls_leave_workspace_reusable(g, ws):
-    """Every call resets the completion counter: repeated calls (and a graph
-    replay) give identical results."""
+    """Every call resets the completion counter: repeated calls give
+    identical results (graph replays of whole steps are covered by the
+    layer tests)."""
     L = syn.decode(32, with_weights=False)
     D = g.DevLayer(L, weights=False)
     first = _fused(g, D.x, D.w_r, L.k, ws, sim=D.sim)
