@@ -150,8 +150,14 @@ struct StCfg {
     static constexpr int MISC_INTS = 8 + 64 + 8;    // tmem slot, abort flag, table size, unit ring, token list, exit flag
     static constexpr int TABLE_INTS = 6 * MOE_MAX_EXPERTS + 8;   // item table + staged active[] and offsets[]
     static constexpr int XCH_BYTES = STK ? 64 * NT * 4 : 0;   // up values of a stacked phase-1 unit
-    static constexpr int SMEM =
-        1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + TABLE_INTS * 4 + EPI_WARPS * 32 * 8 + XCH_BYTES;
+    // dispatch rows whose token and gate are staged in shared memory at the
+    // start, in one pass of the CTA's threads (batches with more rows read
+    // them from global memory: a second pass would put a round trip back).
+    // Batches of more than 32 tokens do not stage: measured, it cost them
+    // 0.5 us even when no row was staged.
+    static constexpr int RT_CAP = NT <= 16 ? 128 : (NT <= 32 ? THREADS : 0);
+    static constexpr int SMEM = 1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + TABLE_INTS * 4 +
+                                EPI_WARPS * 32 * 8 + XCH_BYTES + RT_CAP * 8;
     static constexpr uint32_t TMEM_COLS = 4 * NT;   // two accumulator slots of 2 x NT columns
     static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
     static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256, "TMEM allocation");
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
                       const int32_t* __restrict__ active, const int32_t* __restrict__ row_token,
                       const float* __restrict__ row_gate, __nv_bfloat16* __restrict__ act_g, int* counters,
                       int n_ctr, float* __restrict__ out, float* __restrict__ y_zero, long long y_elems, int H, int I,
-                      int N, int fuse_combine, moe_dev_status* st) {
+                      int N, int fuse_combine, moe_dev_status* st, int m_rows) {
     using C = StCfg<NT, STK>;
     constexpr int CW = C::CW;
     extern __shared__ uint8_t smem_raw[];
@@ -197,6 +203,9 @@ __global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
     int* etok_all = table + C::TABLE_INTS;           // [EPI_WARPS][32] tokens of each epilogue warp
     float* egt_all = reinterpret_cast<float*>(etok_all + C::EPI_WARPS * 32);   // [EPI_WARPS][32] their gates
     float* xch = egt_all + C::EPI_WARPS * 32;        // [NT][64] up values of a stacked unit
+    int* s_rt = reinterpret_cast<int*>(xch + C::XCH_BYTES / 4);   // [RT_CAP] row -> token
+    float* s_rg = reinterpret_cast<float*>(s_rt + C::RT_CAP);     // [RT_CAP] row -> gate
+    const bool rt_staged = C::RT_CAP > 0 && m_rows <= C::RT_CAP;
     UnitTable tb{table, table + MOE_MAX_EXPERTS, table + 2 * MOE_MAX_EXPERTS, table + 3 * MOE_MAX_EXPERTS, 0};
     int* s_act = table + 4 * MOE_MAX_EXPERTS + 4;   // [N + 1] staged copy of active[]
     int* s_off = s_act + MOE_MAX_EXPERTS + 1;        // [N + 1] staged copy of offsets[]
@@ -246,11 +255,29 @@ __global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
     // the producer's first unit id is fetched while the table is built
     int first_unit = 0;
     if (warp == 0 && lane == 0) first_unit = atomicAdd(work_head, 1);
-    // active[] and offsets[] in one round trip (independent loads), then the
-    // item table: prefix over active experts of their chunk counts
-    for (int i = threadIdx.x; i <= N; i += blockDim.x) {
-        s_act[i] = active[i];
-        s_off[i] = offsets[i];
+    // active[] and offsets[] in one round trip, with every row's token and
+    // gate when they fit (independent loads, issued before the stores); then
+    // the item table: prefix over active experts of their chunk counts
+    const int n_stage = rt_staged ? max(N + 1, m_rows) : N + 1;
+    for (int i = threadIdx.x; i < n_stage; i += blockDim.x) {
+        int av = 0, ov = 0, rv = 0;
+        float gv = 0.f;
+        if (i <= N) {
+            av = active[i];
+            ov = offsets[i];
+        }
+        if (rt_staged && i < m_rows) {
+            rv = row_token[i];
+            gv = row_gate[i];
+        }
+        if (i <= N) {
+            s_act[i] = av;
+            s_off[i] = ov;
+        }
+        if (rt_staged && i < m_rows) {
+            s_rt[i] = rv;
+            s_rg[i] = gv;
+        }
     }
     __syncthreads();
     // the last CTA to finish returns the counters to zero for the next call
@@ -370,7 +397,10 @@ __global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
             item_info(tb, item, NT, e, row0, nrows);
             if (p1) {
                 // rows past the chunk repeat its first token; their columns are never used
-                for (int t = lane; t < NT; t += 32) ptok[t] = row_token[row0 + (t < nrows ? t : 0)];
+                for (int t = lane; t < NT; t += 32) {
+                    const int r = row0 + (t < nrows ? t : 0);
+                    ptok[t] = rt_staged ? s_rt[r] : row_token[r];
+                }
                 __syncwarp();
             }
             if (lane == 0) {
@@ -622,8 +652,8 @@ __global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
                 } else {
                     if (lane < CW) {
                         const int t = c_lo + lane;
-                        etok[lane] = (t < nrows) ? row_token[row0 + t] : 0;
-                        egt[lane] = (t < nrows) ? row_gate[row0 + t] : 0.f;
+                        etok[lane] = (t < nrows) ? (rt_staged ? s_rt[row0 + t] : row_token[row0 + t]) : 0;
+                        egt[lane] = (t < nrows) ? (rt_staged ? s_rg[row0 + t] : row_gate[row0 + t]) : 0.f;
                     }
                     __syncwarp();
                     // read the accumulator in chunks of up to 16 columns; it is released right
@@ -1209,7 +1239,7 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
     return launch_pdl(ffn_stream_kernel<NT, STK>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wg64, tm_wu64,
                       tm_wd, tm_x,
                       tm_act, offsets, active, row_token, row_gate, act, counters, static_cast<int>(items + 1), out,
-                      y_zero, static_cast<long long>(T) * H, H, I, N, fuse ? 1 : 0, st);
+                      y_zero, static_cast<long long>(T) * H, H, I, N, fuse ? 1 : 0, st, static_cast<int>(M));
 }
 
 static cudaError_t run_tokmajor(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
