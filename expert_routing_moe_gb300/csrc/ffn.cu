@@ -233,6 +233,12 @@ __global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // TMEM is taken before the dependency wait (the preceding kernels hold none)
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+        tc_fence_before();
+    }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_wg);
         tma_prefetch_desc(&tm_wu);
@@ -342,6 +348,10 @@ __global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
     // n1 + (item * MT + h-tile) * KP2 + K part
     const int n1 = s_items[1] * S, n_total = n1 + s_items[1] * MT * KP2;
     if (n_total == 0) {
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(*tmem_slot, C::TMEM_COLS);
+        }
         finish();
         return;
     }
@@ -358,13 +368,8 @@ __global__ void __launch_bounds__(StCfg<NT, STK>::THREADS, 1)
             part = r - sub * KP2;
         }
     };
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
-    }
-    __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = *tmem_slot;   // published by the barriers since the allocation
     const int KT1 = H / C::BK;
 
     if (warp == 0) {
