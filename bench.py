@@ -43,7 +43,7 @@ EXPERT_BYTES = 3 * H * I * 2
 # kernel (--set full, SERE batch 4 of this workload: 34 active experts, whose
 # algorithmic bytes are 34 * EXPERT_BYTES + T * H * 6).  Set it to None whenever
 # the FFN kernel changes, until it has been captured again.
-FFN_TRAFFIC_CAPTURE = None
+FFN_TRAFFIC_CAPTURE = {"dram_bytes": 324.22e6, "algorithmic_bytes": 321.26e6, "active_experts": 34}
 
 
 def workload_config(extra=None):
