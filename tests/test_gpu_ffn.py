@@ -171,6 +171,23 @@ def test_token_major_many_ranks(g, fuse):
     _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=fuse)
 
 
+@pytest.mark.parametrize("T,N,k,H,I", [
+    (12, 64, 12, 256, 128),    # 16-row chunks, stacked units, 144 rows: tokens and gates from global memory
+    (16, 128, 8, 256, 768),    # 16-row chunks, whole slices, 128 rows staged in shared memory
+    (24, 64, 12, 256, 256),    # 32-row chunks, 288 rows staged
+    (30, 64, 16, 256, 256),    # 32-row chunks, 480 rows: past one staging pass, global loads
+])
+def test_weight_major_unit_and_staging_paths(g, T, N, k, H, I):
+    """Each combination of the weight-major kernel's host-chosen variants:
+    stacked or whole phase-1 units, row tokens and gates staged in shared
+    memory or read from global memory."""
+    L = syn.qwen_layer(T, H=H, N=N, k=k, I=I)
+    D = g.DevLayer(L)
+    ids, gates = _route(L, L.x_bf16, T)
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=False)
+
+
 def test_weight_major_max_experts(g):
     """N = 256 experts (the library's maximum) with k = 16 at a batch of 40:
     up to 256 active experts in the weight-major kernel's item table, 64-row
