@@ -267,7 +267,7 @@ cudaError_t launch_similarity(const void* x, int n, const void* wg, const void* 
     const long long K = static_cast<long long>(n) * H;
     if (!make_tmap(&tm_e, ebf, static_cast<uint64_t>(K), static_cast<uint64_t>(N), 64, 128))
         return cudaErrorInvalidValue;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};   // per device; idempotent, race-free
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;

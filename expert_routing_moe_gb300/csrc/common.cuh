@@ -3,6 +3,7 @@
 // the sm_103a inline-PTX wrappers (mbarrier, TMA, tcgen05).
 #pragma once
 
+#include <atomic>
 #include <cuda_runtime.h>
 #include <stdint.h>
 

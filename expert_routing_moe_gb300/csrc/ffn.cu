@@ -1228,7 +1228,7 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
         !make_tmap(&tm_act, act, I, static_cast<uint64_t>(M), 64, 16))
         return cudaErrorInvalidValue;
     // the attribute is set once per device, on the first (uncaptured) call
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};   // per device; idempotent, race-free
     int devi = 0;
     cudaGetDevice(&devi);
     if (devi < 0 || devi >= 64) return cudaErrorInvalidDevice;
@@ -1274,7 +1274,7 @@ static cudaError_t run_tokmajor(const void* x, const void* wg, const void* wu, c
         !make_tmap(&tm_xp, xp, H, static_cast<uint64_t>(M), 64, 128) ||
         !make_tmap(&tm_act, act, I, static_cast<uint64_t>(M), 64, 128))
         return cudaErrorInvalidValue;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};   // per device; idempotent, race-free
     int devi = 0;
     cudaGetDevice(&devi);
     if (devi < 0 || devi >= 64) return cudaErrorInvalidDevice;

@@ -422,7 +422,7 @@ static cudaError_t rd_launch(const XT* x, const float* w, const RdArgs& a, bool 
                              cudaStream_t s) {
     const dim3 grid((a.N + kRdEpc - 1) / kRdEpc, (a.T + 3) / 4);
     const size_t smem = a.stage_sim ? static_cast<size_t>(a.N) * a.N * 4 : 0;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};   // per device; idempotent, race-free
     int dev = 0;
     cudaGetDevice(&dev);
     if (sere && dev >= 0 && dev < 64 && !attr_set[dev]) {

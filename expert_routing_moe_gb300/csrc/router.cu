@@ -296,7 +296,7 @@ static cudaError_t launch_router_tc(const void* x, const float* w_router, int T,
     if (!make_tmap(&tm_x, x, H, static_cast<uint64_t>(T), C::BK, C::BM) ||
         !make_tmap_f32(&tm_w, w_router, H, static_cast<uint64_t>(N), C::BK, C::BN))
         return cudaErrorInvalidValue;
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};   // per device; idempotent, race-free
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -527,7 +527,7 @@ template <int PL>
 static cudaError_t sere_launch_pl(const float* logits, int do_rank, int T, int N, int k, bool renorm, int32_t* ids,
                                   float* gates, int ld, const moe_sere_params& p, moe_dev_status* st, cudaStream_t s,
                                   bool stage, size_t smem, int csize) {
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64] = {};   // per device; idempotent, race-free
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {

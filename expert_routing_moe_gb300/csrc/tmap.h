@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <atomic>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,7 +41,7 @@ inline bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t
 }
 
 inline int sm_count() {
-    static int cached[64] = {};
+    static std::atomic<int> cached[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 1;
