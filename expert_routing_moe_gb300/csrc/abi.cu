@@ -62,11 +62,17 @@ moe_status_t moe_route_dispatch(const void* x, int x_dtype, const float* w_route
     if (counts == nullptr || offsets == nullptr || active == nullptr) return MOE_ERR_INVALID_ARG;
     if (T > moe::kRouteDispatchMaxT || T * k > moe::kRouteDispatchMaxSlots) return MOE_ERR_UNSUPPORTED;
     if (T == 0) {
+        // no rows; with SERE the union bitmap and the statistics describe the
+        // empty batch too (all zero), not the previous call's
         cudaStream_t s = as_stream(stream);
-        cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
-        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
-        cudaMemsetAsync(active, 0, sizeof(int32_t) * (N + 1), s);
-        return from_cuda(cudaGetLastError());
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(active, 0, sizeof(int32_t) * (N + 1), s);
+        if (e == cudaSuccess && sere != nullptr && sere->union_bitmap != nullptr)
+            e = cudaMemsetAsync(sere->union_bitmap, 0, sizeof(uint32_t) * ((N + 31) / 32), s);
+        if (e == cudaSuccess && sere != nullptr && sere->stats != nullptr)
+            e = cudaMemsetAsync(sere->stats, 0, sizeof(int32_t) * 8, s);
+        return from_cuda(e);
     }
     if (x == nullptr || w_router == nullptr || H < 1 || logits == nullptr || ids == nullptr || gates == nullptr ||
         row_token == nullptr || row_gate == nullptr)
@@ -152,6 +158,7 @@ moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const
         return MOE_ERR_INVALID_ARG;
     cudaStream_t s = as_stream(stream);
     if (dtype == MOE_DTYPE_F32) {
+        if (static_cast<long long>(H + I) * 4 > moe::kFfnF32MaxSmem) return MOE_ERR_UNSUPPORTED;
         return from_cuda(moe::launch_ffn_f32(static_cast<const float*>(x), static_cast<const float*>(w_gate),
                                              static_cast<const float*>(w_up), static_cast<const float*>(w_down), T,
                                              H, I, N, k, offsets, row_token, row_gate, active, flags, out, st, s));

@@ -16,6 +16,8 @@
 // in shared memory and admitted while the running load stays within C.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 #include "permute.cuh"
@@ -373,6 +375,10 @@ __global__ void __launch_bounds__(128) cap_bucket_kernel(const int32_t* __restri
 // equals that of sorting all candidates.
 constexpr int kCapBins = 1024;
 constexpr int kCapPer = kCapacityMaxT / 1024;   // candidates per thread at most
+// dynamic shared memory of cap_admit_kernel at the largest batch: the sort
+// keys padded to a power of two, then one fp32 weight per token
+constexpr int kCapAdmitMaxSmem = kCapacityMaxT * 8 + kCapacityMaxT * 4;
+static_assert(kCapAdmitMaxSmem <= 227 * 1024, "cap_admit shared memory");
 
 __device__ __forceinline__ float cap_weight(const float* token_w, int t) {
     float wt = token_w ? token_w[t] : 1.0f;
@@ -632,13 +638,15 @@ cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int 
     carve(&w, ws, T, N, k, capped);
     w.bias = modality_bias;
     w.r_v = r_v;
+    // an empty batch has no rows: counts, offsets and the active list are zero
+    auto clear_empty = [&]() -> cudaError_t {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(active, 0, sizeof(int32_t) * (N + 1), s);
+        return e;
+    };
     if (!capped) {
-        if (T == 0) {
-            cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
-            cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
-            cudaMemsetAsync(active, 0, sizeof(int32_t) * (N + 1), s);
-            return cudaGetLastError();
-        }
+        if (T == 0) return clear_empty();
         return launch_permute(ids, gates, ld, T, N, k, counts, offsets, row_token, row_gate, active, out_ids,
                               out_gates, slot_row, w.blk_start, st, s);
     }
@@ -652,14 +660,27 @@ cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int 
         size_t P2 = 1;
         while (P2 < static_cast<size_t>(T)) P2 <<= 1;
         const size_t smem = P2 * sizeof(unsigned long long) + static_cast<size_t>(T) * sizeof(float);
-        err = cudaFuncSetAttribute(cap_admit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(smem));
+        // The kernel's dynamic shared-memory limit is raised once per device
+        // to what the largest batch needs and never lowered, so calls of
+        // different sizes from several host threads (or a small call before
+        // a large captured one) cannot undo each other's setting.
+        static std::atomic<bool> attr_set[64] = {};
+        int dev = 0;
+        err = cudaGetDevice(&dev);
         if (err != cudaSuccess) return err;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!attr_set[dev]) {
+            err = cudaFuncSetAttribute(cap_admit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kCapAdmitMaxSmem);
+            if (err != cudaSuccess) return err;
+            attr_set[dev] = true;
+        }
         err = launch_pdl(cap_admit_kernel, dim3(N), dim3(1024), smem, s, gates, ld, T, N, k, capacity_factor,
                          token_w, -1, w, st);
         if (err != cudaSuccess) return err;
         for (int i = 0; i + k < R; ++i) {
-            cudaMemsetAsync(w.cnt2, 0, sizeof(int32_t) * N, s);
+            err = cudaMemsetAsync(w.cnt2, 0, sizeof(int32_t) * N, s);
+            if (err != cudaSuccess) return err;
             err = launch_pdl(cap_offer_kernel, dim3((T + tb - 1) / tb), dim3(tb), 0, s, ids, ld, T, N, k, i, w);
             if (err != cudaSuccess) return err;
             err = launch_pdl(cap_admit_kernel, dim3(N), dim3(1024), smem, s, gates, ld, T, N, k, capacity_factor,
@@ -671,14 +692,15 @@ cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int 
     err = launch_pdl(cap_finalize_kernel, dim3((nfin + tb - 1) / tb), dim3(tb), 0, s, T, N, k, w, slot_status,
                      load_q, cap_q, capacity_factor);
     if (err != cudaSuccess) return err;
-    if (out_ids) cudaMemcpyAsync(out_ids, w.wids, sizeof(int32_t) * T * k, cudaMemcpyDeviceToDevice, s);
-    if (out_gates) cudaMemcpyAsync(out_gates, w.wgates, sizeof(float) * T * k, cudaMemcpyDeviceToDevice, s);
-    if (T == 0) {
-        cudaMemsetAsync(counts, 0, sizeof(int32_t) * N, s);
-        cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1), s);
-        cudaMemsetAsync(active, 0, sizeof(int32_t) * (N + 1), s);
-        return cudaGetLastError();
+    if (out_ids && T > 0) {
+        err = cudaMemcpyAsync(out_ids, w.wids, sizeof(int32_t) * T * k, cudaMemcpyDeviceToDevice, s);
+        if (err != cudaSuccess) return err;
     }
+    if (out_gates && T > 0) {
+        err = cudaMemcpyAsync(out_gates, w.wgates, sizeof(float) * T * k, cudaMemcpyDeviceToDevice, s);
+        if (err != cudaSuccess) return err;
+    }
+    if (T == 0) return clear_empty();
     return launch_permute(w.wids, w.wgates, k, T, N, k, counts, offsets, row_token, row_gate, active, nullptr,
                           nullptr, slot_row, w.blk_start, st, s);
 }

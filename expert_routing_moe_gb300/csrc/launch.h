@@ -59,7 +59,9 @@ cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int 
                             moe_dev_status* st, cudaStream_t s);
 constexpr int kCapacityMaxT = 16384;
 
-// ---- FFN (ffn_simt.cu, ffn_tc.cu) ----
+// ---- FFN (ffn.cu) ----
+// the fp32 kernel holds a row's x and activations in shared memory: (H + I) floats
+constexpr int kFfnF32MaxSmem = 227 * 1024;
 size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype);
 size_t ffn_workspace_zero_bytes(int T, int H, int N, int k, int dtype);
 cudaError_t launch_ffn_f32(const float* x, const float* wg, const float* wu, const float* wd, int T, int H, int I,

@@ -290,6 +290,8 @@ moe_status_t moe_dispatch_capacity_static(const int32_t* ids, const float* gates
  * F32 runs a CUDA-core kernel in fp32.
  * Limits BF16: H % 128 == 0, I % 128 == 0, all pointers 16-byte aligned;
  * rows_out mode needs FUSE_COMBINE off and is accumulated, so zero it first.
+ * Limits F32: (H + I) * 4 <= 227 KiB (a row's x and activations are held
+ * in shared memory); larger sizes return MOE_ERR_UNSUPPORTED.
  */
 moe_status_t moe_ffn_grouped(const void* x, int dtype, const void* w_gate, const void* w_up,
                              const void* w_down, int T, int H, int I, int N, int k, const int32_t* offsets,

@@ -43,9 +43,16 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # bf16 FFN: item counters + the bf16 SwiGLU activations of every dispatch row
+    # bf16 FFN, batches of up to 64 tokens (all-token mode): item counters +
+    # the bf16 SwiGLU activations of the whole batch (padded to 32 tokens)
+    # for each of min(N, T k) experts
     bf = abi.workspace_size(abi.MOE_OP_FFN, 32, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16)
-    assert 32 * 8 * 768 * 2 < bf <= 32 * 8 * 768 * 2 + 4096
+    assert 128 * 32 * 768 * 2 < bf <= 128 * 32 * 768 * 2 + 4096
+    bf1 = abi.workspace_size(abi.MOE_OP_FFN, 1, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16)
+    assert 8 * 16 * 768 * 2 < bf1 <= 8 * 16 * 768 * 2 + 4096
+    # larger batches: the activations of every dispatch row
+    bf = abi.workspace_size(abi.MOE_OP_FFN, 128, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16)
+    assert 128 * 8 * 768 * 2 < bf <= 128 * 8 * 768 * 2 + 4096
     assert abi.workspace_size(abi.MOE_OP_FFN, 32, 64, 128, 8, 2, 2, False, abi.MOE_DTYPE_F32) == 0
     capped = abi.workspace_size(abi.MOE_OP_DISPATCH, 8192, 2048, 768, 128, 8, 10, True, abi.MOE_DTYPE_BF16)
     assert capped >= 2 * 128 * 8192 * 4

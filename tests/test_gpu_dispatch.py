@@ -104,3 +104,69 @@ def test_capacity_prefill_full_size(g):
     ids, gates = oracle.route(l, L.R)
     d = _capacity_case(g, ids, gates, L.N, L.k, L.R, L.token_w, L.gamma)
     assert (d["status"] == 1).sum() > 0 and (d["load"] <= d["cap"]).all()
+
+
+def test_capacity_large_and_small_from_two_host_threads(g):
+    """A large and a small capped dispatch issued over and over from two host
+    threads, each on its own stream: neither call's launch configuration may
+    be undone by the other's (the admission kernel's shared-memory limit is
+    raised once per device to the largest size), and each result stays
+    bit-identical to the same call made alone."""
+    import threading
+    import torch
+    from expert_routing_moe_gb300 import _abi as abi
+
+    L = syn.prefill(with_weights=False)
+    l = oracle.router(L.x_bf16, L.w_r, oracle.DT_BF16)
+    ids_big, gates_big = oracle.route(l, L.R)
+    tw_big = L.token_w
+    small_T = 16
+    ids_small, gates_small, tw_small = ids_big[:small_T].copy(), gates_big[:small_T].copy(), tw_big[:small_T].copy()
+
+    def run(ids, gates, tw, stream, reps, results, errors):
+        try:
+            T = ids.shape[0]
+            dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda:0")
+            di, dg, dw = dev(ids), dev(gates), dev(tw)
+            n = abi.workspace_size(abi.MOE_OP_DISPATCH, T, 1, 1, L.N, L.k, L.R, True, 0)
+            ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda:0")
+            i32 = dict(dtype=torch.int32, device="cuda:0")
+            for _ in range(reps):
+                o = dict(counts=torch.full((L.N,), -7, **i32), offsets=torch.full((L.N + 1,), -7, **i32),
+                         active=torch.full((L.N + 1,), -7, **i32), row_token=torch.full((T * L.k,), -7, **i32),
+                         row_gate=torch.full((T * L.k,), -7.0, dtype=torch.float32, device="cuda:0"),
+                         status=torch.full((T, L.k), 77, dtype=torch.uint8, device="cuda:0"))
+                st = torch.zeros(2, dtype=torch.int32, device="cuda:0")
+                with torch.cuda.stream(stream):
+                    abi.moe_dispatch_capacity(di, dg, L.N, L.k, L.R, o["counts"], o["offsets"], o["row_token"],
+                                              o["row_gate"], o["active"], ws, token_w=dw,
+                                              capacity_factor=L.gamma, slot_status=o["status"], st=st,
+                                              stream=stream)
+                stream.synchronize()
+                assert st.tolist() == [0, 0]
+                results.append({name: t.cpu().numpy() for name, t in o.items()})
+        except Exception as e:  # reported by the main thread
+            errors.append(e)
+
+    # each call made alone first, on the default stream
+    solo = {}
+    for name, (ids, gates, tw) in dict(big=(ids_big, gates_big, tw_big),
+                                        small=(ids_small, gates_small, tw_small)).items():
+        res, err = [], []
+        run(ids, gates, tw, torch.cuda.current_stream(), 1, res, err)
+        assert not err, err
+        solo[name] = res[0]
+    res_big, res_small, errors = [], [], []
+    th = [threading.Thread(target=run, args=(ids_big, gates_big, tw_big, torch.cuda.Stream(), 6, res_big, errors)),
+          threading.Thread(target=run, args=(ids_small, gates_small, tw_small, torch.cuda.Stream(), 40, res_small,
+                                             errors))]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    assert not errors, errors
+    assert len(res_big) == 6 and len(res_small) == 40
+    for name, results in (("big", res_big), ("small", res_small)):
+        for r in results:
+            for key in r:
+                assert np.array_equal(r[key].view(np.uint8), solo[name][key].view(np.uint8)), (name, key)

@@ -175,6 +175,19 @@ def test_empty_batch(g, ws):
     assert g.host(b["counts"]).tolist() == [0] * N
     assert g.host(b["offsets"]).tolist() == [0] * (N + 1)
     assert g.host(b["active"])[0] == 0
+    # with SERE, the union bitmap and the statistics of an empty batch are
+    # zero too, not what the previous call left there
+    sim = torch.eye(N, dtype=torch.float32, device="cuda:0")
+    sp = g.sere_params(sim, 1, 0.5)
+    sp.union_bitmap.fill_(-1)
+    sp.stats.fill_(-7)
+    b = _buffers(0, N, k)
+    moe.moe_route_dispatch(x, w_r, b["logits"], b["ids"], b["gates"], b["counts"], b["offsets"], b["row_token"],
+                           b["row_gate"], b["active"], ws, 0, sp)
+    torch.cuda.synchronize()
+    assert g.host(sp.union_bitmap).tolist() == [0] * ((N + 31) // 32)
+    assert g.host(sp.stats).tolist() == [0] * 8
+    assert g.host(b["counts"]).tolist() == [0] * N
 
 
 def test_layer_forward_uses_single_launch_path(g):
