@@ -781,8 +781,7 @@ def run_stack(args):
         xres.copy_(x0_f32)
         xb.copy_(x0_bf16)
         for lay in stack:
-            lay.route_and_dispatch(xb, sere)
-            lay.ffn(xb, accumulate_into=xres)
+            lay.forward(xb, sere=sere, accumulate_into=xres)
             moe.moe_residual_to_bf16(xres, xb)
 
     res = {}

@@ -26,6 +26,7 @@ MOE_ROUTE_FROM_LOGITS, MOE_ROUTE_RENORM_TOPK = 1, 2
 MOE_FFN_FUSE_COMBINE, MOE_FFN_ZERO_Y = 1, 2
 MOE_OP_DISPATCH, MOE_OP_FFN, MOE_OP_CALIBRATE, MOE_OP_TOKEN_WEIGHTS, MOE_OP_ROUTE_DISPATCH = 1, 2, 3, 4, 5
 ROUTE_DISPATCH_MAX_T, ROUTE_DISPATCH_MAX_SLOTS = 256, 2048
+DECODE_LAYER_MAX_T = 64
 MOE_SLOT_KEPT, MOE_SLOT_REROUTED, MOE_SLOT_DROPPED = 0, 1, 2
 MOE_DEV_OK, MOE_DEV_NONFINITE, MOE_DEV_TIMEOUT, MOE_DEV_BAD_INDEX = 0, 1, 2, 3
 
@@ -42,7 +43,7 @@ class _SereParams(ctypes.Structure):
                 ("protect", ctypes.c_void_p), ("union_bitmap", ctypes.c_void_p), ("stats", ctypes.c_void_p)]
 
 
-EXPORTS = ["moe_route", "moe_route_dispatch", "moe_reroute_sere", "moe_dispatch_capacity", "moe_ffn_grouped", "moe_combine",
+EXPORTS = ["moe_route", "moe_route_dispatch", "moe_decode_layer", "moe_reroute_sere", "moe_dispatch_capacity", "moe_ffn_grouped", "moe_combine",
            "moe_residual_to_bf16", "moe_token_weights", "moe_similarity_calibrate", "moe_workspace_size", "moe_status_string"]
 
 
@@ -60,6 +61,9 @@ def load(path: str = LIB_PATH):
             L.moe_route.restype = i
             L.moe_route_dispatch.argtypes = [p, i, p, i, i, i, i, u32, p, p, p, p, p, p, p, p, p, p, sz, p, p]
             L.moe_route_dispatch.restype = i
+            L.moe_decode_layer.argtypes = [p, p, p, p, p, i, i, i, i, i, u32, u32, p, p, p, p, p, p, p, p, p, p,
+                                           p, sz, p, sz, p, p]
+            L.moe_decode_layer.restype = i
             L.moe_reroute_sere.argtypes = [p, p, i, i, i, i, p, p, p]
             L.moe_reroute_sere.restype = i
             L.moe_dispatch_capacity.argtypes = [p, p, i, i, i, i, i, p, f, p, p, p, p, p, p, p, p, p, p, p, p, p,
@@ -169,6 +173,26 @@ def moe_route_dispatch(x, w_router, logits, ids, gates, counts, offsets, row_tok
                                    _ptr(row_gate), _ptr(active), _ptr(workspace), ws_bytes, _ptr(st),
                                    _stream(stream))
     _check(rc, "moe_route_dispatch")
+
+
+def moe_decode_layer(x, w_router, w_gate, w_up, w_down, logits, ids, gates, counts, offsets, row_token, row_gate,
+                     active, y, route_ws, ffn_ws, route_flags: int = 0, zero_y: bool = True,
+                     sere: Optional[SereParams] = None, st=None, stream=None):
+    """One decode layer (T <= 64, bf16): routing + dispatch in one launch and
+    the FFN with the combine fused in, the FFN starting on the experts known
+    to be active as soon as ranking ends.  y [T][H] fp32 is zeroed first when
+    zero_y, else accumulated into."""
+    T, H = x.shape
+    N, I = w_gate.shape[0], w_gate.shape[1]
+    k = ids.shape[1]
+    sp = None if sere is None else ctypes.byref(sere._c())
+    nb = lambda t: t.numel() * t.element_size()
+    rc = load().moe_decode_layer(_ptr(x), _ptr(w_router), _ptr(w_gate), _ptr(w_up), _ptr(w_down), T, H, I, N, k,
+                                 route_flags, MOE_FFN_ZERO_Y if zero_y else 0, sp, _ptr(logits), _ptr(ids),
+                                 _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(row_token), _ptr(row_gate),
+                                 _ptr(active), _ptr(y), _ptr(route_ws), nb(route_ws), _ptr(ffn_ws), nb(ffn_ws),
+                                 _ptr(st), _stream(stream))
+    _check(rc, "moe_decode_layer")
 
 
 def moe_reroute_sere(ids, gates, N: int, k: int, sere: SereParams, st=None, stream=None):

@@ -17,8 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["abi.cu", "router.cu", "route_dispatch.cu", "dispatch.cu", "dispatch_static.cu", "ffn.cu", "macs.cu",
-           "calib.cu", "cast.cu"]
+SOURCES = ["abi.cu", "router.cu", "route_dispatch.cu", "dispatch.cu", "dispatch_static.cu", "ffn.cu",
+           "ffn_decode.cu", "macs.cu", "calib.cu", "cast.cu"]
 HEADERS = ["common.cuh", "launch.h", "routing.cuh", "permute.cuh", "tmap.h", "../../include/moe_gb300.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -85,8 +85,44 @@ moe_status_t moe_route_dispatch(const void* x, int x_dtype, const float* w_route
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_route_dispatch(x, x_dtype, w_router, T, H, N, k,
                                                 (flags & MOE_ROUTE_RENORM_TOPK) != 0, logits, ids, gates, sere,
-                                                counts, offsets, row_token, row_gate, active, workspace, st,
+                                                counts, offsets, row_token, row_gate, active, workspace, false, st,
                                                 as_stream(stream)));
+}
+
+moe_status_t moe_decode_layer(const void* x, const float* w_router, const void* w_gate, const void* w_up,
+                              const void* w_down, int T, int H, int I, int N, int k, uint32_t route_flags,
+                              uint32_t ffn_flags, const moe_sere_params* sere, float* logits, int32_t* ids,
+                              float* gates, int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,
+                              int32_t* active, float* y, void* route_ws, size_t route_ws_bytes, void* ffn_ws,
+                              size_t ffn_ws_bytes, moe_dev_status* st, void* stream) {
+    if (N < 1 || N > MOE_MAX_EXPERTS || k < 1 || k > MOE_MAX_RANKS || k > N || H < 1 || I < 1)
+        return MOE_ERR_INVALID_ARG;
+    if ((route_flags & ~MOE_ROUTE_RENORM_TOPK) || (ffn_flags & ~MOE_FFN_ZERO_Y)) return MOE_ERR_INVALID_ARG;
+    if (sere != nullptr && !sere_ok(sere, N, k)) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > moe::kDecodeMaxT || T * k > moe::kRouteDispatchMaxSlots) return MOE_ERR_UNSUPPORTED;
+    if (H % 128 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (x == nullptr || w_router == nullptr || w_gate == nullptr || w_up == nullptr || w_down == nullptr ||
+        logits == nullptr || ids == nullptr || gates == nullptr || counts == nullptr || offsets == nullptr ||
+        row_token == nullptr || row_gate == nullptr || active == nullptr || y == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+        !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    if (static_cast<long long>(N) * I > 0x7fffffffLL || static_cast<long long>(N) * H > 0x7fffffffLL)
+        return MOE_ERR_UNSUPPORTED;
+    if (route_ws == nullptr || route_ws_bytes < static_cast<size_t>(moe::kRouteDispatchWs)) return MOE_ERR_WORKSPACE;
+    const size_t need = moe::ffn_workspace(T, H, I, N, k, MOE_DTYPE_BF16);
+    if (ffn_ws == nullptr || ffn_ws_bytes < need) return MOE_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(route_ws) & 255u) != 0 || (reinterpret_cast<uintptr_t>(ffn_ws) & 255u) != 0)
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = as_stream(stream);
+    cudaError_t e = moe::launch_route_dispatch(x, MOE_DTYPE_BF16, w_router, T, H, N, k,
+                                               (route_flags & MOE_ROUTE_RENORM_TOPK) != 0, logits, ids, gates, sere,
+                                               counts, offsets, row_token, row_gate, active, route_ws, true, st, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    const uint32_t* early = static_cast<const uint32_t*>(route_ws) + moe::kRouteDispatchEarlyWord;
+    return from_cuda(moe::launch_ffn_decode(x, w_gate, w_up, w_down, T, H, I, N, k, offsets, row_token, row_gate,
+                                            active, early, MOE_FFN_FUSE_COMBINE | ffn_flags, y, ffn_ws, st, s));
 }
 
 moe_status_t moe_reroute_sere(int32_t* ids, float* gates, int ld, int T, int N, int k, const moe_sere_params* sere,

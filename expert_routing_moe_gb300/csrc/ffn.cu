@@ -7,10 +7,12 @@
 // active experts' weights (the decode bottleneck the SERE article measures in
 // sec. 1.2 / 2.2).
 //
-// bf16 path (tensor cores): one persistent kernel, one CTA per SM, with the
-// weights as the 128-row MMA operand and the tokens as the N operand (decode
-// batches give each expert only a handful of rows); it is described at
-// ffn_stream_kernel below.
+// bf16 path (tensor cores), by batch size:
+//  * up to 64 tokens with k <= 16: the decode kernel of ffn_decode.cu;
+//  * otherwise up to 1023 tokens: ffn_stream_kernel below, one persistent CTA per SM
+//    with the weights as the 128-row MMA operand and each expert's rows, in
+//    chunks of 64 gathered per stage, as the N operand;
+//  * 1024 tokens and more: the token-major kernels (prefill).
 // fp32 path: a CUDA-core kernel, one CTA per row.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -31,22 +33,8 @@ constexpr int kTmCols = 256;   // its MMA N (H-tile of the down projection)
 
 static bool token_major(int T, int H) { return T >= kTokenMajorMinT && H % kTmCols == 0; }
 
-// Token-chunk width of the weight-major kernel for a batch of T tokens.
-static int ffn_nt(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
-
-// Batches of up to this many tokens run the weight-major kernel in
-// all-token mode: every unit multiplies its weight tile by the whole batch
-// (one TMA box of x per stage), and only the routed tokens' columns are used.
-constexpr int kAllTokMaxT = 64;
-static bool all_tok(int T) { return T <= kAllTokMaxT; }
-
-// Rows of the weight-major kernel's activation buffer A: one per dispatch
-// row, or, in all-token mode, NT per active expert (row item * NT + token).
-static long long stream_act_rows(int T, int N, int k) {
-    const long long M = static_cast<long long>(T) * k;
-    if (!all_tok(T)) return M;
-    return (N < M ? N : M) * ffn_nt(T);
-}
+// Token-chunk width of the weight-major kernel.
+constexpr int kStreamNT = 64;
 
 // Upper bound on the items (expert, chunk of <= nt rows) of a dispatch of M rows.
 static long long ffn_max_items(int T, int N, int k, int nt) {
@@ -88,17 +76,20 @@ static TmLayout tm_layout(int T, int H, int I, int N, int k) {
     return L;
 }
 
-// bf16 workspace.  Weight-major: the counters, then A bf16 with I columns
-// (stream_act_rows rows).  Token-major: tm_layout.
+// bf16 workspace.  Decode kernel (T <= 64): its counters, then A with NT
+// rows per expert.  Weight-major: the counters, then A [T*k][I] bf16 (row =
+// dispatch row).  Token-major: tm_layout.
 size_t ffn_workspace(int T, int H, int I, int N, int k, int dtype) {
     if (dtype != MOE_DTYPE_BF16 || T <= 0) return 0;
     if (token_major(T, H)) return tm_layout(T, H, I, N, k).total;
-    return kStreamCtrBytes + static_cast<size_t>(stream_act_rows(T, N, k)) * I * 2;
+    if (ffn_use_decode(T, k)) return ffn_decode_ctr_bytes() + static_cast<size_t>(ffn_decode_act_rows(T, N)) * I * 2;
+    return kStreamCtrBytes + static_cast<size_t>(T) * k * I * 2;
 }
+static_assert(kStreamCtrBytes >= (MOE_MAX_EXPERTS + 4) * 4, "decode kernel counters fit the zeroed region");
 
 // Bytes at the start of the workspace that must be zero before the first
-// call (the weight-major kernel's counters; the token-major kernels clear
-// their own, which follow).
+// call (the decode and weight-major kernels' counters; the token-major
+// kernels clear their own, which follow).
 size_t ffn_workspace_zero_bytes(int T, int H, int N, int k, int dtype) {
     (void)H;
     (void)N;
@@ -144,12 +135,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 // phase-1 units already taken, so the waits end whatever the residency of
 // the grid; a wait that outlasts kWaitLimitNs reports MOE_DEV_TIMEOUT.
 // ---------------------------------------------------------------------------
-// Phase-1 unit modes of the weight-major kernel (template argument HM).
-constexpr int kHmWhole = 0;    // every phase-1 unit is a whole 128-row I-slice
-constexpr int kHmHybrid = 1;   // whole units, then the last items as half (64-row) units
-constexpr int kHmHalf = 2;     // every phase-1 unit is a half unit
-
-template <int NT, int HM = kHmWhole, bool AT = false>
+template <int NT>
 struct StCfg {
     static constexpr int BI = 128;                  // I-slice of a phase-1 unit (MMA M)
     static constexpr int BH = 128;                  // H-tile of a phase-2 unit (MMA M)
@@ -159,7 +145,7 @@ struct StCfg {
     static constexpr int X_ATOM = NT * 128;         // NT rows of one 64-column swizzle atom
     static constexpr int X_BYTES = 2 * X_ATOM;      // phase 2 stages 128 columns of A
     static constexpr int STAGE = W_BYTES + X_BYTES;
-    static constexpr int NSTAGE = NT <= 16 ? (HM != kHmWhole ? 5 : 6) : (NT <= 32 ? 5 : 4);
+    static constexpr int NSTAGE = NT <= 16 ? 6 : (NT <= 32 ? 5 : 4);
     static constexpr int EPI_WARPS = 8;             // two warps per TMEM lane quadrant
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
@@ -168,7 +154,6 @@ struct StCfg {
     static constexpr int NBAR = 2 * NSTAGE + 5 + 2 * QN;
     static constexpr int MISC_INTS = 8 + 64 + 8;    // tmem slot, abort flag, table size, unit ring, token list, exit flag
     static constexpr int TABLE_INTS = 6 * MOE_MAX_EXPERTS + 8;   // item table + staged active[] and offsets[]
-    static constexpr int XCH_BYTES = HM != kHmWhole ? 64 * NT * 4 : 0;   // up values of a half unit
     // dispatch rows whose token and gate are staged in shared memory at the
     // start, in one pass of the CTA's threads (batches with more rows read
     // them from global memory: a second pass would put a round trip back).
@@ -176,7 +161,7 @@ struct StCfg {
     // 0.5 us even when no row was staged.
     static constexpr int RT_CAP = NT <= 16 ? 128 : (NT <= 32 ? THREADS : 0);
     static constexpr int SMEM = 1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + TABLE_INTS * 4 +
-                                EPI_WARPS * 32 * 8 + XCH_BYTES + RT_CAP * 8;
+                                EPI_WARPS * 32 * 8 + RT_CAP * 8;
     static constexpr uint32_t TMEM_COLS = 4 * NT;   // two accumulator slots of 2 x NT columns
     static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
     static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256, "TMEM allocation");
@@ -196,17 +181,16 @@ __device__ __forceinline__ void item_info(const UnitTable& tb, int item, int NT,
     nrows = min(NT, tb.cnt[lo] - c * NT);
 }
 
-template <int NT, int HM, bool AT>
-__global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
+template <int NT>
+__global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
     ffn_stream_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
-                      const __grid_constant__ CUtensorMap tm_wg64, const __grid_constant__ CUtensorMap tm_wu64,
                       const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_act, const int32_t* __restrict__ offsets,
                       const int32_t* __restrict__ active, const int32_t* __restrict__ row_token,
                       const float* __restrict__ row_gate, __nv_bfloat16* __restrict__ act_g, int* counters,
                       int n_ctr, float* __restrict__ out, float* __restrict__ y_zero, long long y_elems, int H, int I,
-                      int N, int fuse_combine, moe_dev_status* st, int m_rows, int n_tok) {
-    using C = StCfg<NT, HM, AT>;
+                      int N, int fuse_combine, moe_dev_status* st, int m_rows) {
+    using C = StCfg<NT>;
     constexpr int CW = C::CW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,8 +205,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
     int* table = misc + C::MISC_INTS;
     int* etok_all = table + C::TABLE_INTS;           // [EPI_WARPS][32] tokens of each epilogue warp
     float* egt_all = reinterpret_cast<float*>(etok_all + C::EPI_WARPS * 32);   // [EPI_WARPS][32] their gates
-    float* xch = egt_all + C::EPI_WARPS * 32;        // [NT][64] up values of a half unit
-    int* s_rt = reinterpret_cast<int*>(xch + C::XCH_BYTES / 4);   // [RT_CAP] row -> token
+    int* s_rt = reinterpret_cast<int*>(egt_all + C::EPI_WARPS * 32);   // [RT_CAP] row -> token
     float* s_rg = reinterpret_cast<float*>(s_rt + C::RT_CAP);     // [RT_CAP] row -> gate
     const bool rt_staged = C::RT_CAP > 0 && m_rows <= C::RT_CAP;
     UnitTable tb{table, table + MOE_MAX_EXPERTS, table + 2 * MOE_MAX_EXPERTS, table + 3 * MOE_MAX_EXPERTS, 0};
@@ -265,8 +248,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_act);
     }
-    const int S = I / C::BI;   // whole phase-1 units per item
-    const int S2 = I / 64;     // half phase-1 units per item
+    const int S = I / C::BI;   // phase-1 units per item
     const int MT = H / C::BH;
     const int KT2 = I / (2 * C::BK);
     int* const work_head = counters;           // next unit to hand out
@@ -328,9 +310,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                 if (e < 0 || e >= N) e = 0;   // a corrupt list cannot index past offsets
                 r0 = s_off[e];
                 cnt = s_off[e + 1] - r0;
-                // rows must lie in [0, T k); in all-token mode an expert holds
-                // each token at most once, so one item per expert
-                if (r0 < 0 || cnt < 0 || r0 + cnt > m_rows || (AT && cnt > n_tok)) {
+                if (r0 < 0 || cnt < 0 || r0 + cnt > m_rows) {   // rows must lie in [0, T k)
                     bad = true;
                     cnt = 0;
                 }
@@ -350,9 +330,8 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
             }
             run += __shfl_sync(kFull, inc, 31);
         }
-        // items index the per-item counters (n_ctr - 1 of them) and, in
-        // all-token mode, NT rows each of A: a dispatch that would exceed
-        // either is reported and nothing is computed
+        // items index the per-item counters (n_ctr - 1 of them): a dispatch
+        // that would exceed them is reported and nothing is computed
         bad = __any_sync(kFull, bad) || run > n_ctr - 1;
         if (lane == 0) {
             if (bad) report(st, MOE_DEV_BAD_INDEX, run);
@@ -369,44 +348,29 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
     // streaming.  (At larger batches the extra reductions into y cost more
     // than the shorter units save.)
     const int KP2 = (KT2 % 2 == 0 && s_items[1] * MT < 2 * static_cast<int>(gridDim.x)) ? 2 : 1;
-    // Half units cover 64 I rows: their 64 gate and 64 up rows are stacked
-    // as one 128-row operand, so an item splits into twice as many phase-1
-    // units.  Items [0, iw) run whole units and items [iw, items) half units.
-    // kHmHalf (chosen on the host for batches whose phase 1 cannot give every
-    // SM a whole 128-row I-slice) makes every item half.  kHmHybrid splits
-    // the last items when the whole units would leave a partial last wave of
-    // at most half the grid: those units, one slice each, then run as twice as
-    // many half units over the SMs that the wave leaves free, so the items of
-    // the last wave publish their activations about half a unit earlier and
-    // their down-projection units stop waiting for them.
-    const int n_items = s_items[1];
-    int iw = n_items;
-    if (HM == kHmHalf) {
-        iw = 0;
-    } else if (HM == kHmHybrid) {
-        const int G = static_cast<int>(gridDim.x), u1 = n_items * S, left = u1 % G;
-        if (u1 > G && left > 0) {
-            const int h = (left + S - 1) / S;
-            if (2 * h * S <= G) iw = n_items - h;
-        }
-    }
     const int KT2P = KT2 / KP2;
-    // units: phase 1 = [0, n1w) as item * S + slice for the whole items, then
-    // [n1w, n1) as n1w + (item - iw) * S2 + half slice, phase 2 =
-    // [n1, n1 + n2) as n1 + (item * MT + h-tile) * KP2 + K part
-    const int n1w = iw * S, n1 = n1w + (n_items - iw) * S2, n_total = n1 + n_items * MT * KP2;
-    // part of a phase-1 unit: 1 for a half unit
+    // units: phase 1 = [0, n1) as item * S + slice, phase 2 = [n1, n1 + n2) as
+    // n1 + (item * MT + h-tile) * KP2 + K part
+    const int n1 = s_items[1] * S, n_total = n1 + s_items[1] * MT * KP2;
+    if (n_total == 0) {
+        // no rows (or a dispatch that was rejected): y, when zeroed here, is
+        // the only output
+        if (y_zero != nullptr)
+            for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < y_elems;
+                 i += static_cast<long long>(gridDim.x) * blockDim.x)
+                y_zero[i] = 0.f;
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(*tmem_slot, C::TMEM_COLS);
+        }
+        finish();
+        return;
+    }
     auto decode = [&](int u, int& item, int& sub, int& part) {
-        if (u < n1w) {
+        if (u < n1) {
             item = u / S;
             sub = u - item * S;
             part = 0;
-        } else if (u < n1) {
-            const int v = u - n1w;
-            const int hi = v / S2;
-            item = iw + hi;
-            sub = v - hi * S2;
-            part = 1;
         } else {
             const int v = u - n1;
             item = v / (MT * KP2);
@@ -445,10 +409,9 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
             const bool p1 = cur < n1;
             int item, sub, part;   // sub: I-slice or H-tile
             decode(cur, item, sub, part);
-            const bool hu = HM != kHmWhole && p1 && part != 0;   // a half phase-1 unit
             int e, row0, nrows;
             item_info(tb, item, NT, e, row0, nrows);
-            if (!AT && p1) {
+            if (p1) {
                 // rows past the chunk repeat its first token; their columns are never used
                 for (int t = lane; t < NT; t += 32) {
                     const int r = row0 + (t < nrows ? t : 0);
@@ -460,8 +423,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                 if (!p1) {
                     // A of this item: all S phase-1 units must have published their slices
                     const unsigned long long t0 = global_ns();
-                    const int need = item < iw ? S : S2;
-                    while (ld_acquire_gpu(item_done + item) < need ||
+                    while (ld_acquire_gpu(item_done + item) < S ||
                            (n_zchunks > 0 && ld_acquire_gpu(zero_done) < n_zchunks)) {
                         if (*abort_flag) {
                             ok = false;
@@ -479,7 +441,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                 }
                 const int n_g4 = (nrows + 3) / 4;
                 const int n16 = (min(NT, max(16, (nrows + 15) & ~15))) / 16;
-                const int nk = p1 ? (hu ? KT1 / 2 : KT1) : KT2P;
+                const int nk = p1 ? KT1 : KT2P;
                 for (int kt = 0; kt < nk && ok; ++kt) {
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
@@ -487,52 +449,24 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                     }
                     const uint32_t dst = ring_a + stage * C::STAGE;
                     const uint32_t fb = bar(B_FULL + stage);
-                    if (hu) {
-                        // two 64-column K chunks; each is [64 gate rows; the same 64 up rows]
-                        const int wrow = e * I + sub * 64;
-                        mbar_arrive_expect_tx(fb, C::W_BYTES + 2 * (AT ? C::X_ATOM : n_g4 * 512));
-                        for (int c = 0; c < 2; ++c) {
-                            const int kc = kt * 2 * C::BK + c * C::BK;
-                            tma_load_2d(dst + c * C::W_BOX, &tm_wg64, kc, wrow, fb, pol_w);
-                            tma_load_2d(dst + c * C::W_BOX + C::W_BOX / 2, &tm_wu64, kc, wrow, fb, pol_w);
-                            if (AT) {
-                                // the whole batch: one box of NT rows (rows past T read as zero)
-                                tma_load_2d(dst + C::W_BYTES + c * C::X_ATOM, &tm_x, kc, 0, fb, pol_x);
-                            } else {
-                                for (int g = 0; g < n_g4; ++g)
-                                    tma_gather4(dst + C::W_BYTES + c * C::X_ATOM + g * 512, &tm_x, kc, ptok[4 * g],
-                                                ptok[4 * g + 1], ptok[4 * g + 2], ptok[4 * g + 3], fb, pol_x);
-                            }
-                        }
-                    } else if (p1) {
+                    if (p1) {
                         const int wrow = e * I + sub * C::BI;
-                        mbar_arrive_expect_tx(fb, C::W_BYTES + (AT ? C::X_ATOM : n_g4 * 512));
+                        mbar_arrive_expect_tx(fb, C::W_BYTES + n_g4 * 512);
                         tma_load_2d(dst, &tm_wg, kt * C::BK, wrow, fb, pol_w);
                         tma_load_2d(dst + C::W_BOX, &tm_wu, kt * C::BK, wrow, fb, pol_w);
-                        if (AT) {
-                            tma_load_2d(dst + C::W_BYTES, &tm_x, kt * C::BK, 0, fb, pol_x);
-                        } else {
-                            for (int g = 0; g < n_g4; ++g)
-                                tma_gather4(dst + C::W_BYTES + g * 512, &tm_x, kt * C::BK, ptok[4 * g],
-                                            ptok[4 * g + 1], ptok[4 * g + 2], ptok[4 * g + 3], fb, pol_x);
-                        }
+                        for (int g = 0; g < n_g4; ++g)
+                            tma_gather4(dst + C::W_BYTES + g * 512, &tm_x, kt * C::BK, ptok[4 * g], ptok[4 * g + 1],
+                                        ptok[4 * g + 2], ptok[4 * g + 3], fb, pol_x);
                     } else {
                         const int wrow = e * H + sub * C::BH;
                         const int kc = (part * KT2P + kt) * 2 * C::BK;   // first K column of this stage
-                        mbar_arrive_expect_tx(fb, C::W_BYTES + 2 * (AT ? C::X_ATOM : n16 * 2048));
+                        mbar_arrive_expect_tx(fb, C::W_BYTES + 2 * n16 * 2048);
                         tma_load_2d(dst, &tm_wd, kc, wrow, fb, pol_w);
                         tma_load_2d(dst + C::W_BOX, &tm_wd, kc + C::BK, wrow, fb, pol_w);
-                        for (int a = 0; a < 2; ++a) {
-                            if (AT) {
-                                // the item's activations for the whole batch: rows item * NT ..
-                                tma_load_2d(dst + C::W_BYTES + a * C::X_ATOM, &tm_act, kc + a * C::BK, item * NT,
-                                            fb, pol_x);
-                            } else {
-                                for (int g = 0; g < n16; ++g)
-                                    tma_load_2d(dst + C::W_BYTES + a * C::X_ATOM + g * 2048, &tm_act,
-                                                kc + a * C::BK, row0 + 16 * g, fb, pol_x);
-                            }
-                        }
+                        for (int a = 0; a < 2; ++a)
+                            for (int g = 0; g < n16; ++g)
+                                tma_load_2d(dst + C::W_BYTES + a * C::X_ATOM + g * 2048, &tm_act,
+                                            kc + a * C::BK, row0 + 16 * g, fb, pol_x);
                     }
                     pend |= 1u << stage;
                     pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -567,18 +501,15 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                 const bool p1 = un < n1;
                 int item, sub, part;
                 decode(un, item, sub, part);
-                const bool hu = HM != kHmWhole && p1 && part != 0;
                 int e, row0, nrows;
                 item_info(tb, item, NT, e, row0, nrows);
-                // the MMA's N is the item's row count (all-token mode: the batch size)
-                // rounded up to 16
-                const int ncol = AT ? n_tok : nrows;
-                const uint32_t idesc = idesc_bf16_f32(128, min(NT, max(16, (ncol + 15) & ~15)));
+                // the MMA's N is the item's row count rounded up to 16
+                const uint32_t idesc = idesc_bf16_f32(128, min(NT, max(16, (nrows + 15) & ~15)));
                 const int b = j & 1;
                 const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
                 if (!mbar_wait(bar(B_ACCE + b), ((j >> 1) & 1) ^ 1, abort_flag, st, kSiteMmaTmemFree)) break;
                 tc_fence_after();
-                const int nk = p1 ? (hu ? KT1 / 2 : KT1) : KT2P;
+                const int nk = p1 ? KT1 : KT2P;
                 for (int kt = 0; kt < nk; ++kt) {
                     if (!mbar_wait(bar(B_FULL + stage), phase, abort_flag, st, kSiteMmaFull)) {
                         ok = false;
@@ -586,7 +517,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t a = ring_a + stage * C::STAGE;
-                    if (p1 && !hu) {
+                    if (p1) {
 #pragma unroll
                         for (int kk = 0; kk < C::BK / 16; ++kk) {
                             const uint64_t dx = sw128_desc(a + C::W_BYTES + kk * 32);
@@ -649,68 +580,19 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
             const bool p1 = un < n1;
             int item, sub, part;
             decode(un, item, sub, part);
-            const bool hu = HM != kHmWhole && p1 && part != 0;
             int e, row0, nrows;
             item_info(tb, item, NT, e, row0, nrows);
             const int b = j & 1;
             const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
-            // accumulator columns that hold results, and the first row of A
-            // written by this item: its dispatch rows, or in all-token mode the
-            // whole batch (columns up to the MMA's N; those past T are zero)
-            const int ncols = AT ? min(NT, max(16, (n_tok + 15) & ~15)) : nrows;
-            const size_t arow0 = AT ? static_cast<size_t>(item) * NT : static_cast<size_t>(row0);
             okw = __all_sync(kFull, mbar_wait(bar(B_ACCF + b), (j >> 1) & 1, abort_flag, st, kSiteEpiG1Done));
-            if (hu) {
-                // accumulator lanes 0-63: gate rows, 64-127: the same up rows.  The
-                // up warps stage their values in shared memory; after a barrier of
-                // all epilogue warps (taken by every warp) the gate warps form the
-                // SwiGLU for the 64 I rows of the unit.
-                if (okw && q >= 2) {
-                    tc_fence_after();
-#pragma unroll
-                    for (int c8 = 0; c8 < CW / 8; ++c8) {
-                        if (c_lo + c8 * 8 >= ncols) break;   // warp-uniform
-                        uint32_t u[8];
-                        tmem_ld8(acc0 + lane_off + c_lo + c8 * 8, u);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj)
-                            xch[(c_lo + c8 * 8 + jj) * 64 + (q - 2) * 32 + lane] = __uint_as_float(u[jj]);
-                    }
-                    tc_fence_before();
-                    mbar_arrive(bar(B_ACCE + b));
-                }
-                okw = named_sync_and(C::EPI_THREADS, okw);
-                if (okw && q < 2) {
-                    tc_fence_after();
-                    __nv_bfloat16* dst = act_g + arow0 * I + sub * 64 + row;
-#pragma unroll
-                    for (int c8 = 0; c8 < CW / 8; ++c8) {
-                        if (c_lo + c8 * 8 >= ncols) break;   // warp-uniform
-                        uint32_t g[8];
-                        tmem_ld8(acc0 + lane_off + c_lo + c8 * 8, g);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const int t = c_lo + c8 * 8 + jj;
-                            if (t < ncols)
-                                dst[static_cast<size_t>(t) * I] =
-                                    __float2bfloat16_rn(silu_mul(__uint_as_float(g[jj]), xch[t * 64 + row]));
-                        }
-                    }
-                    tc_fence_before();
-                    mbar_arrive(bar(B_ACCE + b));
-                    fence_proxy_async_global();
-                    __threadfence();
-                }
-            } else if (okw) {
+            if (okw) {
                 tc_fence_after();
                 if (p1) {
                     // SwiGLU of this thread's I row for the warp's token columns -> A (bf16, row-major)
-                    __nv_bfloat16* dst = act_g + arow0 * I + sub * C::BI + row;
+                    __nv_bfloat16* dst = act_g + static_cast<size_t>(row0) * I + sub * C::BI + row;
 #pragma unroll
                     for (int c8 = 0; c8 < CW / 8; ++c8) {
-                        if (c_lo + c8 * 8 >= ncols) break;   // warp-uniform
+                        if (c_lo + c8 * 8 >= nrows) break;   // warp-uniform
                         uint32_t g[8], u[8];
                         tmem_ld8(acc0 + lane_off + c_lo + c8 * 8, g);
                         tmem_ld8(acc1 + lane_off + c_lo + c8 * 8, u);
@@ -718,7 +600,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) {
                             const int t = c_lo + c8 * 8 + jj;
-                            if (t < ncols)
+                            if (t < nrows)
                                 dst[static_cast<size_t>(t) * I] =
                                     __float2bfloat16_rn(silu_mul(__uint_as_float(g[jj]), __uint_as_float(u[jj])));
                         }
@@ -729,20 +611,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                     fence_proxy_async_global();
                     __threadfence();
                 } else {
-                    if (AT) {
-                        // column c_lo + js is token c_lo + js: etok[js] = its dispatch row
-                        // in this item, or -1 when the token was not routed here
-                        if (lane < CW) etok[lane] = -1;
-                        __syncwarp();
-                        for (int jr = lane; jr < nrows; jr += 32) {
-                            const int r = row0 + jr;
-                            const int t = rt_staged ? s_rt[r] : row_token[r];
-                            if (t >= c_lo && t < c_lo + CW) {
-                                etok[t - c_lo] = r;
-                                egt[t - c_lo] = rt_staged ? s_rg[r] : row_gate[r];
-                            }
-                        }
-                    } else if (lane < CW) {
+                    if (lane < CW) {
                         const int t = c_lo + lane;
                         etok[lane] = (t < nrows) ? (rt_staged ? s_rt[row0 + t] : row_token[row0 + t]) : 0;
                         egt[lane] = (t < nrows) ? (rt_staged ? s_rg[row0 + t] : row_gate[row0 + t]) : 0.f;
@@ -754,7 +623,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                     const int h = sub * C::BH + row;
 #pragma unroll
                     for (int c16 = 0; c16 < CW / CH; ++c16) {
-                        const bool any = c_lo + c16 * CH < ncols;   // warp-uniform
+                        const bool any = c_lo + c16 * CH < nrows;   // warp-uniform
                         uint32_t vv[CH];
                         if (any) {
                             if constexpr (CH == 8) {
@@ -773,15 +642,7 @@ __global__ void __launch_bounds__(StCfg<NT, HM, AT>::THREADS, 1)
                         for (int jj = 0; jj < CH; ++jj) {
                             const int t = c_lo + c16 * CH + jj;
                             const int js = c16 * CH + jj;
-                            if (AT) {
-                                const int r = etok[js];
-                                if (r >= 0) {
-                                    if (fuse_combine)
-                                        atomicAdd(out + static_cast<size_t>(t) * H + h, egt[js] * __uint_as_float(vv[jj]));
-                                    else
-                                        atomicAdd(out + static_cast<size_t>(r) * H + h, __uint_as_float(vv[jj]));
-                                }
-                            } else if (t < nrows) {
+                            if (t < nrows) {
                                 if (fuse_combine)
                                     atomicAdd(out + static_cast<size_t>(etok[js]) * H + h,
                                               egt[js] * __uint_as_float(vv[jj]));
@@ -1298,12 +1159,12 @@ static cudaError_t launch_zero(float* p, long long n, cudaStream_t s, int* c = n
     return launch_pdl(zero_kernel, dim3(grid), dim3(256), 0, s, p, n, c, nc);
 }
 
-template <int NT, int HM, bool AT>
+template <int NT>
 static cudaError_t run_stream(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
                               int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                               const int32_t* active, uint32_t flags, float* out, void* ws, moe_dev_status* st,
                               cudaStream_t s) {
-    using C = StCfg<NT, HM, AT>;
+    using C = StCfg<NT>;
     const bool fuse = (flags & MOE_FFN_FUSE_COMBINE) != 0;
     const long long M = static_cast<long long>(T) * k;
     const long long items = ffn_max_items(T, N, k, NT);
@@ -1313,16 +1174,12 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
     int* counters = static_cast<int*>(ws);
     __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + kStreamCtrBytes);
     float* y_zero = (fuse && (flags & MOE_FFN_ZERO_Y)) ? out : nullptr;
-    CUtensorMap tm_wg, tm_wu, tm_wg64, tm_wu64, tm_wd, tm_x, tm_act;
+    CUtensorMap tm_wg, tm_wu, tm_wd, tm_x, tm_act;
     if (!make_tmap(&tm_wg, wg, H, static_cast<uint64_t>(N) * I, 64, 128) ||
         !make_tmap(&tm_wu, wu, H, static_cast<uint64_t>(N) * I, 64, 128) ||
-        !make_tmap(&tm_wg64, wg, H, static_cast<uint64_t>(N) * I, 64, 64) ||
-        !make_tmap(&tm_wu64, wu, H, static_cast<uint64_t>(N) * I, 64, 64) ||
         !make_tmap(&tm_wd, wd, I, static_cast<uint64_t>(N) * H, 64, 128) ||
-        // token rows: single rows for the gathers, or (all-token mode) boxes of
-        // NT rows covering the whole batch, rows past T read as zero
-        !make_tmap(&tm_x, x, H, static_cast<uint64_t>(T), 64, AT ? NT : 1) ||
-        !make_tmap(&tm_act, act, I, static_cast<uint64_t>(stream_act_rows(T, N, k)), 64, AT ? NT : 16))
+        !make_tmap(&tm_x, x, H, static_cast<uint64_t>(T), 64, 1) ||
+        !make_tmap(&tm_act, act, I, static_cast<uint64_t>(M), 64, 16))
         return cudaErrorInvalidValue;
     // the attribute is set once per device, on the first (uncaptured) call
     static std::atomic<bool> attr_set[64] = {};   // per device; idempotent, race-free
@@ -1331,17 +1188,16 @@ static cudaError_t run_stream(const void* x, const void* wg, const void* wu, con
     if (devi < 0 || devi >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[devi]) {
         cudaError_t ae =
-            cudaFuncSetAttribute(ffn_stream_kernel<NT, HM, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+            cudaFuncSetAttribute(ffn_stream_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (ae != cudaSuccess) return ae;
         attr_set[devi] = true;
     }
-    const long long max_units = items * (I / 64 + H / C::BH);
+    const long long max_units = items * (I / C::BI + H / C::BH);
     int grid = sm_count();
     if (max_units < grid) grid = static_cast<int>(max_units > 0 ? max_units : 1);
-    return launch_pdl(ffn_stream_kernel<NT, HM, AT>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wg64,
-                      tm_wu64, tm_wd, tm_x, tm_act, offsets, active, row_token, row_gate, act, counters,
-                      static_cast<int>(items + 1), out, y_zero, static_cast<long long>(T) * H, H, I, N, fuse ? 1 : 0,
-                      st, static_cast<int>(M), T);
+    return launch_pdl(ffn_stream_kernel<NT>, dim3(grid), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu, tm_wd, tm_x,
+                      tm_act, offsets, active, row_token, row_gate, act, counters, static_cast<int>(items + 1), out,
+                      y_zero, static_cast<long long>(T) * H, H, I, N, fuse ? 1 : 0, st, static_cast<int>(M));
 }
 
 static cudaError_t run_tokmajor(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
@@ -1404,26 +1260,12 @@ cudaError_t launch_ffn_bf16(const void* x, const void* wg, const void* wu, const
     // batches with many rows per expert run token-major on the tensor cores
     if (token_major(T, H))
         return run_tokmajor(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws, st, s);
-    // larger batches: token chunks of 64 rows gathered per stage
-    if (!all_tok(T))
-        return run_stream<64, kHmHybrid, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active,
-                                                flags, out, ws, st, s);
-    switch (ffn_nt(T)) {
-        case 16:
-            // half phase-1 units when even min(N, T*k) active experts give
-            // fewer whole 128-row I-slices than SMs
-            if (static_cast<long long>(N < T * k ? N : T * k) * (I / 128) < sm_count())
-                return run_stream<16, kHmHalf, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active,
-                                                     flags, out, ws, st, s);
-            return run_stream<16, kHmWhole, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active,
-                                                  flags, out, ws, st, s);
-        case 32:
-            return run_stream<32, kHmHybrid, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active,
-                                                   flags, out, ws, st, s);
-        default:
-            return run_stream<64, kHmHybrid, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active,
-                                                   flags, out, ws, st, s);
-    }
+    // decode batches: the all-token kernel (ffn_decode.cu)
+    if (ffn_use_decode(T, k))
+        return launch_ffn_decode(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, nullptr, flags,
+                                 out, ws, st, s);
+    return run_stream<kStreamNT>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, flags, out, ws,
+                                 st, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -44,10 +44,14 @@ constexpr int kSereMaxT = 4096;
 constexpr int kRouteDispatchMaxT = 256;
 constexpr int kRouteDispatchMaxSlots = 2048;   // T * k
 constexpr int kRouteDispatchWs = 512;
+// workspace word where the routing launch publishes its early experts for
+// the decode FFN: a flag, then the bitmap (SERE's primary union P, else the
+// union of all ranked experts), written as soon as ranking ends
+constexpr int kRouteDispatchEarlyWord = 96;
 cudaError_t launch_route_dispatch(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int k,
                                   bool renorm, float* logits, int32_t* ids, float* gates, const moe_sere_params* sere,
                                   int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,
-                                  int32_t* active, void* ws, moe_dev_status* st, cudaStream_t s);
+                                  int32_t* active, void* ws, bool publish_early, moe_dev_status* st, cudaStream_t s);
 
 // ---- dispatch (dispatch.cu) ----
 size_t dispatch_workspace(int T, int N, int k, int R, bool capped);
@@ -58,6 +62,23 @@ cudaError_t launch_dispatch(const int32_t* ids, const float* gates, int ld, int 
                             int32_t* slot_row, uint8_t* slot_status, int64_t* load_q, int64_t* cap_q, void* ws,
                             moe_dev_status* st, cudaStream_t s);
 constexpr int kCapacityMaxT = 16384;
+
+// ---- decode FFN, batches of up to 64 tokens (ffn_decode.cu) ----
+constexpr int kDecodeMaxT = 64;
+// batches the decode kernel runs (it stages every dispatch row, k <= 16)
+inline bool ffn_use_decode(int T, int k) { return T >= 1 && T <= kDecodeMaxT && k <= MOE_MAX_RANKS; }
+// token columns of the decode kernel's MMA operand for a batch of T tokens
+inline int ffn_decode_nt(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
+// its counters (work counter, one per expert, three more) sit in a fixed
+// region at the start of the workspace; the activations follow
+inline size_t ffn_decode_ctr_bytes() { return 2304; }
+long long ffn_decode_act_rows(int T, int N);
+// early: the routing launch's published early experts ([0] flag, then a
+// bitmap), or nullptr to wait for the preceding launch at the start
+cudaError_t launch_ffn_decode(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
+                              int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
+                              const int32_t* active, const uint32_t* early, uint32_t flags, float* out, void* ws,
+                              moe_dev_status* st, cudaStream_t s);
 
 // ---- FFN (ffn.cu) ----
 // the fp32 kernel holds a row's x and activations in shared memory: (H + I) floats

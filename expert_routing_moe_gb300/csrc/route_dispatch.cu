@@ -44,12 +44,14 @@ constexpr int kRdEpc = kRdThreads / 128;
 constexpr int kRdStageN = 128;     // the similarity is staged in shared memory up to N = 128 (64 KiB)
 
 // Workspace words (int32): [0] batch ticket, [8, 16) primary union P,
-// [16, 24) union before the reroute, [32, 32 + ceil(T/4)) group tickets.
-constexpr int kWsTicket = 0, kWsP = 8, kWsUb = 16, kWsGroups = 32;
-static_assert(kWsGroups + kRouteDispatchMaxT / 4 <= kRouteDispatchWs / 4, "workspace words");
+// [16, 24) union before the reroute, [32, 32 + ceil(T/4)) group tickets,
+// [96] early flag and [97, 105) early bitmap (published for the decode FFN).
+constexpr int kWsTicket = 0, kWsP = 8, kWsUb = 16, kWsGroups = 32, kWsEarly = kRouteDispatchEarlyWord;
+static_assert(kWsGroups + kRouteDispatchMaxT / 4 <= kWsEarly, "workspace words");
+static_assert(kWsEarly + 1 + kMaxPerLane <= kRouteDispatchWs / 4, "workspace words");
 
 struct RdArgs {
-    int T, H, N, k, kp, renorm, stage_sim;
+    int T, H, N, k, kp, renorm, stage_sim, publish;
     float rho;
     const float* sim;
     const uint8_t* protect;
@@ -81,10 +83,10 @@ __device__ __forceinline__ void rank_group(const RdArgs& a, int g, moe_dev_statu
     if (lane < a.k) {
         a.ids[static_cast<size_t>(t) * a.k + lane] = id;
         a.gates[static_cast<size_t>(t) * a.k + lane] = gt;
-        if (SERE && id >= 0) {
+        if ((SERE || a.publish) && id >= 0 && id < a.N) {
             uint32_t* ws = reinterpret_cast<uint32_t*>(a.ws);
             atomicOr(&ws[kWsUb + (id >> 5)], 1u << (id & 31));
-            if (lane < a.kp) atomicOr(&ws[kWsP + (id >> 5)], 1u << (id & 31));
+            if (SERE && lane < a.kp) atomicOr(&ws[kWsP + (id >> 5)], 1u << (id & 31));
         }
     }
 }
@@ -232,7 +234,7 @@ __device__ __forceinline__ void batch_tail(const RdArgs& a, float* s_sim, uint64
     const int nw = (T + 31) / 32;
     const uint8_t* prot = (SERE && a.protect != nullptr) ? s_prot : nullptr;
     uint32_t* ws = reinterpret_cast<uint32_t*>(a.ws);
-    if (SERE && threadIdx.x < kMaxPerLane) {
+    if ((SERE || a.publish) && threadIdx.x < kMaxPerLane) {
         Pbits[threadIdx.x] = __ldcg(&ws[kWsP + threadIdx.x]);
         Ubefore[threadIdx.x] = __ldcg(&ws[kWsUb + threadIdx.x]);
         ws[kWsP + threadIdx.x] = 0u;    // consumed: zero for the next call
@@ -241,6 +243,13 @@ __device__ __forceinline__ void batch_tail(const RdArgs& a, float* s_sim, uint64
     if (SERE && a.protect != nullptr && threadIdx.x < N) s_prot[threadIdx.x] = a.protect[threadIdx.x];
     for (int i = threadIdx.x; i < N * nw; i += blockDim.x) bits[i] = 0u;
     __syncthreads();
+    if (a.publish && threadIdx.x == 0) {
+        // the experts the decode FFN may start on now: SERE never takes a
+        // primary away, so P is active whatever the reroute does; without
+        // SERE the union of the ranked experts is the active set
+        for (int w = 0; w < kMaxPerLane; ++w) ws[kWsEarly + 1 + w] = SERE ? Pbits[w] : Ubefore[w];
+        st_release_gpu(reinterpret_cast<int*>(ws) + kWsEarly, 1);
+    }
     // bit t of expert e's presence bitmap marks token t holding e (a token
     // holds an expert at most once)
     for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
@@ -372,6 +381,15 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(const XT*
     __shared__ __align__(8) uint64_t sim_bar;
     __shared__ int abort_flag;
     pdl_wait();
+    if (a.publish && blockIdx.x == 0 && blockIdx.y == 0) {
+        // the early flag goes back to zero before any CTA of this grid lets
+        // the FFN launch, so the FFN can only see this call's publication
+        if (threadIdx.x == 0) {
+            a.ws[kWsEarly] = 0;
+            __threadfence();
+        }
+        __syncthreads();
+    }
     pdl_trigger();
     if (SERE && blockIdx.x == 0 && blockIdx.y == 0) {
         // pull the similarity into the L2 while the logits are computed
@@ -448,8 +466,10 @@ static cudaError_t rd_launch_pl(const XT* x, const float* w, const RdArgs& a, bo
 cudaError_t launch_route_dispatch(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int k,
                                   bool renorm, float* logits, int32_t* ids, float* gates, const moe_sere_params* sere,
                                   int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,
-                                  int32_t* active, void* ws, moe_dev_status* st, cudaStream_t s) {
+                                  int32_t* active, void* ws, bool publish_early, moe_dev_status* st,
+                                  cudaStream_t s) {
     RdArgs a{};
+    a.publish = publish_early ? 1 : 0;
     a.T = T;
     a.H = H;
     a.N = N;

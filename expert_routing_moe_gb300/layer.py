@@ -1,7 +1,10 @@
 """A resident MoE layer: device weights, preallocated buffers and the C-ABI
 calls of one forward pass in order (router + rank (+ SERE) -> dispatch
-(+ capacity) -> grouped FFN with the combine fused in).  Uncapped batches of
-up to 256 tokens take the single-launch routing + dispatch entry point.
+(+ capacity) -> grouped FFN with the combine fused in).  Uncapped bf16
+batches of up to 64 tokens take the one-call decode layer (moe_decode_layer:
+the FFN starts on the experts known to be active while routing finishes);
+other uncapped batches of up to 256 tokens the single-launch routing +
+dispatch entry point.
 Buffers are sized once for a maximum batch, so a forward pass allocates
 nothing and can be captured in a CUDA graph."""
 from __future__ import annotations
@@ -82,6 +85,23 @@ class MoELayer:
                                self.offsets, self.row_token, self.row_gate, self.active, self.ws_route, self.flags,
                                sp, self.status, stream)
 
+    def decode_layer_ok(self, x: torch.Tensor) -> bool:
+        """Whether moe_decode_layer can run this batch: uncapped top-k,
+        bf16 activations and weights, 1 <= T <= 64."""
+        T = x.shape[0]
+        return (self.fused_route_dispatch_ok(T) and 1 <= T <= abi.DECODE_LAYER_MAX_T
+                and x.dtype == torch.bfloat16 and self.w_gate.dtype == torch.bfloat16
+                and self.H % 128 == 0 and self.I % 128 == 0)
+
+    def decode_layer(self, x: torch.Tensor, sere: bool, y: torch.Tensor, zero_y: bool = True, stream=None):
+        """Routing, dispatch and the FFN of one decode batch in one call;
+        y [T][H] fp32 is overwritten (zero_y) or accumulated into."""
+        T = x.shape[0]
+        sp = self.sere_params() if (sere and self.sim is not None) else None
+        abi.moe_decode_layer(x, self.w_router, self.w_gate, self.w_up, self.w_down, self.logits[:T], self.ids[:T],
+                             self.gates[:T], self.counts, self.offsets, self.row_token, self.row_gate, self.active,
+                             y, self.ws_route, self.ws_ffn, self.flags, zero_y, sp, self.status, stream)
+
     def route_and_dispatch(self, x: torch.Tensor, sere: bool, token_w: Optional[torch.Tensor] = None, stream=None):
         """Routing (+ SERE when a similarity matrix is set) and dispatch: one
         launch for uncapped batches of up to 256 tokens, separate calls
@@ -118,14 +138,24 @@ class MoELayer:
                             self.row_gate, self.active, out, self.ws_ffn, flags, self.status, stream)
 
     def forward(self, x: torch.Tensor, sere: bool = False, token_w: Optional[torch.Tensor] = None, stream=None,
-                out: Optional[torch.Tensor] = None):
+                out: Optional[torch.Tensor] = None, accumulate_into: Optional[torch.Tensor] = None):
         """y[T][H] fp32: written into `out` if given, else into (a view of)
-        the layer's output buffer."""
+        the layer's output buffer; or added to `accumulate_into` ([T][H]
+        fp32, e.g. a residual stream), which is then returned."""
         T = x.shape[0]
         if T > self.max_T:
             raise abi.MoeError("batch %d exceeds the layer's max_tokens %d" % (T, self.max_T))
+        if token_w is None and self.decode_layer_ok(x):
+            if accumulate_into is not None:
+                self.decode_layer(x, sere, accumulate_into, zero_y=False, stream=stream)
+                return accumulate_into
+            y = self.y[:T] if out is None else out
+            self.decode_layer(x, sere, y, zero_y=True, stream=stream)
+            return y
         self.route_and_dispatch(x, sere, token_w, stream)
-        self.ffn(x, stream, out=out)
+        self.ffn(x, stream, out=out, accumulate_into=accumulate_into)
+        if accumulate_into is not None:
+            return accumulate_into
         return self.y[:T] if out is None else out
 
     def device_status(self):

@@ -152,6 +152,42 @@ moe_status_t moe_route_dispatch(const void* x, int x_dtype, const float* w_route
                                 size_t ws_bytes, moe_dev_status* st, void* stream);
 
 /*
+ * One decode MoE layer in one call: moe_route_dispatch, then the grouped
+ * SwiGLU FFN with the weighted combine fused in (y = sum_j G(x)_j E_j(x),
+ * "MACS" sec. 3.1 Eq. (1); with `sere`, the "SERE" article's batch reroute,
+ * sec. 4.1-4.2).  The FFN starts streaming the weights of the experts that
+ * are certain to be active -- SERE's primary union P (sec. 4.1: primaries
+ * are never rerouted), or without SERE the union of the ranked experts --
+ * as soon as ranking ends, while the routing launch still reroutes and
+ * permutes; the other experts and the down projections wait for the final
+ * routing.  Results equal moe_route_dispatch followed by moe_ffn_grouped
+ * with MOE_FFN_FUSE_COMBINE (up to the fp32 summation order of y).
+ *
+ *   x, w_router, sere, logits, ids, gates, counts, offsets, row_token,
+ *   row_gate, active: as moe_route_dispatch (x is BF16, [T][H])
+ *   w_gate, w_up [N][I][H], w_down [N][H][I]  bf16 expert weights
+ *   y          [T][H] fp32 out: zeroed first when ffn_flags has
+ *              MOE_FFN_ZERO_Y, else the layer output is added into it
+ *   route_flags  MOE_ROUTE_RENORM_TOPK or 0
+ *   ffn_flags    MOE_FFN_ZERO_Y or 0 (the combine is always fused)
+ *   route_ws   moe_workspace_size(MOE_OP_ROUTE_DISPATCH, ...) bytes
+ *   ffn_ws     moe_workspace_size(MOE_OP_FFN, T, H, I, N, k, k, 0, BF16) bytes
+ *              both 256-byte aligned and ZERO-FILLED before their first use
+ *              (every call leaves their counters at zero); a pair of
+ *              workspaces serves one call at a time.
+ * Limits: 1 <= T <= 64, T * k <= 2048, N <= 256, 1 <= k <= min(16, N),
+ * H % 128 == 0, I % 128 == 0, pointers 16-byte aligned.  Errors: argument
+ * errors return before anything is launched; data-dependent errors and
+ * bounded waits that ran out go to st.
+ */
+moe_status_t moe_decode_layer(const void* x, const float* w_router, const void* w_gate, const void* w_up,
+                              const void* w_down, int T, int H, int I, int N, int k, uint32_t route_flags,
+                              uint32_t ffn_flags, const moe_sere_params* sere, float* logits, int32_t* ids,
+                              float* gates, int32_t* counts, int32_t* offsets, int32_t* row_token,
+                              float* row_gate, int32_t* active, float* y, void* route_ws, size_t route_ws_bytes,
+                              void* ffn_ws, size_t ffn_ws_bytes, moe_dev_status* st, void* stream);
+
+/*
  * SERE batch reroute on given routing ("SERE" article, sec. 4.1: the union P
  * of every token's top-K' primary experts is the shared candidate set; every
  * secondary outside P whose source is not protected (sec. 4.2) moves to its

@@ -43,13 +43,13 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # bf16 FFN, batches of up to 64 tokens (all-token mode): item counters +
-    # the bf16 SwiGLU activations of the whole batch (padded to 32 tokens)
-    # for each of min(N, T k) experts
+    # bf16 FFN, batches of up to 64 tokens (the decode kernel): counters +
+    # the bf16 SwiGLU activations of the whole batch (padded to 16, 32 or 64
+    # tokens) for each of the N experts
     bf = abi.workspace_size(abi.MOE_OP_FFN, 32, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16)
     assert 128 * 32 * 768 * 2 < bf <= 128 * 32 * 768 * 2 + 4096
     bf1 = abi.workspace_size(abi.MOE_OP_FFN, 1, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16)
-    assert 8 * 16 * 768 * 2 < bf1 <= 8 * 16 * 768 * 2 + 4096
+    assert 128 * 16 * 768 * 2 < bf1 <= 128 * 16 * 768 * 2 + 4096
     # larger batches: the activations of every dispatch row
     bf = abi.workspace_size(abi.MOE_OP_FFN, 128, 2048, 768, 128, 8, 8, False, abi.MOE_DTYPE_BF16)
     assert 128 * 8 * 768 * 2 < bf <= 128 * 8 * 768 * 2 + 4096
@@ -100,6 +100,28 @@ def test_route_dispatch_rejects(lib):
     sp = abi._SereParams(3, 0.5, FAKE, None, None, None)        # K' > k
     assert f(*args(sp=ctypes.byref(sp))) == -1
     assert abi.workspace_size(abi.MOE_OP_ROUTE_DISPATCH, 32, 2048, 768, 128, 8, 8, False, 1) == 512
+
+
+def test_decode_layer_rejects(lib):
+    f = lib.moe_decode_layer
+    W = (FAKE, 1 << 30)
+    args = lambda T=32, H=128, I=128, N=8, k=2, rf=0, ff=0, sp=None, y=FAKE, rws=W, fws=W: (
+        FAKE, FAKE, FAKE, FAKE, FAKE, T, H, I, N, k, rf, ff, sp, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, y,
+        *rws, *fws, None, None)
+    assert f(*args(T=65)) == -2                                 # above the decode batch limit
+    assert f(*args(T=0)) == -2                                  # an empty batch has nothing to run
+    assert f(*args(H=192)) == -2                                # H % 128
+    assert f(*args(I=96)) == -2                                 # I % 128
+    assert f(*args(k=9)) == -1                                  # k > N
+    assert f(*args(rf=abi.MOE_ROUTE_FROM_LOGITS)) == -1         # logits are always computed here
+    assert f(*args(ff=abi.MOE_FFN_FUSE_COMBINE)) == -1          # the combine is implied; only ZERO_Y may be set
+    assert f(*args(y=None)) == -1                               # no output
+    assert f(*args(y=ctypes.c_void_p((1 << 20) + 8))) == -1    # misaligned y
+    assert f(*args(rws=(FAKE, 64))) == -4                       # routing workspace too small
+    assert f(*args(fws=(FAKE, 64))) == -4                       # FFN workspace too small
+    assert f(*args(fws=(ctypes.c_void_p((1 << 20) + 16), 1 << 30))) == -1   # misaligned FFN workspace
+    sp = abi._SereParams(3, 0.5, FAKE, None, None, None)        # K' > k
+    assert f(*args(sp=ctypes.byref(sp))) == -1
 
 
 def test_sere_rejects_bad_params(lib):
