@@ -26,10 +26,11 @@ SLOT_KEPT, SLOT_REROUTED, SLOT_DROPPED = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain C11, no contraction of a*b+c)."""
+    """Compile the oracle with gcc (plain C11, no contraction of a*b+c;
+    OpenMP over independent tokens and experts)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + ".tmp%d" % os.getpid()
-        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared",
                _SRC, "-o", tmp, "-lm"]
         subprocess.check_call(cmd)
         os.replace(tmp, _LIB_PATH)
@@ -43,6 +44,10 @@ def lib():
             build()
             L = ctypes.CDLL(_LIB_PATH)
             c_i, c_f, c_p = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+            L.orc_set_threads.restype = None
+            L.orc_set_threads.argtypes = [c_i]
+            L.orc_get_threads.restype = c_i
+            L.orc_get_threads.argtypes = []
             L.orc_exp_spec.restype = c_f
             L.orc_exp_spec.argtypes = [c_f]
             L.orc_exp_spec_array.restype = None
@@ -68,6 +73,18 @@ def lib():
             L.orc_similarity.argtypes = [c_p, c_i, c_i, c_i, c_p, c_p, c_p, c_i, c_i, c_i, c_p]
             _lib = L
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Host threads for the oracle's loops over independent tokens or experts
+    (n <= 0: every host core).  Results do not depend on it.  Returns the
+    count now in effect."""
+    lib().orc_set_threads(int(n))
+    return int(lib().orc_get_threads())
+
+
+def threads() -> int:
+    return int(lib().orc_get_threads())
 
 
 def _p(a):

@@ -15,6 +15,11 @@
  *           section 4.1 (algorithm) and 4.2 (engineering, critical-expert
  *           protection).
  *
+ * Threads: the router, the FFN + combine and the similarity calibration loop
+ * over independent tokens or experts with OpenMP (orc_set_threads).  Each
+ * output element is computed by one thread in the order written, so results
+ * are identical for every thread count.
+ *
  * Precision: everything the layer computes in floating point is done in
  * double, except the steps whose result decides an integer (the ranking, the
  * gates that order capacity admission, the similarity threshold, the merged
@@ -50,6 +55,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_OK 0
 #define ORC_EINVAL -1
@@ -123,6 +131,9 @@ static double ld_val(const void* p, int dtype, size_t i) {
 /* ------------------------------------------------------------------ */
 int orc_router(const void* x, int x_dtype, const float* w_r, int T, int H, int N, float* logits) {
     if (!x || !w_r || !logits || T < 0 || H <= 0 || N <= 0) return ORC_EINVAL;
+    /* tokens are independent: each thread owns whole rows of logits, and the
+       sum over h runs in the same order whatever the thread count */
+#pragma omp parallel for schedule(dynamic, 1)
     for (int t = 0; t < T; ++t)
         for (int j = 0; j < N; ++j) {
             double acc = 0.0;
@@ -131,6 +142,26 @@ int orc_router(const void* x, int x_dtype, const float* w_r, int T, int H, int N
             logits[(size_t)t * N + j] = (float)acc;
         }
     return ORC_OK;
+}
+
+/* Host threads used by the loops over independent tokens or experts (the
+   router, the FFN + combine, the similarity calibration's expert outputs).
+   Results do not depend on it: every output element is computed by one
+   thread in the order written.  n <= 0 selects every host core. */
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
+
+int orc_get_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
 }
 
 /* ------------------------------------------------------------------ */
@@ -483,40 +514,55 @@ int orc_ffn_combine(const void* x, int x_dtype, const void* w_gate, const void* 
     if (!x || !w_gate || !w_up || !w_down || !ids || !gates || !tok || !y || H <= 0 || I <= 0 || N <= 0 ||
         k <= 0 || ld < k || ntok < 0)
         return ORC_EINVAL;
-    double* xv = (double*)malloc(sizeof(double) * (size_t)H);
-    double* act = (double*)malloc(sizeof(double) * (size_t)I);
-    if (!xv || !act) { free(xv); free(act); return ORC_ENOMEM; }
     for (int n = 0; n < ntok; ++n) {
         int t = tok[n];
-        if (t < 0 || t >= T) { free(xv); free(act); return ORC_EINVAL; }
-        for (int h = 0; h < H; ++h) xv[h] = ld_val(x, x_dtype, (size_t)t * H + h);
-        double* yo = y + (size_t)n * H;
-        for (int h = 0; h < H; ++h) yo[h] = 0.0;
-        for (int r = 0; r < k; ++r) {
-            int e = ids[(size_t)t * ld + r];
-            if (e < 0) continue;
-            if (e >= N) { free(xv); free(act); return ORC_EINVAL; }
-            double g = (double)gates[(size_t)t * ld + r];
-            for (int i = 0; i < I; ++i) {
-                double a = 0.0, b = 0.0;
-                size_t base = ((size_t)e * I + i) * H;
-                for (int h = 0; h < H; ++h) {
-                    a += ld_val(w_gate, w_dtype, base + h) * xv[h];
-                    b += ld_val(w_up, w_dtype, base + h) * xv[h];
+        if (t < 0 || t >= T) return ORC_EINVAL;
+        for (int r = 0; r < k; ++r)
+            if (ids[(size_t)t * ld + r] >= N) return ORC_EINVAL;
+    }
+    int rc = ORC_OK;
+    /* tokens are independent: one thread computes a token's whole output row
+       in the order below, so the result does not depend on the thread count */
+#pragma omp parallel
+    {
+        double* xv = (double*)malloc(sizeof(double) * (size_t)H);
+        double* act = (double*)malloc(sizeof(double) * (size_t)I);
+        if (!xv || !act) {
+#pragma omp atomic write
+            rc = ORC_ENOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int n = 0; n < ntok; ++n) {
+            if (!xv || !act) continue;
+            int t = tok[n];
+            for (int h = 0; h < H; ++h) xv[h] = ld_val(x, x_dtype, (size_t)t * H + h);
+            double* yo = y + (size_t)n * H;
+            for (int h = 0; h < H; ++h) yo[h] = 0.0;
+            for (int r = 0; r < k; ++r) {
+                int e = ids[(size_t)t * ld + r];
+                if (e < 0) continue;
+                double g = (double)gates[(size_t)t * ld + r];
+                for (int i = 0; i < I; ++i) {
+                    double a = 0.0, b = 0.0;
+                    size_t base = ((size_t)e * I + i) * H;
+                    for (int h = 0; h < H; ++h) {
+                        a += ld_val(w_gate, w_dtype, base + h) * xv[h];
+                        b += ld_val(w_up, w_dtype, base + h) * xv[h];
+                    }
+                    act[i] = a / (1.0 + exp(-a)) * b;
                 }
-                act[i] = a / (1.0 + exp(-a)) * b;
-            }
-            for (int h = 0; h < H; ++h) {
-                double acc = 0.0;
-                size_t base = ((size_t)e * H + h) * I;
-                for (int i = 0; i < I; ++i) acc += ld_val(w_down, w_dtype, base + i) * act[i];
-                yo[h] += g * acc;
+                for (int h = 0; h < H; ++h) {
+                    double acc = 0.0;
+                    size_t base = ((size_t)e * H + h) * I;
+                    for (int i = 0; i < I; ++i) acc += ld_val(w_down, w_dtype, base + i) * act[i];
+                    yo[h] += g * acc;
+                }
             }
         }
+        free(xv);
+        free(act);
     }
-    free(xv);
-    free(act);
-    return ORC_OK;
+    return rc;
 }
 
 /* ------------------------------------------------------------------ */
@@ -594,30 +640,48 @@ int orc_similarity(const void* x, int x_dtype, int n, int H, const void* w_gate,
                    const void* w_down, int w_dtype, int I, int N, double* sim) {
     if (n < 1 || H < 1 || I < 1 || N < 1 || !x || !w_gate || !w_up || !w_down || !sim) return ORC_EINVAL;
     double* E = (double*)malloc(sizeof(double) * (size_t)N * n * H);
-    double* xv = (double*)malloc(sizeof(double) * (size_t)H);
-    double* act = (double*)malloc(sizeof(double) * (size_t)I);
-    if (!E || !xv || !act) { free(E); free(xv); free(act); return ORC_ENOMEM; }
-    for (int e = 0; e < N; ++e)
-        for (int t = 0; t < n; ++t) {
-            for (int h = 0; h < H; ++h) xv[h] = ld_val(x, x_dtype, (size_t)t * H + h);
-            for (int i = 0; i < I; ++i) {
-                double a = 0.0, b = 0.0;
-                const size_t base = ((size_t)e * I + i) * H;
-                for (int h = 0; h < H; ++h) {
-                    a += ld_val(w_gate, w_dtype, base + h) * xv[h];
-                    b += ld_val(w_up, w_dtype, base + h) * xv[h];
+    if (!E) return ORC_ENOMEM;
+    int rc = ORC_OK;
+    /* experts are independent: one thread computes an expert's outputs for
+       every calibration token, in the order below */
+#pragma omp parallel
+    {
+        double* xv = (double*)malloc(sizeof(double) * (size_t)H);
+        double* act = (double*)malloc(sizeof(double) * (size_t)I);
+        if (!xv || !act) {
+#pragma omp atomic write
+            rc = ORC_ENOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int e = 0; e < N; ++e) {
+            if (!xv || !act) continue;
+            for (int t = 0; t < n; ++t) {
+                for (int h = 0; h < H; ++h) xv[h] = ld_val(x, x_dtype, (size_t)t * H + h);
+                for (int i = 0; i < I; ++i) {
+                    double a = 0.0, b = 0.0;
+                    const size_t base = ((size_t)e * I + i) * H;
+                    for (int h = 0; h < H; ++h) {
+                        a += ld_val(w_gate, w_dtype, base + h) * xv[h];
+                        b += ld_val(w_up, w_dtype, base + h) * xv[h];
+                    }
+                    act[i] = a / (1.0 + exp(-a)) * b;
                 }
-                act[i] = a / (1.0 + exp(-a)) * b;
-            }
-            double* eo = E + ((size_t)e * n + t) * H;
-            for (int h = 0; h < H; ++h) {
-                double acc = 0.0;
-                const size_t base = ((size_t)e * H + h) * I;
-                for (int i = 0; i < I; ++i) acc += ld_val(w_down, w_dtype, base + i) * act[i];
-                eo[h] = acc;
+                double* eo = E + ((size_t)e * n + t) * H;
+                for (int h = 0; h < H; ++h) {
+                    double acc = 0.0;
+                    const size_t base = ((size_t)e * H + h) * I;
+                    for (int i = 0; i < I; ++i) acc += ld_val(w_down, w_dtype, base + i) * act[i];
+                    eo[h] = acc;
+                }
             }
         }
+        free(xv);
+        free(act);
+    }
+    if (rc != ORC_OK) { free(E); return rc; }
     const size_t K = (size_t)n * H;
+    /* each pair (i, j) is summed by one thread in the order below */
+#pragma omp parallel for schedule(dynamic, 1)
     for (int i = 0; i < N; ++i)
         for (int j = i; j < N; ++j) {
             double gij = 0.0, gii = 0.0, gjj = 0.0;
@@ -633,7 +697,5 @@ int orc_similarity(const void* x, int x_dtype, int n, int H, const void* w_gate,
             sim[(size_t)j * N + i] = v;
         }
     free(E);
-    free(xv);
-    free(act);
     return ORC_OK;
 }

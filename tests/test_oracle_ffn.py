@@ -86,3 +86,25 @@ def test_whole_tiny_layer_is_eq1():
             ref[t] += p[t, j] * E[j, t]
     assert np.array_equal(out["ids"], top.astype(np.int32))
     assert np.max(np.abs(out["y"] - ref)) <= 1e-5 * np.sqrt(np.mean(ref ** 2))
+
+
+def test_thread_count_does_not_change_results():
+    """The oracle's OpenMP loops (router, FFN + combine, similarity) give the
+    same bits with one thread and with every host core."""
+    L = syn.qwen_layer(24, H=128, N=8, k=3, I=64)
+    xb = L.x_bf16
+    try:
+        outs = []
+        for nt in (1, 0):
+            oracle.set_threads(nt)
+            logits = oracle.router(xb, L.w_r, oracle.DT_BF16)
+            ids, gates = oracle.route(logits, L.k)
+            y = oracle.ffn_combine(xb, L.w_gate, L.w_up, L.w_down, ids, gates, L.k, x_dtype=oracle.DT_BF16,
+                                   w_dtype=oracle.DT_BF16)
+            sim = oracle.similarity(xb[:5], L.w_gate, L.w_up, L.w_down, x_dtype=oracle.DT_BF16,
+                                    w_dtype=oracle.DT_BF16)
+            outs.append((logits, y, sim))
+        for a, b in zip(*outs):
+            assert np.array_equal(a, b)
+    finally:
+        oracle.set_threads(0)
