@@ -39,11 +39,40 @@ STEP_GROUP = 16  # layer steps per captured graph (decode and sweep)
 METRIC = "MoE-layer decode tokens/s (SERE K'=2, rho=0.5; top-8 alongside)"
 UNIT = "tokens/s"
 EXPERT_BYTES = 3 * H * I * 2
-# DRAM bytes (read + write) of one FFN launch from an ncu capture of the current
-# kernel (--set full, SERE batch 4 of this workload: 34 active experts, whose
-# algorithmic bytes are 34 * EXPERT_BYTES + T * H * 6).  Set it to None whenever
-# the FFN kernel changes, until it has been captured again.
-FFN_TRAFFIC_CAPTURE = {"dram_bytes": 324.22e6, "algorithmic_bytes": 321.26e6, "active_experts": 34}
+# The committed ncu summary of the decode FFN kernel.  Its DRAM traffic is
+# reported only while the kernel's sources hash to the value recorded in it.
+FFN_PROFILE = os.path.join(ROOT, "profiles", "ffn_decode_kernel_decode_b32_full.md")
+FFN_SOURCES = [os.path.join(ROOT, "expert_routing_moe_gb300", "csrc", f)
+               for f in ("ffn_decode.cu", "common.cuh", "tmap.h")]
+
+
+def ffn_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for f in FFN_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ffn_traffic_capture():
+    """(dram bytes, algorithmic bytes, active experts) of one FFN launch from
+    the committed ncu summary, or None when the summary is missing or was
+    taken on other kernel sources than the ones built now."""
+    if not os.path.exists(FFN_PROFILE):
+        return None
+    kv = {}
+    for line in open(FFN_PROFILE):
+        if line.startswith("- ") and ": " in line:
+            key, val = line[2:].split(": ", 1)
+            kv[key.strip()] = val.strip().strip("`")
+    try:
+        if kv["sources_sha256"] != ffn_sources_sha256():
+            return None
+        return (float(kv["traffic_bytes_per_launch"]), float(kv["algorithmic_bytes_per_launch"]),
+                int(kv["active_experts"]))
+    except (KeyError, ValueError):
+        return None
 
 
 def workload_config(extra=None):
@@ -134,11 +163,14 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline leg)
 # ---------------------------------------------------------------------------
-def oracle_sample(budget_s: float, max_batches: int = 64):
+def oracle_sample(budget_s: float, max_batches: int = 64, threads: int = 1):
     """Times the oracle layer (router -> rank -> SERE -> permute -> FFN) on
-    whole decode batches of the workload until `budget_s` is used."""
+    whole decode batches of the workload until `budget_s` is used, with
+    `threads` host threads (0: every core).  Returns (tokens/s, seconds,
+    batches, threads used)."""
     import oracle
     from expert_routing_moe_gb300 import synthetic as syn
+    nt = oracle.set_threads(threads)
     L = syn.decode(T)
     L.k_primary, L.rho = K_PRIMARY, RHO
     oracle.layer(L, sere_on=True, tokens=np.arange(1))  # load + warm the library
@@ -152,7 +184,19 @@ def oracle_sample(budget_s: float, max_batches: int = 64):
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
-    return toks / el, el, nb
+    return toks / el, el, nb, nt
+
+
+def cpu_baseline_legs(budget_s: float):
+    """The oracle on every host core and on one, each on whole batches of
+    the decode workload for about `budget_s` seconds."""
+    v, el, nb, nt = oracle_sample(budget_s, threads=0)
+    v1, el1, nb1, _ = oracle_sample(budget_s, threads=1)
+    what = "whole decode batches of %d tokens through the oracle layer (router, rank, SERE, permute, FFN + combine)"
+    return {"value": v, "unit": UNIT, "cores": nt, "kind": "oracle",
+            "sample": "%d %s in %.1f s on %d threads (OpenMP over tokens)" % (nb, what % T, el, nt),
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1,
+                              "sample": "%d %s in %.1f s on one thread" % (nb1, what % T, el1)}}
 
 
 def run_reference(args):
@@ -162,6 +206,7 @@ def run_reference(args):
     import oracle
     from expert_routing_moe_gb300 import synthetic as syn
     oracle.build()
+    nt = oracle.set_threads(0)  # every host core (OpenMP over tokens)
     L = syn.decode(T)
     L.k_primary, L.rho = K_PRIMARY, RHO
     # per-step sample: whole batches when the run fits in ~3 minutes, else a token subset
@@ -184,12 +229,12 @@ def run_reference(args):
     el = time.perf_counter() - t0
     value = ntok * args.steps / el
     sample = ("oracle layer per step: router, rank and SERE over the whole batch of %d tokens, FFN + combine for "
-              "%d token(s) of it" % (T, ntok))
+              "%d token(s) of it; %d host threads" % (T, ntok, nt))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -247,18 +292,18 @@ def _capture(torch, stream, layers, xs, sere, token_w=None):
     return graphs
 
 
-def _capture_steps(torch, stream, layers, xs, sere, token_w=None, group=1):
+def _capture_steps(torch, stream, layers, xs, sere, token_w=None, group=1, starts=None):
     """Graphs of `group` consecutive layer steps each (routing, dispatch and
     FFN per step, chained by programmatic dependent launch), step i on batch
     i mod len(xs) and weight copy (i mod len(xs)) mod len(layers); one graph
-    per starting batch."""
+    per starting batch in `starts` (default: every batch)."""
     graphs = []
     nb = len(xs)
     with torch.cuda.stream(stream):
-        for b0 in range(nb):
+        for j, b0 in enumerate(range(nb) if starts is None else starts):
             for i in range(group):
                 b = (b0 + i) % nb
-                for _ in range(2 if b0 == 0 else 1):
+                for _ in range(2 if j == 0 else 1):
                     layers[b % len(layers)].forward(xs[b], sere=sere, token_w=token_w)
             stream.synchronize()
             g = torch.cuda.CUDAGraph()
@@ -269,6 +314,65 @@ def _capture_steps(torch, stream, layers, xs, sere, token_w=None, group=1):
             graphs.append(g)
     torch.cuda.synchronize()
     return graphs
+
+
+class StepGraphs:
+    """Exactly `steps` layer steps as graph replays: steps // group replays of
+    graphs of `group` steps (rotating over the starting batches), then one
+    graph of the remaining steps % group steps."""
+
+    def __init__(self, torch, stream, layers, xs, sere, steps, token_w=None, group=STEP_GROUP):
+        self.group = group
+        self.full = _capture_steps(torch, stream, layers, xs, sere, token_w, group=group)
+        self.r = steps % group
+        self.rem = (_capture_steps(torch, stream, layers, xs, sere, token_w, group=self.r, starts=[0])[0]
+                    if self.r else None)
+
+    def run(self, steps, stream, torch):
+        if steps % self.group != self.r:
+            raise ValueError("the graphs were captured for a remainder of %d steps, not %d"
+                             % (self.r, steps % self.group))
+        nb = len(self.full)
+        with torch.cuda.stream(stream):
+            for i in range(steps // self.group):
+                self.full[i % nb].replay()
+            if self.rem is not None:
+                self.rem.replay()
+
+
+def _timed_passes(torch, dev, stream, sg, steps, warmup, ws, passes):
+    """`passes` timed passes of exactly `steps` steps each (after at least
+    `warmup` untimed steps), every pass bracketed by a barrier and a device
+    synchronize on both sides and timed with CUDA events on the replay
+    stream; each pass's time is the maximum over ranks.  Returns the per-pass
+    times (ms)."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    nb = len(sg.full)
+    with torch.cuda.stream(stream):
+        for i in range(-(-warmup // sg.group)):
+            sg.full[i % nb].replay()
+    out = []
+    for _ in range(passes):
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        sg.run(steps, stream, torch)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        out.append(_max_over_ranks(torch, dev, ws, e0.elapsed_time(e1)))
+    return out
+
+
+def _pass_summary(ms, steps):
+    a = np.asarray(ms) / steps
+    return {"passes": len(ms), "steps_per_pass": steps, "ms_per_step_median": float(np.median(a)),
+            "ms_per_step_min": float(a.min()), "ms_per_step_max": float(a.max()),
+            "spread_pct": float((a.max() - a.min()) / np.median(a) * 100.0)}
 
 
 def _timed_steps(torch, stream, graphs, steps, warmup, ws, group=1):
@@ -429,22 +533,22 @@ def run_ours(args):
 
     us_sere, _ = _active_counts(torch, moe, stream, layers, xs, True)
     us_top8, _ = _active_counts(torch, moe, stream, layers, xs, False)
-    s_sere = _capture_steps(torch, stream, layers, xs, True, group=STEP_GROUP)
-    s_top8 = _capture_steps(torch, stream, layers, xs, False, group=STEP_GROUP)
+    s_sere = StepGraphs(torch, stream, layers, xs, True, args.steps)
+    s_top8 = StepGraphs(torch, stream, layers, xs, False, args.steps)
     g_sere = _capture(torch, stream, layers, xs, True)
     g_top8 = _capture(torch, stream, layers, xs, False)
     # routing + SERE + permutation in one launch, then the FFN tensor-core kernel (which
     # zeroes y and resets its own counters)
-    assert layers[0].fused_route_dispatch_ok(T)
+    assert layers[0].decode_layer_ok(xs[0])
     launches_per_step = 2
 
     clk = ClockSampler(local if ws > 1 else 0)
     clk.start()
     if args.clock_soak > 0:
         _soak(torch, stream, g_sere, args.clock_soak)
-    # the headline: whole layer steps, STEP_GROUP per graph
-    total_ms, steps_t = _timed_steps(torch, stream, s_sere, args.steps, args.warmup, ws, group=STEP_GROUP)
-    total_ms = _max_over_ranks(torch, dev, ws, total_ms)
+    # the headline: exactly args.steps whole layer steps per pass, median of the passes
+    p_sere = _timed_passes(torch, dev, stream, s_sere, args.steps, args.warmup, ws, args.passes)
+    total_ms, steps_t = float(np.median(p_sere)), args.steps
     # the FFN's own duration: events around every FFN call inside the step graphs (else,
     # where events cannot be captured, a routing graph and an FFN graph with events between)
     inline = _ffn_inline(torch, stream, layers, xs, True)
@@ -455,10 +559,10 @@ def run_ours(args):
         _, ffn_ms = _timed(torch, stream, g_sere, args.steps, args.warmup, ws)
         ffn_b = [i % N_BATCHES for i in range(args.steps)]
         ffn_how = "events between a routing graph and an FFN graph per step"
-    clocks = clk.stop()
     ffn_bytes = [us_sere[b] * EXPERT_BYTES + T * H * 2 + T * H * 4 for b in ffn_b]
-    t8_ms, t8_steps = _timed_steps(torch, stream, s_top8, args.steps, args.warmup, ws, group=STEP_GROUP)
-    t8_ms = _max_over_ranks(torch, dev, ws, t8_ms)
+    p_top8 = _timed_passes(torch, dev, stream, s_top8, args.steps, args.warmup, ws, args.passes)
+    t8_ms = float(np.median(p_top8))
+    clocks = clk.stop()
     inline8 = _ffn_inline(torch, stream, layers, xs, False)
     if inline8 is not None:
         t8_ffn_ms, t8_b = inline8
@@ -509,30 +613,43 @@ def run_ours(args):
 
     # the pipelined loop of E2E_GROUP steps is captured once (two streams joined
     # by events) and replayed, as a serving loop would, so that the host enqueues
-    # one graph per E2E_GROUP steps instead of every copy and call
+    # one graph per E2E_GROUP steps instead of every copy and call; a graph of the
+    # remaining steps makes every pass exactly args.steps steps
     e2e_steps(2)
     torch.cuda.synchronize()
-    g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        e_fork = torch.cuda.Event()
-        e_fork.record(stream)
-        e2e_steps(E2E_GROUP, e_fork)
-    n_rep = max(1, args.steps // E2E_GROUP)
+
+    def e2e_graph(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e_fork = torch.cuda.Event()
+            e_fork.record(stream)
+            e2e_steps(n, e_fork)
+        return g
+
+    g_e2e = e2e_graph(E2E_GROUP)
+    g_e2e_rem = e2e_graph(args.steps % E2E_GROUP) if args.steps % E2E_GROUP else None
     with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup // E2E_GROUP)):
+        for _ in range(-(-args.warmup // E2E_GROUP)):
             g_e2e.replay()
-    torch.cuda.synchronize()
-    if ws > 1:
-        torch.distributed.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(n_rep):
-            g_e2e.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_steps_timed = n_rep * E2E_GROUP
-    e2e_ms = _max_over_ranks(torch, dev, ws, e0.elapsed_time(e1))
+    p_e2e = []
+    for _ in range(args.passes):
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps // E2E_GROUP):
+                g_e2e.replay()
+            if g_e2e_rem is not None:
+                g_e2e_rem.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        p_e2e.append(_max_over_ranks(torch, dev, ws, e0.elapsed_time(e1)))
+    e2e_ms = float(np.median(p_e2e))
     for lay in layers:
         code, detail = lay.device_status()
         if code != 0:
@@ -540,43 +657,45 @@ def run_ours(args):
 
     peak, peak_src = load_peaks()
     achieved = sum(ffn_bytes) / (sum(ffn_ms) / 1e3) / 1e9
+    cap = ffn_traffic_capture()
     line = {
         "metric": METRIC, "value": job_throughput(ws, T, steps_t, total_ms), "unit": UNIT, "n_gpus": ws,
         "steps": steps_t, "warmup": args.warmup, "ms_per_step": total_ms / steps_t,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Dirichlet-skewed router logits, N(0,0.02) bf16 experts)",
         "config": workload_config({"parallelism": "replicas" if ws > 1 else "single GPU",
-                                   "cuda_graphs": "value: graphs of 16 layer steps, each step the single-launch "
-                                                  "router + rank + SERE + permutation and then the FFN, on "
-                                                  "its own batch and weight copy; roofline: " + ffn_how +
-                                                  "; e2e: groups of 16 steps, each step "
-                                                  "uploading its x from pinned host memory and reading its y "
-                                                  "back on a copy stream overlapped with the layer, captured "
-                                                  "as one graph and replayed"}),
+                                   "cuda_graphs": "value: graphs of 16 layer steps (and one of the remaining "
+                                                  "steps), each step the single-launch router + rank + SERE + "
+                                                  "permutation and then the FFN, on its own batch and weight "
+                                                  "copy; median of %d timed passes of exactly %d steps; "
+                                                  "roofline: %s; e2e: groups of 16 steps, each step uploading "
+                                                  "its x from pinned host memory and reading its y back on a "
+                                                  "copy stream overlapped with the layer, captured as one graph "
+                                                  "and replayed" % (args.passes, args.steps, ffn_how)}),
+        "timing": _pass_summary(p_sere, steps_t),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": args.traffic if args.traffic is not None else
-                     (FFN_TRAFFIC_CAPTURE["dram_bytes"] if FFN_TRAFFIC_CAPTURE else None),
-                     "traffic_launch_algorithmic_bytes": FFN_TRAFFIC_CAPTURE["algorithmic_bytes"]
-                     if FFN_TRAFFIC_CAPTURE and args.traffic is None else None,
-                     "kernel": "moe_ffn_grouped (the tcgen05 FFN kernel, y zeroed inside)",
+                     "traffic": cap[0] if cap else None,
+                     "traffic_launch_algorithmic_bytes": cap[1] if cap else None,
+                     "traffic_source": ("ncu capture of the current kernel sources (%d active experts), %s"
+                                        % (cap[2], os.path.relpath(FFN_PROFILE, ROOT))) if cap else
+                                       "no ncu capture of the current kernel sources",
+                     "kernel": "ffn_decode_kernel (moe_ffn_grouped: the tcgen05 FFN with the combine fused in, "
+                               "y zeroed inside)",
                      "peak_source": peak_src,
                      "bytes_per_launch_mean": float(np.mean(ffn_bytes)),
                      "ms_per_launch_mean": float(np.mean(ffn_ms))},
         "active_experts": {"sere_mean": float(np.mean(us_sere)), "top8_mean": float(np.mean(us_top8))},
-        "top8": {"value": job_throughput(ws, T, t8_steps, t8_ms), "ms_per_step": t8_ms / t8_steps,
+        "top8": {"value": job_throughput(ws, T, args.steps, t8_ms), "ms_per_step": t8_ms / args.steps,
+                 "timing": _pass_summary(p_top8, args.steps),
                  "ffn_ms_mean": float(np.mean(t8_ffn_ms)),
                  "ffn_gbs": sum(t8_bytes) / (sum(t8_ffn_ms) / 1e3) / 1e9},
-        "e2e": {"value": job_throughput(ws, T, e2e_steps_timed, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
-                "d2h_bytes_per_step": T * H * 4},
+        "e2e": {"value": job_throughput(ws, T, args.steps, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 4, "timing": _pass_summary(p_e2e, args.steps)},
         "gpu_launches": launches_per_step * steps_t,
         "clocks": clocks,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, el, nb = oracle_sample(args.cpu_budget)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": "%d whole decode batches of %d tokens through the oracle layer "
-                                          "(router, rank, SERE, permute, FFN + combine) in %.1f s"
-                                          % (nb, T, el)}
+        line["cpu_baseline"] = cpu_baseline_legs(args.cpu_budget)
     elif rank == 0:
         line["cpu_baseline"] = None
     if rank == 0:
@@ -840,20 +959,22 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
+                    help="seconds of oracle time for each cpu_baseline leg (all cores, one core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=4, help="expert-weight copies rotated per step")
     ap.add_argument("--clock-soak", type=float, default=1.5, help="seconds of untimed load while sampling clocks")
     ap.add_argument("--workload", choices=["decode", "sweep", "prefill", "stack", "calibrate"], default="decode",
                     help="decode (the headline line) or one of the further workloads")
     ap.add_argument("--layers", type=int, default=48, help="layers of the stack workload")
-    ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per FFN launch from an ncu capture of the same kernel build, if known")
+    ap.add_argument("--passes", type=int, default=5, help="timed passes of --steps steps (median reported)")
     args = ap.parse_args()
     global N_COPIES
     N_COPIES = max(1, args.copies)
     if args.warmup < 3:
         args.warmup = 3
+    if args.steps < 1 or args.passes < 1:
+        ap.error("--steps and --passes must be positive")
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "sweep":

@@ -30,7 +30,14 @@ def _layer(g, L, D, capped=False):
                         capacity_factor=L.gamma if capped else 0.0)
 
 
-def _run(g, L, sere, capped=False, tokens=None, max_mismatch=0):
+def _router_bound_ok(L, gl, ref_logits):
+    """The GPU router's fp32 logits agree with the oracle's double-accumulated
+    ones within the fp32 dot-product bound H * 2^-24 * sum_h |x_h W_jh|."""
+    xabs = np.abs(L.x.astype(np.float64)) @ np.abs(L.w_r.astype(np.float64)).T
+    assert np.all(np.abs(gl - ref_logits) <= L.H * 2.0 ** -24 * xabs + 1e-30)
+
+
+def _run(g, L, sere, capped=False, tokens=None):
     D = g.DevLayer(L)
     layer = _layer(g, L, D, capped)
     y = layer.forward(D.x, sere=sere, token_w=D.token_w if capped else None)
@@ -38,17 +45,14 @@ def _run(g, L, sere, capped=False, tokens=None, max_mismatch=0):
     code, detail = layer.device_status()
     assert code == 0, (code, detail)
     ref = oracle.layer(L, sere_on=sere, capacity_on=capped, tokens=tokens)
-    # the GPU router's fp32 logits agree with the oracle's to rounding
     gl = g.host(layer.logits[:L.T])
-    xabs = np.abs(L.x.astype(np.float64)) @ np.abs(L.w_r.astype(np.float64)).T
-    assert np.all(np.abs(gl - ref["logits"]) <= L.H * 2.0 ** -24 * xabs + 1e-30)
+    _router_bound_ok(L, gl, ref["logits"])
+    # a token may route differently only where the fp32 router's rounding can
+    # reorder its ranking: adjacent logits closer than 1e-5 (the stated exclusion)
     ok = _gap(ref["logits"], (L.R if capped else L.k)) >= 1e-5
     ids = g.host((layer.out_ids if capped else layer.ids)[:L.T])
     same = np.all(ids == ref["ids"], axis=1)
-    # tokens whose routing differs must be near-ties of the fp32 router; with
-    # capacity coupling a near-tie can move a few other tokens as well
-    assert int((~same & ok).sum()) <= max_mismatch, np.nonzero(~same & ok)
-    ok &= same
+    assert np.all(same[ok]), np.nonzero(~same & ok)
     yt = g.host(y) if tokens is None else g.host(y)[tokens]
     okt = ok if tokens is None else ok[tokens]
     g.assert_y_close(yt[okt], ref["y"][okt], "layer")
@@ -77,14 +81,37 @@ def test_decode_layer_top8_vs_sere(g):
     assert int(l1.active[0].item()) == r1["perm"]["active"][0]
 
 
-def test_prefill_capacity_layer_sampled(g):
+def test_prefill_capacity_layer_full(g):
+    """The capacity prefill layer at full size (8192 tokens, R = 10, gamma =
+    1.25), every token checked.  Capacity couples tokens: one token's near-tie
+    can change which other tokens an expert admits, so the routing is checked
+    in two parts that need no exclusion at all.  (a) The GPU router's fp32
+    logits are within the fp32 dot-product bound of the oracle's.  (b) Given
+    the GPU's own logits, the oracle's ranking, admission, overflow rounds and
+    permutation equal the GPU's bit for bit, and every token's y is within
+    2e-2 * rms(y) of the oracle's."""
     L = syn.prefill()
-    toks = np.sort(np.random.default_rng(1).choice(L.T, 48, replace=False)).astype(np.int32)
-    layer, ref = _run(g, L, sere=False, capped=True, tokens=toks, max_mismatch=L.T // 1000)
-    load = g.host(layer.load_q)
-    assert (load <= ref["cap"]).all()
-    st = g.host(layer.slot_status[:L.T])
-    assert (st == 1).sum() > 0
+    D = g.DevLayer(L)
+    layer = _layer(g, L, D, capped=True)
+    y = layer.forward(D.x, token_w=D.token_w)
+    torch.cuda.synchronize()
+    code, detail = layer.device_status()
+    assert code == 0, (code, detail)
+    gl = g.host(layer.logits[:L.T])
+    _router_bound_ok(L, gl, oracle.router(L.x_bf16, L.w_r, oracle.DT_BF16))
+    ref = oracle.layer(L, sere_on=False, capacity_on=True, logits=np.ascontiguousarray(gl))
+    assert np.array_equal(g.host(layer.out_ids[:L.T]), ref["ids"])
+    assert np.array_equal(g.host(layer.out_gates[:L.T]).view(np.uint32), ref["gates"].view(np.uint32))
+    assert np.array_equal(g.host(layer.slot_status[:L.T]), ref["status"])
+    assert np.array_equal(g.host(layer.load_q), ref["load"])
+    assert int(layer.cap_q.item()) == ref["cap"]
+    p = ref["perm"]
+    m = int(p["offsets"][L.N])
+    assert np.array_equal(g.host(layer.offsets), p["offsets"])
+    assert np.array_equal(g.host(layer.row_token[:m]), p["row_token"])
+    assert (g.host(layer.load_q) <= ref["cap"]).all()
+    assert (ref["status"] == oracle.SLOT_REROUTED).sum() > 0 and (ref["status"] == oracle.SLOT_DROPPED).sum() > 0
+    g.assert_y_close(g.host(y), ref["y"], "prefill layer, all tokens")
 
 
 def test_decode_steps_replayed_from_one_graph(g):

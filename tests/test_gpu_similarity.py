@@ -75,16 +75,38 @@ def test_similarity_constructed_pairs_on_gpu(g):
     assert s[3, 4] == 0.0
 
 
-def test_similarity_full_shape_properties_and_sampled_pairs(g):
+def test_similarity_full_shape_every_pair(g):
     """The Qwen3-30B-A3B-shaped experts (128 x 2048 x 768) on 64 calibration
-    tokens: symmetry, unit diagonal, bounds, and two sampled pairs against the
-    oracle run on just those two experts."""
+    tokens, every one of the 8128 pairs against the oracle.  Sixteen experts
+    are made partners of another one (shared gate and up rows, a down
+    projection mixed with noise at 16 strengths), so that the true cosines
+    also cover the range around rho = 0.5 where SERE decides.
+
+    What the tolerance means for those decisions: the GPU's cosine is within
+    4 * 2^-7 of the oracle's, so `sim > rho` can differ from the oracle's only
+    for a pair whose exact cosine lies within that distance of rho; every
+    other pair is checked to decide alike."""
     L = syn.decode(32)
-    x = syn.f32_to_bf16_bits(np.random.default_rng(2).standard_normal((64, L.H)).astype(np.float32))
-    s = _gpu_sim(g, x, L.w_gate, L.w_up, L.w_down)
+    wg, wu, wd = (np.array(w) for w in (L.w_gate, L.w_up, L.w_down))
+    rng = np.random.default_rng(3)
+    for j in range(16):
+        a, b = 2 * j, 2 * j + 1
+        wg[b], wu[b] = wg[a], wu[a]
+        c = 0.2 * j
+        wd[b] = syn.f32_to_bf16_bits(syn.bf16_bits_to_f32(wd[a]) +
+                                     c * rng.standard_normal(wd[a].shape).astype(np.float32) * 0.02)
+    x = syn.f32_to_bf16_bits(rng.standard_normal((64, L.H)).astype(np.float32))
+    s = _gpu_sim(g, x, wg, wu, wd)
     assert np.array_equal(s, s.T) and np.all(np.diag(s) == 1.0)
     assert np.all(np.abs(s) <= 1.0 + 1e-6) and np.all(np.isfinite(s))
-    for i, j in [(3, 77), (120, 5)]:
-        sub = [np.ascontiguousarray(w[[i, j]]) for w in (L.w_gate, L.w_up, L.w_down)]
-        ref = oracle.similarity(x, *sub, oracle.DT_BF16, oracle.DT_BF16)
-        assert abs(s[i, j] - ref[0, 1]) <= TOL
+    oracle.set_threads(0)
+    ref = oracle.similarity(x, wg, wu, wd, oracle.DT_BF16, oracle.DT_BF16)
+    iu = np.triu_indices(L.N, 1)
+    err = np.abs(s[iu] - ref[iu])
+    assert err.max() <= TOL, (float(err.max()), np.unravel_index(np.argmax(np.abs(s - ref) - np.eye(L.N)), s.shape))
+    rho = 0.5
+    far = np.abs(ref[iu] - rho) > TOL
+    assert np.array_equal(s[iu][far] > rho, ref[iu][far] > rho)
+    # the constructed partners span both sides of rho
+    pair = np.array([ref[2 * j, 2 * j + 1] for j in range(16)])
+    assert (pair > rho + TOL).sum() >= 3 and (pair < rho - TOL).sum() >= 3, pair
