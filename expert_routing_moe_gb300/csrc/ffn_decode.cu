@@ -70,7 +70,7 @@ struct DcCfg {
     static constexpr int NBAR = 2 * NSTAGE + 6 + 2 * QN;
     static constexpr int MISC_INTS = 16;
     static constexpr int RT_CAP = NT * MOE_MAX_RANKS;   // every dispatch row (T <= NT, k <= 16)
-    static constexpr int LIST_INTS = 3 * MOE_MAX_EXPERTS + (MOE_MAX_EXPERTS + 1) + MOE_MAX_EXPERTS / 32;
+    static constexpr int LIST_INTS = 3 * MOE_MAX_EXPERTS + (MOE_MAX_EXPERTS + 1) + 2 * (MOE_MAX_EXPERTS / 32);
     static constexpr int XCH_BYTES = HALF ? 64 * NT * 4 : 0;
     static constexpr int SMEM = 1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + LIST_INTS * 4 +
                                 EPI_WARPS * 32 * 8 + XCH_BYTES + RT_CAP * 8;
@@ -120,10 +120,11 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
     int* s_cnt = misc + 2 + C::QN;                   // nE, nL, nA, n1, n_total, KP2, last-CTA flag
     int* elist = misc + C::MISC_INTS;                // [N] early experts, ascending
     int* llist = elist + MOE_MAX_EXPERTS;            // [N] other active experts, ascending
-    int* alist = llist + MOE_MAX_EXPERTS;            // [N] active experts (the dispatch's list)
+    int* alist = llist + MOE_MAX_EXPERTS;            // [N] active experts, in phase-2 order
     int* s_off = alist + MOE_MAX_EXPERTS;            // [N + 1] dispatch offsets
     uint32_t* ebits = reinterpret_cast<uint32_t*>(s_off + MOE_MAX_EXPERTS + 1);   // early bitmap
-    int* etok_all = reinterpret_cast<int*>(ebits + MOE_MAX_EXPERTS / 32);         // [EPI_WARPS][32]
+    uint32_t* abits = ebits + MOE_MAX_EXPERTS / 32;                                // active bitmap
+    int* etok_all = reinterpret_cast<int*>(abits + MOE_MAX_EXPERTS / 32);         // [EPI_WARPS][32]
     float* egt_all = reinterpret_cast<float*>(etok_all + C::EPI_WARPS * 32);      // [EPI_WARPS][32]
     float* xch = egt_all + C::EPI_WARPS * 32;                                      // [NT][64] half units
     int* s_rt = reinterpret_cast<int*>(xch + C::XCH_BYTES / 4);                    // [RT_CAP] row -> token
@@ -328,6 +329,26 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
             if (late) llist[nl + __popc(m & ((1u << lane) - 1u))] = e;
             nl += __popc(m);
         }
+        // Phase 2 visits the experts in the order their phase 1 was handed out:
+        // the early experts that are active, then the others.  A down
+        // projection handed out right after the first wave of phase-1 units
+        // then belongs to an expert whose activations are (nearly) published,
+        // instead of waiting for an expert whose phase 1 runs in the last wave.
+        if (lane < nw) abits[lane] = 0u;
+        __syncwarp();
+        for (int a = lane; a < na; a += 32) atomicOr(&abits[alist[a] >> 5], 1u << (alist[a] & 31));
+        __syncwarp();
+        int np = 0;
+        for (int base = 0; base < nE; base += 32) {
+            const int a = base + lane;
+            const int e = a < nE ? elist[a] : 0;
+            const bool act = a < nE && (abits[e >> 5] >> (e & 31) & 1u);
+            const unsigned m = __ballot_sync(kFull, act);
+            if (act) alist[np + __popc(m & ((1u << lane) - 1u))] = e;
+            np += __popc(m);
+        }
+        for (int a = lane; a < nl; a += 32) alist[np + a] = llist[a];
+        __syncwarp();
         if (lane == 0) {
             if (bad) report(st, MOE_DEV_BAD_INDEX, s_cnt[2]);
             const int n1 = (nE + nl) * S;
