@@ -174,17 +174,35 @@ def oracle_sample(budget_s: float, max_batches: int = 64, threads: int = 1):
     L = syn.decode(T)
     L.k_primary, L.rho = K_PRIMARY, RHO
     oracle.layer(L, sere_on=True, tokens=np.arange(1))  # load + warm the library
+    # the batches are drawn before the clock starts
+    batches = []
+    for b in range(N_BATCHES):
+        Lb = syn.decode(T, with_weights=False, token_stream_offset=b)
+        Lb.w_gate, Lb.w_up, Lb.w_down = L.w_gate, L.w_up, L.w_down
+        batches.append(Lb)
     toks, t0, nb = 0, time.perf_counter(), 0
     while nb < max_batches:
-        Lb = syn.decode(T, with_weights=False, token_stream_offset=nb)
-        Lb.w_gate, Lb.w_up, Lb.w_down = L.w_gate, L.w_up, L.w_down
-        oracle.layer(Lb, sere_on=True)
+        oracle.layer(batches[nb % N_BATCHES], sere_on=True)
         toks += T
         nb += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
     return toks / el, el, nb, nt
+
+
+def oracle_timed(Ls, budget_s: float, threads: int, sere: bool, capacity: bool = False, tokens=None):
+    """Runs oracle.layer over the layers of Ls in turn until `budget_s` is
+    used (at least one).  Returns (seconds, layers run, threads used)."""
+    import oracle
+    nt = oracle.set_threads(threads)
+    t0, n = time.perf_counter(), 0
+    while True:
+        oracle.layer(Ls[n % len(Ls)], sere_on=sere, capacity_on=capacity, tokens=tokens)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return time.perf_counter() - t0, n, nt
 
 
 def cpu_baseline_legs(budget_s: float):
@@ -743,12 +761,25 @@ def run_sweep(args):
                          "ffn_us_mean": float(np.mean(ffn)) * 1e3, "ffn_gbs": gbs, "ffn_frac": gbs / peak})
             del graphs, steps_g, layers
     clocks = clk.stop()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle layer (SERE K'=2) on whole batches of each size, all host cores and one
+        Lw = syn.sweep(32)
+        cpu = {"kind": "oracle", "unit": "tokens/s", "rows": []}
+        for B in (1, 8, 32, 64, 128):
+            Lb = syn.sweep(B, with_weights=False)
+            Lb.w_gate, Lb.w_up, Lb.w_down = Lw.w_gate, Lw.w_up, Lw.w_down
+            row = {"batch": B}
+            for key, nth in (("all_cores", 0), ("one_core", 1)):
+                el, n, nt = oracle_timed([Lb], args.cpu_budget / 5, nth, True)
+                row[key] = {"value": B * n / el, "cores": nt, "sample": "%d whole batch(es) in %.1f s" % (n, el)}
+            cpu["rows"].append(row)
     if rank == 0:
         print(json.dumps({"workload": "decode batch sweep, 16 protected experts per layer, rho=0.5",
                           "metric": "MoE-layer decode tokens/s and FFN HBM GB/s", "peak_gbs": peak,
                           "peak_source": peak_src, "steps": args.steps, "warmup": args.warmup,
                           "l2": "%d weight copies and %d token batches rotated" % (N_COPIES, N_BATCHES),
-                          "rows": rows, "clocks": clocks}), flush=True)
+                          "rows": rows, "clocks": clocks, "cpu_baseline": cpu}), flush=True)
     return 0
 
 
@@ -812,6 +843,20 @@ def run_prefill(args):
             "modality_groups": "seeded: 32 visual, 32 text, 64 shared experts"}
     flops = 2.0 * 3 * H * I * rows[0]
     ffn_s = float(np.mean(ffn)) / 1e3
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle layer: router, ranking, capacity and permutation over all 8192 tokens,
+        # FFN + combine on a 256-token sample, scaled to the whole batch
+        cpu = {"kind": "oracle", "unit": "tokens/s"}
+        smp = np.sort(np.random.default_rng(5).choice(L.T, 256, replace=False)).astype(np.int32)
+        for key, nth in (("all_cores", 0), ("one_core", 1)):
+            el_r, _, nt = oracle_timed([L], 0.0, nth, False, capacity=True, tokens=np.arange(0, dtype=np.int32))
+            el_f, _, _ = oracle_timed([L], 0.0, nth, False, capacity=True, tokens=smp)
+            est = el_r + (el_f - el_r) * L.T / len(smp)
+            cpu[key] = {"value": L.T / est, "cores": nt,
+                        "sample": "routing + capacity over all %d tokens %.2f s; FFN on %d tokens %.2f s, "
+                                  "scaled to all tokens (extrapolated): %.1f s per layer"
+                                  % (L.T, el_r, len(smp), el_f - el_r, est)}
     if rank == 0:
         print(json.dumps({"workload": "capacity-mode prefill layer: 8192 tokens (70%% visual, w~Beta(2,5)), "
                                       "hidden 2048, 128 experts, top-8, R=10, gamma=1.25, intermediate 768",
@@ -820,7 +865,7 @@ def run_prefill(args):
                           "ffn_ms": ffn_s * 1e3, "rows_admitted": rows[0], "active_experts": us[0],
                           "ffn_tflops": flops / ffn_s / 1e12, "peak_tflops": tf,
                           "ffn_frac": flops / ffn_s / 1e12 / tf, "steps": steps, "clocks": clocks,
-                          "macs_entropy_weights_and_expert_capacity": macs}), flush=True)
+                          "macs_entropy_weights_and_expert_capacity": macs, "cpu_baseline": cpu}), flush=True)
     return 0
 
 
@@ -942,6 +987,29 @@ def run_stack(args):
                      "steps": steps, "clocks": clocks}
         del g
     peak, peak_src = load_peaks()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle on 4 sampled layers of the step (SERE K'=2, batch 64; one host weight
+        # set, as the oracle's time does not depend on the values), scaled to all layers
+        import oracle
+        Lw = syn.decode(B)
+        Ls = []
+        for l in range(4):
+            Ll = syn.decode(B, layer=l, with_weights=False)
+            Ll.w_gate, Ll.w_up, Ll.w_down = Lw.w_gate, Lw.w_up, Lw.w_down
+            Ll.sim, Ll.protect = syn.stack_sim(l), syn.stack_protect(l)
+            Ls.append(Ll)
+        cpu = {"kind": "oracle", "unit": "tokens/s"}
+        for key, nth in (("all_cores", 0), ("one_core", 1)):
+            nt = oracle.set_threads(nth)
+            t0 = time.perf_counter()
+            for Ll in Ls:
+                oracle.layer(Ll, sere_on=True)
+            el = time.perf_counter() - t0
+            per_step = el / len(Ls) * nl
+            cpu[key] = {"value": B / per_step, "cores": nt,
+                        "sample": "%d sampled layers in %.1f s, scaled to %d layers (extrapolated): %.1f s per step"
+                                  % (len(Ls), el, nl, per_step)}
     if rank == 0:
         print(json.dumps({"workload": "decode step over %d MoE layers, batch %d, hidden 2048, 128 experts, top-8, "
                                       "intermediate 768, %.1f GB of bf16 experts resident; SERE K'=2 and K'=1 at "
@@ -949,7 +1017,7 @@ def run_stack(args):
                                       "plain top-2" % (nl, B, nl * N * EXPERT_BYTES / 1e9),
                           "metric": "decode step tokens/s (one CUDA graph per step)", "peak_gbs": peak,
                           "peak_source": peak_src, "residual": "x_{l+1} = x_l + y_l in fp32 (the FFN accumulates into it), rounded to bf16 per layer by moe_residual_to_bf16",
-                          **res}), flush=True)
+                          "cpu_baseline": cpu, **res}), flush=True)
     return 0
 
 

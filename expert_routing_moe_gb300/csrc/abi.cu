@@ -238,7 +238,11 @@ moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const u
     if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
     if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
     if (!(eps > 0.f) || !(delta == delta) || delta - delta != 0.f) return MOE_ERR_INVALID_ARG;   // eps > 0, delta finite
-    if (T == 0) return MOE_OK;
+    if (T > (1 << 24)) return MOE_ERR_UNSUPPORTED;   // the fixed-point sums are sized for 2^24 tokens
+    if (T == 0) {
+        if (r_v == nullptr) return MOE_OK;
+        return from_cuda(cudaMemsetAsync(r_v, 0, sizeof(float), as_stream(stream)));
+    }
     if (x == nullptr || is_visual == nullptr || entropy == nullptr || token_w == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x)) return MOE_ERR_INVALID_ARG;
     if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;

@@ -11,17 +11,19 @@
 // Kernel 1: one warp per token, H = ln Z - (sum e_d (z_d - m)) / Z with
 // m = max z and e_d = exp(z_d - m) (CUDA's fast exponential intrinsic: its
 // error is far below the entropy's fp32 summation error), fixed lane order and
-// xor butterfly.  Rows
-// of up to 2048 features are read once, into registers, and both passes run
-// from there.  Kernel 1 also leaves per-CTA partials (count, sum, sum of
-// squares of the visual entropies, in double, in a fixed order) in the
-// workspace.
-// Kernel 2: one thread per token over ceil(T / 256) CTAs.  Every CTA reduces
-// the kernel-1 partials itself, in the same fixed order, so all CTAs hold
-// bit-identical statistics; each evaluates its tokens' sigmoids in fp32 and
-// leaves its (visual, total) weight sums in double.  The last CTA to finish
-// (a ticket counter that kernel 1 clears) sums those in CTA order for R_v, so
-// the results are reproducible bit for bit.
+// xor butterfly.  A row of up to 2048 features is read once into registers
+// (bf16 rows stay packed, 32 registers a lane) and both passes run from
+// there.  Each CTA leaves the count, sum and sum of squares of its visual
+// tokens' entropies as 64-bit fixed-point integers (2^-32 and 2^-24 units).
+// Kernel 2: one thread per token over ceil(T / 256) CTAs.  Every CTA adds up
+// the kernel-1 partials itself; integer sums do not depend on their order,
+// so every CTA holds the same statistics, converted to mean and 1/(sigma +
+// eps) in double by one thread.  Each thread evaluates its token's sigmoid in
+// fp32; the CTA's (visual, total) weight sums are again fixed-point integers
+// (2^-32 units), which the last CTA to finish (a ticket that kernel 1
+// clears) adds up for R_v.  So the results are reproducible bit for bit,
+// and double precision -- slow on this part -- is used for a few scalar
+// operations only.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -44,14 +46,28 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// Per-CTA partial statistics of the visual tokens' entropies (count, sum,
-// sum of squares), in double, summed by thread 0 over its 8 tokens in order.
+// Per-CTA partial statistics of the visual tokens' entropies: count, sum
+// (2^-32 units) and sum of squares (2^-24 units) as integers.  Entropies lie
+// in [0, ln D], so with T <= 2^24 tokens neither sum can overflow.
 struct EntPart {
-    double n, s, s2;
+    long long n, s1, s2;
 };
+constexpr float kEntScale1 = 4294967296.0f;   // 2^32
+constexpr float kEntScale2 = 16777216.0f;     // 2^24
+constexpr float kWScale = 4294967296.0f;      // 2^32, weights in [0, 1]
+
+// h*h in 2^-24 units, from its exact two-term fp32 split (hi + lo = h*h).
+__device__ __forceinline__ long long sq_fixed(float h) {
+    const float hi = h * h;
+    const float lo = fmaf(h, h, -hi);
+    return __float2ll_rn(hi * kEntScale2) + __float2ll_rn(lo * kEntScale2);
+}
 
 // Chunks of 8 features per lane that a register-cached row holds (H <= 2048).
 constexpr int kEntRegChunks = 8;
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
 // Max, then sum of e and e * (z - m), over one lane's chunks of a row.
 template <typename XT, bool CACHED>
@@ -59,7 +75,45 @@ __device__ __forceinline__ void entropy_lane_sums(const XT* row, int H, int lane
                                                   bool& finite) {
     m = -INFINITY;
     finite = true;
-    if constexpr (CACHED) {
+    if constexpr (CACHED && sizeof(XT) == 2) {
+        // bf16 row kept packed: 8 x 16 bytes per lane, unpacked in each pass
+        uint4 q[kEntRegChunks];
+#pragma unroll
+        for (int c = 0; c < kEntRegChunks; ++c) {
+            const int h = lane * 8 + c * 256;
+            q[c] = (h < H) ? *reinterpret_cast<const uint4*>(row + h) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int c = 0; c < kEntRegChunks; ++c) {
+            if (lane * 8 + c * 256 < H) {
+                const uint32_t u[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = bf_lo(u[j]), b = bf_hi(u[j]);
+                    finite &= isfinite(a) && isfinite(b);
+                    m = fmaxf(m, fmaxf(a, b));
+                }
+            }
+        }
+        for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+        Z = 0.f;
+        S1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < kEntRegChunks; ++c) {
+            if (lane * 8 + c * 256 < H) {
+                const uint32_t u[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float d0 = bf_lo(u[j]) - m, d1 = bf_hi(u[j]) - m;
+                    const float e0 = __expf(d0), e1 = __expf(d1);
+                    Z += e0;
+                    S1 = fmaf(e0, d0, S1);
+                    Z += e1;
+                    S1 = fmaf(e1, d1, S1);
+                }
+            }
+        }
+    } else if constexpr (CACHED) {
         float v[kEntRegChunks][8];
 #pragma unroll
         for (int c = 0; c < kEntRegChunks; ++c) {
@@ -123,10 +177,37 @@ __device__ __forceinline__ void entropy_lane_sums(const XT* row, int H, int lane
     }
 }
 
-// Sums of the weights of one CTA of kernel 2 (visual, all), in double.
+// Sums of the weights of one CTA of kernel 2 (visual, all), 2^-32 units.
 struct WPart {
-    double wv, wall;
+    long long wv, wall;
 };
+
+// Sum of NV int64 values over the block (any order gives the same result);
+// every thread gets the totals.  red: [NV][33].
+template <int NV>
+__device__ __forceinline__ void block_sum_i64(long long (&v)[NV], long long (*red)[33]) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        for (int off = 16; off >= 1; off >>= 1) v[i] += __shfl_xor_sync(kFull, v[i], off);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) red[i][threadIdx.x >> 5] = v[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int nw = static_cast<int>(blockDim.x >> 5);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            long long t = static_cast<int>(threadIdx.x) < nw ? red[i][threadIdx.x] : 0;
+            for (int off = 16; off >= 1; off >>= 1) t += __shfl_xor_sync(kFull, t, off);
+            if (threadIdx.x == 0) red[i][32] = t;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = red[i][32];
+}
 
 template <typename XT, bool CACHED>
 __global__ void __launch_bounds__(256) token_entropy_kernel(const XT* __restrict__ x, int T, int H,
@@ -158,46 +239,19 @@ __global__ void __launch_bounds__(256) token_entropy_kernel(const XT* __restrict
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        EntPart p{0.0, 0.0, 0.0};
-        for (int w = 0; w < 8; ++w) {
-            const int tw = blockIdx.x * 8 + w;
-            if (tw < T && is_visual[tw]) {
-                const double h = static_cast<double>(s_h[w]);
-                p.n += 1.0;
-                p.s += h;
-                p.s2 += h * h;
-            }
+    if (warp == 0) {
+        // lanes 0..7: this CTA's tokens as fixed-point terms, summed with integer shuffles
+        const int tw = blockIdx.x * 8 + lane;
+        const bool v = lane < 8 && tw < T && is_visual[tw] != 0;
+        const float h = v ? s_h[lane] : 0.f;
+        long long n = v ? 1 : 0, q1 = v ? __float2ll_rn(h * kEntScale1) : 0, q2 = v ? sq_fixed(h) : 0;
+        for (int off = 4; off >= 1; off >>= 1) {
+            n += __shfl_xor_sync(kFull, n, off);
+            q1 += __shfl_xor_sync(kFull, q1, off);
+            q2 += __shfl_xor_sync(kFull, q2, off);
         }
-        parts[blockIdx.x] = p;
+        if (lane == 0) parts[blockIdx.x] = EntPart{n, q1, q2};
     }
-}
-
-// Sums of NV values over the block in double, fixed order: warp butterfly,
-// then thread 0 adds the warp sums in order and broadcasts (one thread doing
-// the few adds: fp64 throughput on one SM is small).  red: [NV][33].
-template <int NV>
-__device__ __forceinline__ void block_sum_f64(double (&v)[NV], double (*red)[33]) {
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-        for (int off = 16; off >= 1; off >>= 1) v[i] += __shfl_xor_sync(kFull, v[i], off);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) {
-#pragma unroll
-        for (int i = 0; i < NV; ++i) red[i][threadIdx.x >> 5] = v[i];
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            double t = 0.0;
-            for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[i][w];
-            red[i][32] = t;
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = red[i][32];
 }
 
 __global__ void __launch_bounds__(256) token_weights_kernel(const float* __restrict__ entropy,
@@ -206,7 +260,8 @@ __global__ void __launch_bounds__(256) token_weights_kernel(const float* __restr
                                                             float delta, float eps, float* __restrict__ token_w,
                                                             WPart* __restrict__ wparts, int* __restrict__ ticket,
                                                             float* __restrict__ r_v) {
-    __shared__ double red[3][33];
+    __shared__ long long red[3][33];
+    __shared__ float s_mu, s_inv;
     __shared__ bool s_last;
     pdl_wait();
     pdl_trigger();
@@ -214,24 +269,23 @@ __global__ void __launch_bounds__(256) token_weights_kernel(const float* __restr
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     const bool vis_t = t < T && is_visual[t] != 0;
     const float ent_t = vis_t ? entropy[t] : 0.f;
-    double st3[3] = {0.0, 0.0, 0.0};   // count, sum, sum of squares
+    long long st3[3] = {0, 0, 0};   // count, sum, sum of squares (fixed point)
     for (int i = threadIdx.x; i < nparts; i += blockDim.x) {
         const EntPart p = parts[i];
         st3[0] += p.n;
-        st3[1] += p.s;
+        st3[1] += p.s1;
         st3[2] += p.s2;
     }
-    block_sum_f64<3>(st3, red);
-    // population statistics, by one thread (a double division or square
-    // root is tens of fp64 operations, and fp64 throughput per SM is small);
-    // the one-pass variance in double is exact to far below the fp32
-    // entropies' own rounding at these magnitudes (|H| <= ln D)
-    __shared__ float s_mu, s_inv;
+    block_sum_i64<3>(st3, red);
+    // population statistics by one thread: a double division or square root
+    // is tens of fp64 operations, and fp64 throughput per SM is small.  The
+    // one-pass variance is exact to far below the fp32 entropies' rounding:
+    // the sums are exact integers and double keeps 53 bits of each quotient.
     if (threadIdx.x == 0) {
-        const double nv = st3[0], s = st3[1], s2 = st3[2];
-        const double mu = nv > 0.0 ? s / nv : 0.0;
-        const double sigma = nv > 0.0 ? sqrt(fmax(s2 / nv - mu * mu, 0.0)) : 0.0;
-        // the z-score's scale once in double; each token's sigmoid in fp32
+        const double nv = static_cast<double>(st3[0]);
+        const double mu = nv > 0.0 ? static_cast<double>(st3[1]) / (nv * 4294967296.0) : 0.0;
+        const double m2 = nv > 0.0 ? static_cast<double>(st3[2]) / (nv * 16777216.0) : 0.0;
+        const double sigma = sqrt(fmax(m2 - mu * mu, 0.0));
         s_inv = static_cast<float>(1.0 / (sigma + static_cast<double>(eps)));
         s_mu = static_cast<float>(mu);
     }
@@ -248,8 +302,8 @@ __global__ void __launch_bounds__(256) token_weights_kernel(const float* __restr
         token_w[t] = w;
     }
     if (r_v == nullptr) return;   // uniform over the grid
-    double ws2[2] = {static_cast<double>(wv), static_cast<double>(w)};
-    block_sum_f64<2>(ws2, red);
+    long long ws2[2] = {__float2ll_rn(wv * kWScale), __float2ll_rn(w * kWScale)};
+    block_sum_i64<2>(ws2, red);
     if (threadIdx.x == 0) {
         wparts[blockIdx.x] = WPart{ws2[0], ws2[1]};
         __threadfence();
@@ -258,15 +312,14 @@ __global__ void __launch_bounds__(256) token_weights_kernel(const float* __restr
     __syncthreads();
     if (!s_last) return;   // uniform over the block
     __threadfence();
-    double tot[2] = {0.0, 0.0};
+    long long tot[2] = {0, 0};
     for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x) {
         tot[0] += __ldcg(&wparts[i].wv);
         tot[1] += __ldcg(&wparts[i].wall);
     }
-    block_sum_f64<2>(tot, red);
+    block_sum_i64<2>(tot, red);
     if (threadIdx.x == 0) {
-        const double av = tot[0], aa = tot[1];
-        *r_v = static_cast<float>(aa > 0.0 ? av / aa : 0.0);
+        *r_v = static_cast<float>(tot[1] > 0 ? static_cast<double>(tot[0]) / static_cast<double>(tot[1]) : 0.0);
         *ticket = 0;
     }
 }

@@ -382,9 +382,13 @@ moe_status_t moe_similarity_calibrate(const void* x, int n, const void* w_gate, 
  *              initial contents needed
  * Entropies and weights are computed in fp32 (one warp per token for the
  * entropy); the statistics (count, sum and sum of squares of the visual
- * entropies, population variance) and R_v are summed in double, in a fixed
- * order, so results are reproducible bit for bit.  Two calls must not share
- * a workspace concurrently (it holds a completion counter).
+ * entropies, population variance) and the two weight sums of R_v are added
+ * up as 64-bit fixed-point integers (entropy in 2^-32, its square in 2^-24,
+ * weights in 2^-32 units), so results do not depend on summation order and
+ * are reproducible bit for bit; mean, variance and R_v are then formed in
+ * double.  T is at most 2^24 (MOE_ERR_UNSUPPORTED beyond), which keeps those
+ * sums in range.  Two calls must not share a workspace concurrently (it
+ * holds a completion counter).
  * A non-finite feature sets MOE_DEV_NONFINITE (detail = token) in st.
  */
 moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,

@@ -204,6 +204,8 @@ def test_token_weights_rejects(lib):
     assert f(FAKE, 1, 4, 64, None, 1.0, 1e-6, FAKE, FAKE, None, *W, None, None) == -1    # no is_visual
     assert f(FAKE, 1, 4, 64, FAKE, 1.0, 1e-6, FAKE, FAKE, None, FAKE, 0, None, None) == -4   # no workspace
     assert f(None, 1, 0, 64, None, 1.0, 1e-6, None, None, None, None, 0, None, None) == 0    # empty batch
+    big = (1 << 24) + 1                                                                       # fixed-point range
+    assert f(FAKE, 1, big, 64, FAKE, 1.0, 1e-6, FAKE, FAKE, None, *W, None, None) == -2
 
 
 def test_similarity_calibrate_rejects(lib):

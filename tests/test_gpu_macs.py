@@ -163,3 +163,15 @@ def test_per_expert_capacity_from_visual_ratio(g):
     assert (g.host(load_q) <= Ce).all()
     # a visual-leaning batch (R_v > 1/2) gives visual experts more room than text experts
     assert (r_h > 0.5) == (Ce[bias == 1].min() > Ce[bias == -1].max())
+
+
+def test_token_weights_empty_batch_clears_rv(g):
+    """An empty batch launches nothing but still reports R_v = 0."""
+    rv = torch.full((1,), 7.0, dtype=torch.float32, device=g.DEV)
+    e = torch.empty(0, dtype=torch.float32, device=g.DEV)
+    st = g.status_tensor()
+    moe.moe_token_weights(torch.empty(0, 64, dtype=torch.bfloat16, device=g.DEV),
+                          torch.empty(0, dtype=torch.uint8, device=g.DEV), e, e, rv, 1.0, 1e-6, st)
+    torch.cuda.synchronize()
+    g.assert_status_ok(st)
+    assert float(rv.item()) == 0.0
