@@ -118,7 +118,8 @@ moe_status_t moe_decode_layer(const void* x, const float* w_router, const void* 
     cudaStream_t s = as_stream(stream);
     cudaError_t e = moe::launch_route_dispatch(x, MOE_DTYPE_BF16, w_router, T, H, N, k,
                                                (route_flags & MOE_ROUTE_RENORM_TOPK) != 0, logits, ids, gates, sere,
-                                               counts, offsets, row_token, row_gate, active, route_ws, true, st, s);
+                                               counts, offsets, row_token, row_gate, active, route_ws, true, st, s,
+                                               moe::ffn_decode_one_wave_experts(T, I, N, k));
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const uint32_t* early = static_cast<const uint32_t*>(route_ws) + moe::kRouteDispatchEarlyWord;
     return from_cuda(moe::launch_ffn_decode(x, w_gate, w_up, w_down, T, H, I, N, k, offsets, row_token, row_gate,

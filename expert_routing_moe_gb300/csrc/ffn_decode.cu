@@ -745,6 +745,18 @@ static cudaError_t run_decode(const void* x, const void* wg, const void* wu, con
                       counters, out, y_zero, T, H, I, N, k, fuse ? 1 : 0, st);
 }
 
+static bool decode_half_units(int T, int I, int N, int k) {
+    return ffn_decode_nt(T) == 16 && static_cast<long long>(N < T * k ? N : T * k) * (I / 128) < sm_count();
+}
+
+int ffn_decode_units_per_expert(int T, int I, int N, int k) {
+    return decode_half_units(T, I, N, k) ? I / 64 : I / 128;
+}
+
+int ffn_decode_one_wave_experts(int T, int I, int N, int k) {
+    return sm_count() / ffn_decode_units_per_expert(T, I, N, k);
+}
+
 cudaError_t launch_ffn_decode(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
                               int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                               const int32_t* active, const uint32_t* early, uint32_t flags, float* out, void* ws,

@@ -48,10 +48,16 @@ constexpr int kRouteDispatchWs = 512;
 // the decode FFN: a flag, then the bitmap (SERE's primary union P, else the
 // union of all ranked experts), written as soon as ranking ends
 constexpr int kRouteDispatchEarlyWord = 96;
+// spec_union_max > 0 (with SERE and publish_early): when the batch's ranked
+// union has at most that many experts, the first set published is the whole
+// union instead of P, so the decode FFN streams every candidate's phase 1
+// at once (its SMs would otherwise idle); experts that then move lose only
+// their phase 1
 cudaError_t launch_route_dispatch(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int k,
                                   bool renorm, float* logits, int32_t* ids, float* gates, const moe_sere_params* sere,
                                   int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,
-                                  int32_t* active, void* ws, bool publish_early, moe_dev_status* st, cudaStream_t s);
+                                  int32_t* active, void* ws, bool publish_early, moe_dev_status* st, cudaStream_t s,
+                                  int spec_union_max = 0);
 
 // ---- dispatch (dispatch.cu) ----
 size_t dispatch_workspace(int T, int N, int k, int R, bool capped);
@@ -73,6 +79,11 @@ inline int ffn_decode_nt(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
 // region at the start of the workspace; the activations follow
 inline size_t ffn_decode_ctr_bytes() { return 2304; }
 long long ffn_decode_act_rows(int T, int N);
+// phase-1 units per expert the decode kernel runs for this shape (I/128, or
+// I/64 when it takes half units)
+int ffn_decode_units_per_expert(int T, int I, int N, int k);
+// the most experts whose phase-1 units all fit one wave of the SMs
+int ffn_decode_one_wave_experts(int T, int I, int N, int k);
 // early: the routing launch's published early experts ([0] flag, then a
 // bitmap), or nullptr to wait for the preceding launch at the start
 cudaError_t launch_ffn_decode(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,

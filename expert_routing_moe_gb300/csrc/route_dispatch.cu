@@ -51,7 +51,7 @@ static_assert(kWsGroups + kRouteDispatchMaxT / 4 <= kWsEarly, "workspace words")
 static_assert(kWsEarly + 1 + kMaxPerLane <= kRouteDispatchWs / 4, "workspace words");
 
 struct RdArgs {
-    int T, H, N, k, kp, renorm, stage_sim, publish;
+    int T, H, N, k, kp, renorm, stage_sim, publish, spec_max;
     float rho;
     const float* sim;
     const uint8_t* protect;
@@ -246,8 +246,14 @@ __device__ __forceinline__ void batch_tail(const RdArgs& a, float* s_sim, uint64
     if (a.publish && threadIdx.x == 0) {
         // the experts the decode FFN may start on now: SERE never takes a
         // primary away, so P is active whatever the reroute does; without
-        // SERE the union of the ranked experts is the active set
-        for (int w = 0; w < kMaxPerLane; ++w) ws[kWsEarly + 1 + w] = SERE ? Pbits[w] : Ubefore[w];
+        // SERE the union of the ranked experts is the active set.  A SERE
+        // union small enough for one wave of the FFN's phase-1 units is
+        // published whole: SMs that would idle stream every candidate, and an
+        // expert that then moves costs only its phase 1.
+        int nu = 0;
+        for (int w = 0; w < kMaxPerLane; ++w) nu += __popc(Ubefore[w]);
+        const bool whole = !SERE || nu <= a.spec_max;
+        for (int w = 0; w < kMaxPerLane; ++w) ws[kWsEarly + 1 + w] = whole ? Ubefore[w] : Pbits[w];
         st_release_gpu(reinterpret_cast<int*>(ws) + kWsEarly, 1);
     }
     // bit t of expert e's presence bitmap marks token t holding e (a token
@@ -467,9 +473,10 @@ cudaError_t launch_route_dispatch(const void* x, int x_dtype, const float* w_rou
                                   bool renorm, float* logits, int32_t* ids, float* gates, const moe_sere_params* sere,
                                   int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,
                                   int32_t* active, void* ws, bool publish_early, moe_dev_status* st,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, int spec_union_max) {
     RdArgs a{};
     a.publish = publish_early ? 1 : 0;
+    a.spec_max = spec_union_max;
     a.T = T;
     a.H = H;
     a.N = N;

@@ -206,8 +206,31 @@ def test_token_major_prefill_shape_sampled(g, qwen):
     Lt = syn.prefill(with_weights=False)
     x_dev = g.dev(Lt.x_bf16, torch.bfloat16)
     ids, gates = _route(L, Lt.x_bf16, Lt.T)
-    tokens = np.arange(0, Lt.T, 337, dtype=np.int32)
+    tokens = np.sort(np.random.default_rng(11).choice(Lt.T, 1024, replace=False)).astype(np.int32)
+    oracle.set_threads(0)
     _ffn_case(g, L, D, Lt.x_bf16, x_dev, ids, gates, tokens)
+
+
+@pytest.mark.parametrize("fuse", [True, False])
+def test_token_major_shared_workspace_and_empty_dispatch(g, fuse):
+    """Three token-major calls on one workspace (zeroed once): a normal batch,
+    a batch whose every slot is empty (no units at all: y must still be
+    written, as zeros), the normal batch again; each matches the oracle."""
+    L = syn.qwen_layer(1100, H=512, N=8, k=2, I=256)
+    D = g.DevLayer(L)
+    ids, gates = _skewed_ids(np.random.default_rng(5), 1100, 8, 2)
+    empty_ids = np.full_like(ids, -1)
+    empty_gates = np.zeros_like(gates)
+    ws = g.ffn_workspace(D.x, D.w_gate, L.k, L.T)
+    for ii, gg in ((ids, gates), (empty_ids, empty_gates), (ids, gates)):
+        d = g.gpu_dispatch(g.dev(ii), g.dev(gg), L.N, L.k, L.k)
+        y = g.gpu_ffn(D.x, D.w_gate, D.w_up, D.w_down, L.k, d["dev"], L.T, fuse=fuse, ws=ws)
+        if (ii < 0).all():
+            assert np.all(y == 0.0)
+        else:
+            yref = oracle.ffn_combine(L.x_bf16, L.w_gate, L.w_up, L.w_down, ii, gg, L.k, None, oracle.DT_BF16,
+                                      oracle.DT_BF16)
+            g.assert_y_close(y, yref, "token-major shared workspace fuse=%d" % fuse)
 
 
 def test_dependency_wait_times_out_cleanly(g, qwen):
