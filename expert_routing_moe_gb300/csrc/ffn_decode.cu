@@ -745,6 +745,8 @@ static cudaError_t run_decode(const void* x, const void* wg, const void* wu, con
                       counters, out, y_zero, T, H, I, N, k, fuse ? 1 : 0, st);
 }
 
+// half phase-1 units when even min(N, T*k) active experts give fewer whole
+// 128-row I-slices than SMs
 static bool decode_half_units(int T, int I, int N, int k) {
     return ffn_decode_nt(T) == 16 && static_cast<long long>(N < T * k ? N : T * k) * (I / 128) < sm_count();
 }
@@ -764,9 +766,7 @@ cudaError_t launch_ffn_decode(const void* x, const void* wg, const void* wu, con
     if (T < 1 || T > kDecodeMaxT || k > MOE_MAX_RANKS || N > MOE_MAX_EXPERTS) return cudaErrorInvalidValue;
     switch (ffn_decode_nt(T)) {
         case 16:
-            // half phase-1 units when even min(N, T*k) active experts give
-            // fewer whole 128-row I-slices than SMs
-            if (static_cast<long long>(N < T * k ? N : T * k) * (I / 128) < sm_count())
+            if (decode_half_units(T, I, N, k))
                 return run_decode<16, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
                                             flags, out, ws, st, s);
             return run_decode<16, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
