@@ -37,7 +37,7 @@ def _gpu_weights(g, x_dev, vis, delta=1.0, eps=1e-6):
 
 
 @pytest.mark.parametrize("T,H,dtype,delta", [(8192, 2048, "bf16", 1.0), (300, 256, "f32", 2.5),
-                                             (37, 128, "bf16", 0.5)])
+                                             (37, 128, "bf16", 0.5), (20000, 256, "bf16", 1.5)])
 def test_token_weights_match_oracle(g, T, H, dtype, delta):
     if H == 2048:
         L = syn.prefill(T, with_weights=False)
@@ -175,3 +175,29 @@ def test_token_weights_empty_batch_clears_rv(g):
     torch.cuda.synchronize()
     g.assert_status_ok(st)
     assert float(rv.item()) == 0.0
+
+
+def test_token_weights_one_workspace_across_sizes(g):
+    """One workspace serves calls of different batch sizes in any order: each
+    call matches a call on a fresh workspace bit for bit (the completion
+    counter is cleared by every call)."""
+    from expert_routing_moe_gb300 import _abi as abi
+    rng = np.random.default_rng(11)
+    ws = torch.zeros(abi.workspace_size(abi.MOE_OP_TOKEN_WEIGHTS, 20000, 1, 1, 1, 1, 1, False, 0),
+                     dtype=torch.uint8, device=g.DEV)
+    for T in (2000, 20000, 2000, 37, 20000):
+        x = syn.f32_to_bf16_bits((rng.standard_normal((T, 256)) * rng.uniform(0.2, 4.0, size=(T, 1))).astype(np.float32))
+        vis = (rng.random(T) < 0.6).astype(np.uint8)
+        x_dev, v_dev = g.dev(x, torch.bfloat16), g.dev(vis)
+        outs = []
+        for w_s in (ws, None):
+            ent = torch.empty(T, dtype=torch.float32, device=g.DEV)
+            w = torch.empty(T, dtype=torch.float32, device=g.DEV)
+            rv = torch.empty(1, dtype=torch.float32, device=g.DEV)
+            st = g.status_tensor()
+            moe.moe_token_weights(x_dev, v_dev, ent, w, rv, 1.0, 1e-6, st, workspace=w_s)
+            torch.cuda.synchronize()
+            g.assert_status_ok(st)
+            outs.append((g.host(ent), g.host(w), float(rv.item())))
+        assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+        assert outs[0][2] == outs[1][2]
