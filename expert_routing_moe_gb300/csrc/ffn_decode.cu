@@ -746,9 +746,12 @@ static cudaError_t run_decode(const void* x, const void* wg, const void* wu, con
 }
 
 // half phase-1 units when even min(N, T*k) active experts give fewer whole
-// 128-row I-slices than SMs
+// 128-row I-slices than SMs, and for batches of up to 8 tokens, whose few
+// dozen active experts fill barely one wave of whole slices: twice the units
+// let the work counter even out SMs that stream at different rates
 static bool decode_half_units(int T, int I, int N, int k) {
-    return ffn_decode_nt(T) == 16 && static_cast<long long>(N < T * k ? N : T * k) * (I / 128) < sm_count();
+    return ffn_decode_nt(T) == 16 &&
+           (T <= 8 || static_cast<long long>(N < T * k ? N : T * k) * (I / 128) < sm_count());
 }
 
 int ffn_decode_units_per_expert(int T, int I, int N, int k) {
