@@ -728,7 +728,8 @@ def run_ours(args):
 # ---------------------------------------------------------------------------
 def run_sweep(args):
     """Decode batch sweep with 16 protected experts: top-8 and SERE K'=1, 2 at
-    rho = 0.5, batch in {1, 8, 32, 64, 128}; per-layer time, union, FFN GB/s."""
+    rho = 0.5, batch in --batches (default 1, 8, 32, 64, 128); per-layer time,
+    union, FFN GB/s."""
     torch, moe, dev, ws, rank, local = _gpu_setup()
     from expert_routing_moe_gb300 import synthetic as syn
     peak, peak_src = load_peaks()
@@ -738,7 +739,7 @@ def run_sweep(args):
     copies = _device_copies(torch, dev, L0, N_COPIES, 1000 * syn.CONFIG_SWEEP + 10 * (rank + 1))
     clk = ClockSampler(local if ws > 1 else 0)
     clk.start()
-    for B in (1, 8, 32, 64, 128):
+    for B in args.batches:
         Lb0 = syn.sweep(B, with_weights=False)
         w_r = torch.from_numpy(Lb0.w_r).to(dev)
         sim = torch.from_numpy(Lb0.sim).to(dev)
@@ -766,7 +767,7 @@ def run_sweep(args):
         # the oracle layer (SERE K'=2) on whole batches of each size, all host cores and one
         Lw = syn.sweep(32)
         cpu = {"kind": "oracle", "unit": "tokens/s", "rows": []}
-        for B in (1, 8, 32, 64, 128):
+        for B in args.batches:
             Lb = syn.sweep(B, with_weights=False)
             Lb.w_gate, Lb.w_up, Lb.w_down = Lw.w_gate, Lw.w_up, Lw.w_down
             row = {"batch": B}
@@ -1036,6 +1037,8 @@ def main():
                     help="decode (the headline line) or one of the further workloads")
     ap.add_argument("--layers", type=int, default=48, help="layers of the stack workload")
     ap.add_argument("--passes", type=int, default=5, help="timed passes of --steps steps (median reported)")
+    ap.add_argument("--batches", type=lambda v: [int(b) for b in v.split(",")], default=[1, 8, 32, 64, 128],
+                    help="comma-separated decode batches of the sweep workload (each 1..128)")
     args = ap.parse_args()
     global N_COPIES
     N_COPIES = max(1, args.copies)

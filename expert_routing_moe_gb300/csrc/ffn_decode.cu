@@ -19,7 +19,8 @@
 //    and counts its units in done[e]; nothing in phase 1 depends on the
 //    routing beyond the expert id.
 //  * Early start.  When the routing launch publishes its early experts (the
-//    primary union P of SERE, or the whole union for plain top-k) as soon as
+//    primary union P of SERE, the whole union before the reroute when its
+//    phase-1 units fit one wave, or the union for plain top-k) as soon as
 //    ranking ends, the kernel streams those experts' phase 1 while the
 //    routing launch still reroutes and permutes; only the remaining experts'
 //    phase 1 and the down projections wait for the final routing, which a
@@ -32,7 +33,7 @@
 //                      W_down (and per K half when small batches leave SMs
 //                      idle): gate * W_down A^T added into y.
 // A phase-1 unit is one 128-row I-slice of W_gate and W_up over K = H (or,
-// for batches of at most 3 tokens, a half unit: 64 gate and 64 up rows
+// for batches of at most 16 tokens, a half unit: 64 gate and 64 up rows
 // stacked as one 128-row operand); a phase-2 unit waits (bounded, acquire)
 // until its expert's S phase-1 units have published A.  The warp roles and
 // TMEM accumulators are those of the weight-major kernel in ffn.cu.
@@ -745,17 +746,14 @@ static cudaError_t run_decode(const void* x, const void* wg, const void* wu, con
                       counters, out, y_zero, T, H, I, N, k, fuse ? 1 : 0, st);
 }
 
-// half phase-1 units when even min(N, T*k) active experts give fewer whole
-// 128-row I-slices than SMs, and for batches of up to 8 tokens, whose few
-// dozen active experts fill barely one wave of whole slices: twice the units
-// let the work counter even out SMs that stream at different rates
-static bool decode_half_units(int T, int I, int N, int k) {
-    return ffn_decode_nt(T) == 16 &&
-           (T <= 8 || static_cast<long long>(N < T * k ? N : T * k) * (I / 128) < sm_count());
-}
+// half phase-1 units for batches of up to 16 tokens: their few dozen active
+// experts give at most a wave or two of whole 128-row I-slices (fewer than
+// the SMs when T*k or N is small), and twice the units let the work counter
+// even out SMs that stream at different rates
+static bool decode_half_units(int T) { return ffn_decode_nt(T) == 16; }
 
 int ffn_decode_units_per_expert(int T, int I, int N, int k) {
-    return decode_half_units(T, I, N, k) ? I / 64 : I / 128;
+    return decode_half_units(T) ? I / 64 : I / 128;
 }
 
 int ffn_decode_one_wave_experts(int T, int I, int N, int k) {
@@ -769,11 +767,8 @@ cudaError_t launch_ffn_decode(const void* x, const void* wg, const void* wu, con
     if (T < 1 || T > kDecodeMaxT || k > MOE_MAX_RANKS || N > MOE_MAX_EXPERTS) return cudaErrorInvalidValue;
     switch (ffn_decode_nt(T)) {
         case 16:
-            if (decode_half_units(T, I, N, k))
-                return run_decode<16, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
-                                            flags, out, ws, st, s);
-            return run_decode<16, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
-                                         flags, out, ws, st, s);
+            return run_decode<16, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
+                                        flags, out, ws, st, s);
         case 32:
             return run_decode<32, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
                                          flags, out, ws, st, s);

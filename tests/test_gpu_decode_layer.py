@@ -1,6 +1,7 @@
-"""GPU parity of the one-call decode layer (moe_decode_layer): the routing
-launch publishes the experts certain to be active as soon as ranking ends
-and the FFN starts on them while routing finishes.  Its routing outputs must
+"""GPU parity of the one-call decode layer (moe_decode_layer): as soon as
+ranking ends the routing launch publishes the experts the FFN may start on
+(the union before the reroute, or SERE's primary union P) and the FFN
+streams their phase 1 while routing finishes.  Its routing outputs must
 be bit-identical to moe_route_dispatch, its y equal to moe_route_dispatch
 followed by moe_ffn_grouped up to the fp32 order of the reductions into y,
 and within the stated bar of the oracle; over batch sizes 1 to 64 (half and
@@ -182,3 +183,64 @@ def test_decode_layer_exercises_the_reroute(g):
     st = lay.stats.cpu().numpy()
     assert st[0] > st[2] > st[1]   # union before > union after > |P|
     assert st[3] > 0 and st[4] > 0  # moved and merged slots
+
+
+EARLY_WORD = 96   # the routing workspace's early flag; the early bitmap follows it
+
+
+def _bits(words, N):
+    return {e for e in range(N) if int(words[e >> 5]) >> (e & 31) & 1}
+
+
+def test_decode_layer_publishes_the_right_early_set(g):
+    """Which experts the routing launch lets the FFN start on, at the Qwen
+    shape over batches 1 to 64 and K' = 1, 2: the union before the reroute
+    when its phase-1 units fit one wave of the SMs (an expert that then
+    moves costs only its phase 1), else SERE's primary union P, which a
+    reroute never takes an expert from.  Both cases must be reached, P must
+    lie inside the final union, and the layer must equal the separate calls
+    bit for bit in its routing."""
+    Lw = syn.decode(32)
+    Dw = g.DevLayer(Lw)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N, I = Lw.N, Lw.I
+    seen = set()
+    for T in (1, 3, 5, 8, 12, 16, 24, 32, 48, 64):
+        x = g.DevLayer(syn.decode(T, with_weights=False), weights=False).x
+        for kp in (1, 2):
+            mk = lambda: moe.MoELayer(Dw.w_r, Dw.w_gate, Dw.w_up, Dw.w_down, k=Lw.k, max_tokens=T, sim=Dw.sim,
+                                      k_primary=kp, rho=Lw.rho)
+            a, b, c = mk(), mk(), mk()
+            assert a.decode_layer_ok(x)
+            ya = torch.zeros(T, Lw.H, dtype=torch.float32, device="cuda:0")
+            a.decode_layer(x, True, ya)
+            b.route_dispatch(x, True)
+            b.ffn(x)
+            c.route_dispatch(x, False)   # plain top-k: the union before the reroute
+            torch.cuda.synchronize()
+            for lay in (a, b, c):
+                assert lay.device_status()[0] == 0
+            for name in ROUTE_OUT:
+                va, vb = getattr(a, name).cpu().numpy(), getattr(b, name).cpu().numpy()
+                if name in ("ids", "gates"):
+                    va, vb = va[:T], vb[:T]
+                if name == "active":
+                    va, vb = va[:1 + va[0]], vb[:1 + vb[0]]
+                assert np.array_equal(va.view(np.uint32), vb.view(np.uint32)), (T, kp, name)
+            y2 = b.y[:T].cpu().numpy()
+            rms = float(np.sqrt(np.mean(y2.astype(np.float64) ** 2)))
+            assert float(np.max(np.abs(ya.cpu().numpy() - y2))) <= 1e-4 * rms
+            ws = a.ws_route.view(torch.int32).cpu().numpy()
+            assert ws[EARLY_WORD] == 1
+            early = _bits(ws[EARLY_WORD + 1:EARLY_WORD + 9].view(np.uint32), N)
+            before = set(np.flatnonzero(c.counts[:N].cpu().numpy() > 0).tolist())
+            after = set(np.flatnonzero(a.counts[:N].cpu().numpy() > 0).tolist())
+            P = _bits(a.union_bitmap.cpu().numpy().view(np.uint32), N)
+            st = a.stats.cpu().numpy()
+            assert len(before) == st[0] and len(P) == st[1] and len(after) == st[2]
+            assert P <= after <= before
+            wave = sms // (I // 64 if T <= 16 else I // 128)
+            case, want = ("before", before) if len(before) <= wave else ("primary", P)
+            assert early == want, (T, kp, case, sorted(early ^ want))
+            seen.add(case)
+    assert seen == {"before", "primary"}, seen

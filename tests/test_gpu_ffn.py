@@ -245,7 +245,7 @@ def test_dependency_wait_times_out_cleanly(g, qwen):
     d = g.gpu_dispatch(g.dev(ids), g.dev(gates), L.N, L.k, L.k)
     ws = g.ffn_workspace(D.x, D.w_gate, L.k, L.T)
     # batch 32: one 32-row chunk per active expert, I / 128 phase-1 units each
-    # (stacked 64-row units are used only for batches of a few tokens)
+    # (stacked 64-row units are used only for batches of up to 16 tokens)
     n1 = int(d["active"][0]) * (L.I // 128)
     ws[:4].view(torch.int32)[0] = n1
     y = torch.full((L.T, L.H), float("nan"), dtype=torch.float32, device=g.DEV)
