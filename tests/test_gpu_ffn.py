@@ -153,6 +153,22 @@ def test_token_major_multi_chunk_ragged(g, fuse):
     _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=fuse)
 
 
+@pytest.mark.parametrize("fuse", [True, False])
+def test_token_major_item_boundaries(g, fuse):
+    """Experts with 256, 128, 129, 1, 384, 97, 29 and 0 rows (k = 1, 1024
+    tokens in shuffled order) in the token-major kernel's 128-row items:
+    whole items, an expert of exactly one item, items followed by a
+    single-row one, partial items and an empty expert."""
+    counts = [256, 128, 129, 1, 384, 97, 29, 0]
+    T = sum(counts)
+    L = syn.qwen_layer(T, H=512, N=len(counts), k=1, I=256)
+    D = g.DevLayer(L)
+    rng = np.random.default_rng(5)
+    ids = rng.permutation(np.repeat(np.arange(len(counts)), counts)).astype(np.int32)[:, None]
+    gates = rng.random((T, 1)).astype(np.float32) + 0.25
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=fuse)
+
+
 def test_token_major_odd_tiles(g):
     """I = 384 (three slices) and H = 768 (three 256-row tiles) in the token-major kernel."""
     L = syn.qwen_layer(1024, H=768, N=6, k=3, I=384)
