@@ -49,10 +49,11 @@ constexpr int kRouteDispatchWs = 512;
 // union of all ranked experts), written as soon as ranking ends
 constexpr int kRouteDispatchEarlyWord = 96;
 // spec_union_max > 0 (with SERE and publish_early): when the batch's ranked
-// union has at most that many experts, the first set published is the whole
-// union instead of P, so the decode FFN streams every candidate's phase 1
-// at once (its SMs would otherwise idle); experts that then move lose only
-// their phase 1
+// union has at most that many experts, or at most twice that many while P
+// has at most a third that many and the rest more than that many, the set
+// published is the whole union instead of P, so the decode FFN streams every candidate's phase 1 at once
+// (its SMs would otherwise idle); experts that then move lose only their
+// phase 1
 cudaError_t launch_route_dispatch(const void* x, int x_dtype, const float* w_router, int T, int H, int N, int k,
                                   bool renorm, float* logits, int32_t* ids, float* gates, const moe_sere_params* sere,
                                   int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_gate,

@@ -248,11 +248,18 @@ __device__ __forceinline__ void batch_tail(const RdArgs& a, float* s_sim, uint64
         // primary away, so P is active whatever the reroute does; without
         // SERE the union of the ranked experts is the active set.  A SERE
         // union small enough for one wave of the FFN's phase-1 units is
-        // published whole: SMs that would idle stream every candidate, and an
-        // expert that then moves costs only its phase 1.
-        int nu = 0;
-        for (int w = 0; w < kMaxPerLane; ++w) nu += __popc(Ubefore[w]);
-        const bool whole = !SERE || nu <= a.spec_max;
+        // published whole: SMs that would idle stream every candidate, and
+        // an expert that then moves costs only its phase 1.  So is one within
+        // two waves whose P would keep at most a third of a wave busy while
+        // the experts outside P need more than a wave (they could not start
+        // in a single wave after the final routing either).
+        int nu = 0, np = 0;
+        for (int w = 0; w < kMaxPerLane; ++w) {
+            nu += __popc(Ubefore[w]);
+            np += __popc(Pbits[w]);
+        }
+        const int sm = a.spec_max;
+        const bool whole = !SERE || nu <= sm || (3 * np <= sm && nu - np > sm && nu <= 2 * sm);
         for (int w = 0; w < kMaxPerLane; ++w) ws[kWsEarly + 1 + w] = whole ? Ubefore[w] : Pbits[w];
         st_release_gpu(reinterpret_cast<int*>(ws) + kWsEarly, 1);
     }

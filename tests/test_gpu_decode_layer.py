@@ -195,9 +195,10 @@ def _bits(words, N):
 def test_decode_layer_publishes_the_right_early_set(g):
     """Which experts the routing launch lets the FFN start on, at the Qwen
     shape over batches 1 to 64 and K' = 1, 2: the union before the reroute
-    when its phase-1 units fit one wave of the SMs (an expert that then
-    moves costs only its phase 1), else SERE's primary union P, which a
-    reroute never takes an expert from.  Both cases must be reached, P must
+    when its phase-1 units fit one wave of the SMs, or two waves while P's
+    units would fill at most a third of one and the other experts' more than
+    one (an expert that then moves costs only its phase 1), else SERE's
+    primary union P, which a reroute never takes an expert from.  Both cases must be reached, P must
     lie inside the final union, and the layer must equal the separate calls
     bit for bit in its routing."""
     Lw = syn.decode(32)
@@ -240,7 +241,9 @@ def test_decode_layer_publishes_the_right_early_set(g):
             assert len(before) == st[0] and len(P) == st[1] and len(after) == st[2]
             assert P <= after <= before
             wave = sms // (I // 64 if T <= 16 else I // 128)
-            case, want = ("before", before) if len(before) <= wave else ("primary", P)
+            nu, np_ = len(before), len(P)
+            whole = nu <= wave or (3 * np_ <= wave and nu - np_ > wave and nu <= 2 * wave)
+            case, want = ("before", before) if whole else ("primary", P)
             assert early == want, (T, kp, case, sorted(early ^ want))
             seen.add(case)
     assert seen == {"before", "primary"}, seen
