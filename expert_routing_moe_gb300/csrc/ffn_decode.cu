@@ -32,11 +32,12 @@
 //   [n1, n1 + nA*MT*KP)  phase 2: per active expert, per 128-row H-tile of
 //                      W_down (and per K half when small batches leave SMs
 //                      idle): gate * W_down A^T added into y.
-// A phase-1 unit is one 128-row I-slice of W_gate and W_up over K = H (or,
-// for batches of at most 16 tokens, a half unit: 64 gate and 64 up rows
-// stacked as one 128-row operand); a phase-2 unit waits (bounded, acquire)
-// until its expert's S phase-1 units have published A.  The warp roles and
-// TMEM accumulators are those of the weight-major kernel in ffn.cu.
+// A phase-1 unit is a half slice: 64 gate rows and the same 64 up rows of
+// W_gate and W_up, stacked as one 128-row MMA operand, over K = H (S = I/64
+// units per expert); the epilogue pairs each gate row with its up row
+// through shared memory.  A phase-2 unit waits (bounded, acquire) until its
+// expert's S phase-1 units have published A.  The warp roles are those of
+// the weight-major kernel in ffn.cu.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -51,17 +52,16 @@ namespace {
 
 __device__ __forceinline__ float silu_mul_d(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
-template <int NT, bool HALF>
+template <int NT>
 struct DcCfg {
-    static constexpr int BI = 128;                  // I-slice of a phase-1 unit (MMA M)
     static constexpr int BH = 128;                  // H-tile of a phase-2 unit (MMA M)
     static constexpr int BK = 64;                   // one 128-byte swizzle row of bf16
     static constexpr int W_BOX = 128 * 64 * 2;      // 16 KiB
     static constexpr int W_BYTES = 2 * W_BOX;       // weights per stage
     static constexpr int X_ATOM = NT * 128;         // NT token rows of one 64-column K chunk
-    static constexpr int X_BYTES = 2 * X_ATOM;      // half units and phase 2 take two K chunks per stage
+    static constexpr int X_BYTES = 2 * X_ATOM;      // every stage takes two K chunks
     static constexpr int STAGE = W_BYTES + X_BYTES;
-    static constexpr int NSTAGE = NT <= 16 ? (HALF ? 5 : 6) : (NT <= 32 ? 5 : 4);
+    static constexpr int NSTAGE = NT <= 32 ? 5 : 4;
     static constexpr int EPI_WARPS = 8;             // two warps per TMEM lane quadrant
     static constexpr int SCHED_WARP = 2 + EPI_WARPS;
     static constexpr int THREADS = 32 * (SCHED_WARP + 1);
@@ -72,12 +72,12 @@ struct DcCfg {
     static constexpr int MISC_INTS = 16;
     static constexpr int RT_CAP = NT * MOE_MAX_RANKS;   // every dispatch row (T <= NT, k <= 16)
     static constexpr int LIST_INTS = 3 * MOE_MAX_EXPERTS + (MOE_MAX_EXPERTS + 1) + 2 * (MOE_MAX_EXPERTS / 32);
-    static constexpr int XCH_BYTES = HALF ? 64 * NT * 4 : 0;
+    static constexpr int XCH_BYTES = 64 * NT * 4;  // the up rows of a phase-1 unit, [NT][64] fp32
     static constexpr int SMEM = 1024 + NSTAGE * STAGE + NBAR * 8 + MISC_INTS * 4 + LIST_INTS * 4 +
                                 EPI_WARPS * 32 * 8 + XCH_BYTES + RT_CAP * 8;
-    static constexpr uint32_t TMEM_COLS = 4 * NT;   // two accumulator slots of 2 x NT columns
+    static constexpr uint32_t TMEM_COLS = 2 * NT;   // two accumulator slots of NT columns
     static_assert(STAGE % 1024 == 0, "stages must stay 1024-byte aligned");
-    static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256, "TMEM allocation");
+    static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128, "TMEM allocation");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(CW == 8 || CW == 16 || CW == 32, "epilogue column split");
 };
@@ -98,17 +98,16 @@ __device__ __forceinline__ int compact_experts(const uint32_t* bm, int N, int* l
 
 }  // namespace
 
-template <int NT, bool HALF>
-__global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
-    ffn_decode_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
-                      const __grid_constant__ CUtensorMap tm_wg64, const __grid_constant__ CUtensorMap tm_wu64,
+template <int NT>
+__global__ void __launch_bounds__(DcCfg<NT>::THREADS, 1)
+    ffn_decode_kernel(const __grid_constant__ CUtensorMap tm_wg64, const __grid_constant__ CUtensorMap tm_wu64,
                       const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_act, const int32_t* __restrict__ offsets,
                       const int32_t* __restrict__ active, const int32_t* __restrict__ row_token,
                       const float* __restrict__ row_gate, const uint32_t* early, __nv_bfloat16* __restrict__ act_g,
                       int* counters, float* __restrict__ out, float* __restrict__ y_zero, int T, int H, int I, int N,
                       int k, int fuse_combine, moe_dev_status* st) {
-    using C = DcCfg<NT, HALF>;
+    using C = DcCfg<NT>;
     constexpr int CW = C::CW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -161,8 +160,8 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
         tc_fence_before();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_wg);
-        tma_prefetch_desc(&tm_wu);
+        tma_prefetch_desc(&tm_wg64);
+        tma_prefetch_desc(&tm_wu64);
         tma_prefetch_desc(&tm_wd);
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_act);
@@ -220,7 +219,7 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
     }
     __syncthreads();
     const int nE = s_cnt[0];
-    const int S = HALF ? I / 64 : I / C::BI;   // phase-1 units per expert
+    const int S = I / 64;                      // phase-1 units (half slices) per expert
     const int MT = H / C::BH;
     const int KT1 = H / C::BK;
     const int KT2 = I / (2 * C::BK);
@@ -418,7 +417,7 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
                     }
                     fence_proxy_async_global();
                 }
-                const int nk = d.p1 ? (HALF ? KT1 / 2 : KT1) : KT2 / s_cnt[5];
+                const int nk = d.p1 ? KT1 / 2 : KT2 / s_cnt[5];
                 for (int kt = 0; kt < nk && ok; ++kt) {
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
@@ -426,7 +425,7 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
                     }
                     const uint32_t dst = ring_a + stage * C::STAGE;
                     const uint32_t fb = bar(B_FULL + stage);
-                    if (d.p1 && HALF) {
+                    if (d.p1) {
                         // two 64-column K chunks; each is [64 gate rows; the same 64 up rows]
                         const int wrow = d.e * I + d.sub * 64;
                         mbar_arrive_expect_tx(fb, C::W_BYTES + 2 * C::X_ATOM);
@@ -436,12 +435,6 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
                             tma_load_2d(dst + c * C::W_BOX + C::W_BOX / 2, &tm_wu64, kc, wrow, fb, pol_w);
                             tma_load_2d(dst + C::W_BYTES + c * C::X_ATOM, &tm_x, kc, 0, fb, pol_x);
                         }
-                    } else if (d.p1) {
-                        const int wrow = d.e * I + d.sub * C::BI;
-                        mbar_arrive_expect_tx(fb, C::W_BYTES + C::X_ATOM);
-                        tma_load_2d(dst, &tm_wg, kt * C::BK, wrow, fb, pol_w);
-                        tma_load_2d(dst + C::W_BOX, &tm_wu, kt * C::BK, wrow, fb, pol_w);
-                        tma_load_2d(dst + C::W_BYTES, &tm_x, kt * C::BK, 0, fb, pol_x);
                     } else {
                         const int wrow = d.e * H + d.sub * C::BH;
                         const int kc = (d.part * nk + kt) * 2 * C::BK;   // first K column of this stage
@@ -490,10 +483,10 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
                 }
                 const bool p1 = un < (table ? s_cnt[3] : nEU);
                 const int b = j & 1;
-                const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
+                const uint32_t acc0 = tmem + b * NT;
                 if (!mbar_wait(bar(B_ACCE + b), ((j >> 1) & 1) ^ 1, abort_flag, st, kSiteMmaTmemFree)) break;
                 tc_fence_after();
-                const int nk = p1 ? (HALF ? KT1 / 2 : KT1) : KT2 / s_cnt[5];
+                const int nk = p1 ? KT1 / 2 : KT2 / s_cnt[5];
                 for (int kt = 0; kt < nk; ++kt) {
                     if (!mbar_wait(bar(B_FULL + stage), phase, abort_flag, st, kSiteMmaFull)) {
                         ok = false;
@@ -501,21 +494,13 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t a = ring_a + stage * C::STAGE;
-                    if (p1 && !HALF) {
+                    // two K chunks: 128 weight rows (phase 1: 64 gate and 64 up rows
+                    // stacked) against the NT token columns of the same chunk
 #pragma unroll
-                        for (int kk = 0; kk < C::BK / 16; ++kk) {
-                            const uint64_t dx = sw128_desc(a + C::W_BYTES + kk * 32);
-                            const uint32_t acc = (kt | kk) != 0;
-                            tc_mma_bf16(acc0, sw128_desc(a + kk * 32), dx, idesc, acc);
-                            tc_mma_bf16(acc1, sw128_desc(a + C::W_BOX + kk * 32), dx, idesc, acc);
-                        }
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < 2 * C::BK / 16; ++kk) {
-                            const uint64_t dw = sw128_desc(a + (kk >> 2) * C::W_BOX + (kk & 3) * 32);
-                            const uint64_t dx = sw128_desc(a + C::W_BYTES + (kk >> 2) * C::X_ATOM + (kk & 3) * 32);
-                            tc_mma_bf16(acc0, dw, dx, idesc, (kt | kk) != 0);
-                        }
+                    for (int kk = 0; kk < 2 * C::BK / 16; ++kk) {
+                        const uint64_t dw = sw128_desc(a + (kk >> 2) * C::W_BOX + (kk & 3) * 32);
+                        const uint64_t dx = sw128_desc(a + C::W_BYTES + (kk >> 2) * C::X_ATOM + (kk & 3) * 32);
+                        tc_mma_bf16(acc0, dw, dx, idesc, (kt | kk) != 0);
                     }
                     tc_commit(bar(B_EMPTY + stage));
                     if (++stage == C::NSTAGE) {
@@ -569,9 +554,9 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
             Unit d{};
             if (okw) decode(un, d);
             const int b = j & 1;
-            const uint32_t acc0 = tmem + b * 2 * NT, acc1 = acc0 + NT;
+            const uint32_t acc0 = tmem + b * NT;
             okw = __all_sync(kFull, okw && mbar_wait(bar(B_ACCF + b), (j >> 1) & 1, abort_flag, st, kSiteEpiG1Done));
-            if (HALF && d.p1) {
+            if (d.p1) {
                 // accumulator lanes 0-63: gate rows, 64-127: the same up rows.  The
                 // up warps stage their values in shared memory; after a barrier of
                 // all epilogue warps (taken by every warp) the gate warps form the
@@ -615,74 +600,50 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
                 }
             } else if (okw) {
                 tc_fence_after();
-                if (d.p1) {
-                    // SwiGLU of this thread's I row for the warp's token columns -> A (bf16)
-                    __nv_bfloat16* dst = act_g + static_cast<size_t>(d.e) * NT * I + d.sub * C::BI + row;
+                // column c_lo + js is token c_lo + js: etok[js] = its dispatch row
+                // for this expert, or -1 when the token was not routed here
+                if (lane < CW) etok[lane] = -1;
+                __syncwarp();
+                for (int jr = lane; jr < d.cnt; jr += 32) {
+                    const int r = d.row0 + jr;
+                    const int t = s_rt[r];
+                    if (t >= c_lo && t < c_lo + CW && t < T) {
+                        etok[t - c_lo] = r;
+                        egt[t - c_lo] = s_rg[r];
+                    }
+                }
+                __syncwarp();
+                // read the accumulator in chunks of up to 16 columns; it is released right
+                // after the last read, before the last chunk's reductions
+                constexpr int CH = CW < 16 ? CW : 16;
+                const int h = d.sub * C::BH + row;
 #pragma unroll
-                    for (int c8 = 0; c8 < CW / 8; ++c8) {
-                        if (c_lo + c8 * 8 >= ncol) break;   // warp-uniform
-                        uint32_t g[8], u[8];
-                        tmem_ld8(acc0 + lane_off + c_lo + c8 * 8, g);
-                        tmem_ld8(acc1 + lane_off + c_lo + c8 * 8, u);
+                for (int c16 = 0; c16 < CW / CH; ++c16) {
+                    const bool any = c_lo + c16 * CH < ncol;   // warp-uniform
+                    uint32_t vv[CH];
+                    if (any) {
+                        if constexpr (CH == 8) {
+                            tmem_ld8(acc0 + lane_off + c_lo, vv);
+                        } else {
+                            tmem_ld16(acc0 + lane_off + c_lo + c16 * CH, vv);
+                        }
                         tmem_ld_wait();
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const int t = c_lo + c8 * 8 + jj;
-                            dst[static_cast<size_t>(t) * I] =
-                                __float2bfloat16_rn(silu_mul_d(__uint_as_float(g[jj]), __uint_as_float(u[jj])));
-                        }
                     }
-                    tc_fence_before();
-                    mbar_arrive(bar(B_ACCE + b));
-                    // make the stores visible to the phase-2 TMA loads of other CTAs
-                    fence_proxy_async_global();
-                    __threadfence();
-                } else {
-                    // column c_lo + js is token c_lo + js: etok[js] = its dispatch row
-                    // for this expert, or -1 when the token was not routed here
-                    if (lane < CW) etok[lane] = -1;
-                    __syncwarp();
-                    for (int jr = lane; jr < d.cnt; jr += 32) {
-                        const int r = d.row0 + jr;
-                        const int t = s_rt[r];
-                        if (t >= c_lo && t < c_lo + CW && t < T) {
-                            etok[t - c_lo] = r;
-                            egt[t - c_lo] = s_rg[r];
-                        }
+                    if (c16 == CW / CH - 1) {
+                        tc_fence_before();
+                        mbar_arrive(bar(B_ACCE + b));
                     }
-                    __syncwarp();
-                    // read the accumulator in chunks of up to 16 columns; it is released right
-                    // after the last read, before the last chunk's reductions
-                    constexpr int CH = CW < 16 ? CW : 16;
-                    const int h = d.sub * C::BH + row;
+                    if (!any) continue;
 #pragma unroll
-                    for (int c16 = 0; c16 < CW / CH; ++c16) {
-                        const bool any = c_lo + c16 * CH < ncol;   // warp-uniform
-                        uint32_t vv[CH];
-                        if (any) {
-                            if constexpr (CH == 8) {
-                                tmem_ld8(acc0 + lane_off + c_lo, vv);
-                            } else {
-                                tmem_ld16(acc0 + lane_off + c_lo + c16 * CH, vv);
-                            }
-                            tmem_ld_wait();
-                        }
-                        if (c16 == CW / CH - 1) {
-                            tc_fence_before();
-                            mbar_arrive(bar(B_ACCE + b));
-                        }
-                        if (!any) continue;
-#pragma unroll
-                        for (int jj = 0; jj < CH; ++jj) {
-                            const int js = c16 * CH + jj;
-                            const int r = etok[js];
-                            if (r >= 0) {
-                                if (fuse_combine)
-                                    atomicAdd(out + static_cast<size_t>(c_lo + js) * H + h,
-                                              egt[js] * __uint_as_float(vv[jj]));
-                                else
-                                    atomicAdd(out + static_cast<size_t>(r) * H + h, __uint_as_float(vv[jj]));
-                            }
+                    for (int jj = 0; jj < CH; ++jj) {
+                        const int js = c16 * CH + jj;
+                        const int r = etok[js];
+                        if (r >= 0) {
+                            if (fuse_combine)
+                                atomicAdd(out + static_cast<size_t>(c_lo + js) * H + h,
+                                          egt[js] * __uint_as_float(vv[jj]));
+                            else
+                                atomicAdd(out + static_cast<size_t>(r) * H + h, __uint_as_float(vv[jj]));
                         }
                     }
                 }
@@ -711,20 +672,18 @@ __global__ void __launch_bounds__(DcCfg<NT, HALF>::THREADS, 1)
 // Rows of the decode kernel's activation buffer: NT per expert.
 long long ffn_decode_act_rows(int T, int N) { return static_cast<long long>(N) * ffn_decode_nt(T); }
 
-template <int NT, bool HALF>
+template <int NT>
 static cudaError_t run_decode(const void* x, const void* wg, const void* wu, const void* wd, int T, int H, int I,
                               int N, int k, const int32_t* offsets, const int32_t* row_token, const float* row_gate,
                               const int32_t* active, const uint32_t* early, uint32_t flags, float* out, void* ws,
                               moe_dev_status* st, cudaStream_t s) {
-    using C = DcCfg<NT, HALF>;
+    using C = DcCfg<NT>;
     const bool fuse = (flags & MOE_FFN_FUSE_COMBINE) != 0;
     int* counters = static_cast<int*>(ws);
     __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + ffn_decode_ctr_bytes());
     float* y_zero = (fuse && (flags & MOE_FFN_ZERO_Y)) ? out : nullptr;
-    CUtensorMap tm_wg, tm_wu, tm_wg64, tm_wu64, tm_wd, tm_x, tm_act;
-    if (!make_tmap(&tm_wg, wg, H, static_cast<uint64_t>(N) * I, 64, 128) ||
-        !make_tmap(&tm_wu, wu, H, static_cast<uint64_t>(N) * I, 64, 128) ||
-        !make_tmap(&tm_wg64, wg, H, static_cast<uint64_t>(N) * I, 64, 64) ||
+    CUtensorMap tm_wg64, tm_wu64, tm_wd, tm_x, tm_act;
+    if (!make_tmap(&tm_wg64, wg, H, static_cast<uint64_t>(N) * I, 64, 64) ||
         !make_tmap(&tm_wu64, wu, H, static_cast<uint64_t>(N) * I, 64, 64) ||
         !make_tmap(&tm_wd, wd, I, static_cast<uint64_t>(N) * H, 64, 128) ||
         // the whole batch as one box of NT rows (rows past T read as zero)
@@ -737,23 +696,26 @@ static cudaError_t run_decode(const void* x, const void* wg, const void* wu, con
     if (e != cudaSuccess) return e;
     if (devi < 0 || devi >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[devi]) {
-        e = cudaFuncSetAttribute(ffn_decode_kernel<NT, HALF>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(ffn_decode_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set[devi] = true;
     }
-    return launch_pdl(ffn_decode_kernel<NT, HALF>, dim3(sm_count()), dim3(C::THREADS), C::SMEM, s, tm_wg, tm_wu,
-                      tm_wg64, tm_wu64, tm_wd, tm_x, tm_act, offsets, active, row_token, row_gate, early, act,
+    return launch_pdl(ffn_decode_kernel<NT>, dim3(sm_count()), dim3(C::THREADS), C::SMEM, s, tm_wg64, tm_wu64,
+                      tm_wd, tm_x, tm_act, offsets, active, row_token, row_gate, early, act,
                       counters, out, y_zero, T, H, I, N, k, fuse ? 1 : 0, st);
 }
 
-// half phase-1 units for batches of up to 16 tokens: their few dozen active
-// experts give at most a wave or two of whole 128-row I-slices (fewer than
-// the SMs when T*k or N is small), and twice the units let the work counter
-// even out SMs that stream at different rates
-static bool decode_half_units(int T) { return ffn_decode_nt(T) == 16; }
-
+// Phase-1 units are half slices (64 gate and 64 up rows) at every batch: a
+// few dozen active experts give only a wave or two of whole 128-row
+// I-slices (fewer than the SMs when T*k or N is small), so the experts whose
+// phase 1 falls in the last, partial wave would hold up their down
+// projections; twice the units let the work counter even out SMs that
+// stream at different rates.
 int ffn_decode_units_per_expert(int T, int I, int N, int k) {
-    return decode_half_units(T) ? I / 64 : I / 128;
+    (void)T;
+    (void)N;
+    (void)k;
+    return I / 64;
 }
 
 int ffn_decode_one_wave_experts(int T, int I, int N, int k) {
@@ -767,14 +729,14 @@ cudaError_t launch_ffn_decode(const void* x, const void* wg, const void* wu, con
     if (T < 1 || T > kDecodeMaxT || k > MOE_MAX_RANKS || N > MOE_MAX_EXPERTS) return cudaErrorInvalidValue;
     switch (ffn_decode_nt(T)) {
         case 16:
-            return run_decode<16, true>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
-                                        flags, out, ws, st, s);
+            return run_decode<16>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early, flags,
+                                  out, ws, st, s);
         case 32:
-            return run_decode<32, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
-                                         flags, out, ws, st, s);
+            return run_decode<32>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early, flags,
+                                  out, ws, st, s);
         default:
-            return run_decode<64, false>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early,
-                                         flags, out, ws, st, s);
+            return run_decode<64>(x, wg, wu, wd, T, H, I, N, k, offsets, row_token, row_gate, active, early, flags,
+                                  out, ws, st, s);
     }
 }
 

@@ -4,8 +4,8 @@ ranking ends the routing launch publishes the experts the FFN may start on
 streams their phase 1 while routing finishes.  Its routing outputs must
 be bit-identical to moe_route_dispatch, its y equal to moe_route_dispatch
 followed by moe_ffn_grouped up to the fp32 order of the reductions into y,
-and within the stated bar of the oracle; over batch sizes 1 to 64 (half and
-whole phase-1 units, ragged token columns), with and without SERE,
+and within the stated bar of the oracle; over batch sizes 1 to 64 (16-, 32-
+and 64-column token tiles, ragged token columns), with and without SERE,
 protection, renormalised gates, accumulation into y, repeated calls on one
 pair of workspaces, and steps captured in one CUDA graph."""
 import numpy as np
@@ -240,7 +240,7 @@ def test_decode_layer_publishes_the_right_early_set(g):
             st = a.stats.cpu().numpy()
             assert len(before) == st[0] and len(P) == st[1] and len(after) == st[2]
             assert P <= after <= before
-            wave = sms // (I // 64 if T <= 16 else I // 128)
+            wave = sms // (I // 64)   # half-slice phase-1 units: I / 64 per expert
             nu, np_ = len(before), len(P)
             whole = nu <= wave or (3 * np_ <= wave and nu - np_ > wave and nu <= 2 * wave)
             case, want = ("before", before) if whole else ("primary", P)

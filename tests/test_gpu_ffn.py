@@ -78,8 +78,9 @@ def test_decode_bf16_batch128_sampled(g, qwen):
 
 
 def test_small_bf16_multi_chunk_ragged(g):
-    """T=200 with a skewed routing: the hottest expert has > 64 rows, so it is
-    split into several token chunks with a ragged tail; H and I span several tiles."""
+    """T=200 (the weight-major kernel) with a skewed routing: the hottest
+    expert has > 64 rows, so it is split into several token chunks with a
+    ragged tail; H and I span several tiles."""
     L = syn.qwen_layer(200, H=384, N=16, k=4, I=256)
     D = g.DevLayer(L)
     rng = np.random.default_rng(0)
@@ -92,7 +93,8 @@ def test_small_bf16_multi_chunk_ragged(g):
 
 
 def test_small_bf16_odd_slice_count(g):
-    """I = 384: three 128-row slices per expert; H = 256: two down-projection tiles."""
+    """The decode kernel at I = 384 (six half-slice phase-1 units per expert)
+    and H = 256 (two down-projection tiles)."""
     L = syn.qwen_layer(24, H=256, N=8, k=3, I=384)
     D = g.DevLayer(L)
     ids, gates = _route(L, L.x_bf16, 24)
@@ -188,15 +190,15 @@ def test_token_major_many_ranks(g, fuse):
 
 
 @pytest.mark.parametrize("T,N,k,H,I", [
-    (12, 64, 12, 256, 128),    # 16-row chunks, stacked units, 144 rows: tokens and gates from global memory
-    (16, 128, 8, 256, 768),    # 16-row chunks, whole slices, 128 rows staged in shared memory
-    (24, 64, 12, 256, 256),    # 32-row chunks, 288 rows staged
-    (30, 64, 16, 256, 256),    # 32-row chunks, 480 rows: past one staging pass, global loads
+    (12, 64, 12, 256, 128),    # 16-column token tile, k = 12, two half units per expert
+    (16, 128, 8, 256, 768),    # 16-column tile, full Qwen expert width
+    (24, 64, 12, 256, 256),    # 32-column tile, 288 dispatch rows
+    (30, 64, 16, 256, 256),    # 32-column tile, k = 16: 480 dispatch rows
 ])
-def test_weight_major_unit_and_staging_paths(g, T, N, k, H, I):
-    """Each combination of the weight-major kernel's host-chosen variants:
-    stacked or whole phase-1 units, row tokens and gates staged in shared
-    memory or read from global memory."""
+def test_decode_kernel_odd_shapes(g, T, N, k, H, I):
+    """The decode kernel (every batch of up to 64 tokens) at shapes off the
+    Qwen one: k = 12 and 16, I = 128 and 256, H = 256; fused combine and
+    rows out."""
     L = syn.qwen_layer(T, H=H, N=N, k=k, I=I)
     D = g.DevLayer(L)
     ids, gates = _route(L, L.x_bf16, T)
@@ -204,15 +206,32 @@ def test_weight_major_unit_and_staging_paths(g, T, N, k, H, I):
     _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=False)
 
 
-def test_weight_major_max_experts(g):
+def test_decode_kernel_max_experts(g):
     """N = 256 experts (the library's maximum) with k = 16 at a batch of 40:
-    up to 256 active experts in the weight-major kernel's item table, 64-row
-    token chunks."""
+    up to 256 active experts in the decode kernel's expert lists."""
     L = syn.qwen_layer(40, H=256, N=256, k=16, I=128)
     D = g.DevLayer(L)
     ids, gates = _route(L, L.x_bf16, 40)
     assert len(np.unique(ids[ids >= 0])) > 128
     _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
+
+
+@pytest.mark.parametrize("T,N,k,H,I", [
+    (65, 64, 8, 256, 128),     # the smallest weight-major batch; one I-slice per expert
+    (100, 128, 8, 256, 768),   # the Qwen expert width
+    (300, 64, 12, 512, 256),   # k = 12, two 64-row chunks for most experts
+    (80, 256, 16, 256, 128),   # N = 256 and k = 16: up to 256 active experts in the item table
+    (1000, 32, 4, 256, 384),   # the largest weight-major batch class, many chunks per expert
+])
+def test_weight_major_kernel_shapes(g, T, N, k, H, I):
+    """The weight-major kernel (batches of 65 to 1023 tokens: the weights as
+    the 128-row MMA operand, each expert's rows in chunks of 64 as N), fused
+    combine and rows out."""
+    L = syn.qwen_layer(T, H=H, N=N, k=k, I=I)
+    D = g.DevLayer(L)
+    ids, gates = _route(L, L.x_bf16, T)
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
+    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=False)
 
 
 def test_token_major_prefill_shape_sampled(g, qwen):
@@ -251,8 +270,9 @@ def test_token_major_shared_workspace_and_empty_dispatch(g, fuse):
 
 def test_dependency_wait_times_out_cleanly(g, qwen):
     """Failure detection without a fault: the work counter is preset past the
-    phase-1 units, so every CTA draws only phase-2 units whose activations
-    nothing will publish (a flag that nothing sets).  The bounded wait runs
+    phase-1 units, so after its static first unit every CTA draws only
+    phase-2 units, and the experts whose phase-1 units were skipped never
+    publish their activations (a flag that nothing sets).  The bounded wait runs
     out, the launch reports MOE_DEV_TIMEOUT at the dependency site and
     returns; the last CTA still returns the counters to zero, so the same
     workspace then serves a normal call."""
@@ -260,9 +280,9 @@ def test_dependency_wait_times_out_cleanly(g, qwen):
     ids, gates = _route(L, L.x_bf16, L.T)
     d = g.gpu_dispatch(g.dev(ids), g.dev(gates), L.N, L.k, L.k)
     ws = g.ffn_workspace(D.x, D.w_gate, L.k, L.T)
-    # batch 32: one 32-row chunk per active expert, I / 128 phase-1 units each
-    # (stacked 64-row units are used only for batches of up to 16 tokens)
-    n1 = int(d["active"][0]) * (L.I // 128)
+    # batch 32: one 32-row chunk per active expert and I / 64 phase-1 units
+    # each (half slices: 64 gate and 64 up rows stacked)
+    n1 = int(d["active"][0]) * (L.I // 64)
     ws[:4].view(torch.int32)[0] = n1
     y = torch.full((L.T, L.H), float("nan"), dtype=torch.float32, device=g.DEV)
     st = g.status_tensor()
