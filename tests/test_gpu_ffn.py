@@ -219,19 +219,24 @@ def test_decode_kernel_max_experts(g):
 @pytest.mark.parametrize("T,N,k,H,I", [
     (65, 64, 8, 256, 128),     # the smallest weight-major batch; one I-slice per expert
     (100, 128, 8, 256, 768),   # the Qwen expert width
-    (300, 64, 12, 512, 256),   # k = 12, two 64-row chunks for most experts
-    (80, 256, 16, 256, 128),   # N = 256 and k = 16: up to 256 active experts in the item table
-    (1000, 32, 4, 256, 384),   # the largest weight-major batch class, many chunks per expert
+    (300, 64, 12, 512, 256),   # k = 12: about 56 rows per expert, some in two 64-row chunks
+    (80, 256, 16, 256, 128),   # N = 256 and k = 16: 255 active experts in the item table
+    (1000, 32, 4, 256, 384),   # near the largest weight-major batch: two or three chunks per expert
 ])
 def test_weight_major_kernel_shapes(g, T, N, k, H, I):
     """The weight-major kernel (batches of 65 to 1023 tokens: the weights as
     the 128-row MMA operand, each expert's rows in chunks of 64 as N), fused
-    combine and rows out."""
+    combine and rows out.  The activations are N(0, 1): the synthetic layers
+    scale x to give their router logits a set spread, which at H = 256 means
+    x of rms ~400 and a y whose largest elements are 13x its rms, where the
+    bf16 rounding of the SwiGLU activations alone reaches 2e-2 * rms."""
     L = syn.qwen_layer(T, H=H, N=N, k=k, I=I)
     D = g.DevLayer(L)
-    ids, gates = _route(L, L.x_bf16, T)
-    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
-    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates, fuse=False)
+    x_bits = syn.f32_to_bf16_bits(np.random.default_rng(T).standard_normal((T, H)).astype(np.float32))
+    x_dev = g.dev(x_bits, torch.bfloat16)
+    ids, gates = _route(L, x_bits, T)
+    _ffn_case(g, L, D, x_bits, x_dev, ids, gates)
+    _ffn_case(g, L, D, x_bits, x_dev, ids, gates, fuse=False)
 
 
 def test_token_major_prefill_shape_sampled(g, qwen):
