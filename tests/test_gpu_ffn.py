@@ -208,12 +208,16 @@ def test_decode_kernel_odd_shapes(g, T, N, k, H, I):
 
 def test_decode_kernel_max_experts(g):
     """N = 256 experts (the library's maximum) with k = 16 at a batch of 40:
-    up to 256 active experts in the decode kernel's expert lists."""
+    up to 256 active experts in the decode kernel's expert lists.  N(0, 1)
+    activations, as in the weight-major shapes below (the synthetic x is
+    scaled to rms ~300 at this shape)."""
     L = syn.qwen_layer(40, H=256, N=256, k=16, I=128)
     D = g.DevLayer(L)
-    ids, gates = _route(L, L.x_bf16, 40)
+    x_bits = syn.f32_to_bf16_bits(np.random.default_rng(40).standard_normal((40, 256)).astype(np.float32))
+    x_dev = g.dev(x_bits, torch.bfloat16)
+    ids, gates = _route(L, x_bits, 40)
     assert len(np.unique(ids[ids >= 0])) > 128
-    _ffn_case(g, L, D, L.x_bf16, D.x, ids, gates)
+    _ffn_case(g, L, D, x_bits, x_dev, ids, gates)
 
 
 @pytest.mark.parametrize("T,N,k,H,I", [
