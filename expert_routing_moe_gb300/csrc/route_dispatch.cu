@@ -393,25 +393,28 @@ __global__ void __launch_bounds__(kRdThreads, 1) route_dispatch_kernel(const XT*
     __shared__ bool s_last;
     __shared__ __align__(8) uint64_t sim_bar;
     __shared__ int abort_flag;
-    pdl_wait();
-    if (a.publish && blockIdx.x == 0 && blockIdx.y == 0) {
-        // the early flag goes back to zero before any CTA of this grid lets
-        // the FFN launch, so the FFN can only see this call's publication
-        if (threadIdx.x == 0) {
-            a.ws[kWsEarly] = 0;
-            __threadfence();
+    // 1. this CTA's tile of router logits; its first W_r lines are requested
+    // before the wait for the preceding launch (which does not write W_r)
+    auto after_first_loads = [&]() {
+        pdl_wait();
+        if (a.publish && blockIdx.x == 0 && blockIdx.y == 0) {
+            // the early flag goes back to zero before any CTA of this grid lets
+            // the FFN launch, so the FFN can only see this call's publication
+            if (threadIdx.x == 0) {
+                a.ws[kWsEarly] = 0;
+                __threadfence();
+            }
+            __syncthreads();
         }
-        __syncthreads();
-    }
-    pdl_trigger();
-    if (SERE && blockIdx.x == 0 && blockIdx.y == 0) {
-        // pull the similarity into the L2 while the logits are computed
-        const int lines = (a.N * a.N * 4 + 127) / 128;
-        for (int l = threadIdx.x; l < lines; l += blockDim.x) prefetch_l2_keep(a.sim + l * 32);
-    }
-    // 1. this CTA's tile of router logits
+        pdl_trigger();
+        if (SERE && blockIdx.x == 0 && blockIdx.y == 0) {
+            // pull the similarity into the L2 while the logits are computed
+            const int lines = (a.N * a.N * 4 + 127) / 128;
+            for (int l = threadIdx.x; l < lines; l += blockDim.x) prefetch_l2_keep(a.sim + l * 32);
+        }
+    };
     router_tile<XT, kRdEpc, (sizeof(XT) == 2 ? 4 : 2)>(x, w, a.T, a.H, a.N, blockIdx.x * kRdEpc, blockIdx.y * 4,
-                                                         a.logits, part);
+                                                         a.logits, part, after_first_loads);
     // the CTA's logit writes are published by its ticket (barrier, then an
     // acquire-release fetch-and-add by one thread)
     __syncthreads();

@@ -64,14 +64,37 @@ struct XRaw<__nv_bfloat16> {
     static __device__ __forceinline__ type zero() { return make_uint2(0u, 0u); }
 };
 
-template <typename XT, int EPC, int U = 4>
+// Runs nothing; the default step between a router tile's first weight
+// prefetches and the rest of it.
+struct NoStep {
+    __device__ __forceinline__ void operator()() const {}
+};
+
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+
+// `mid` is called by every thread of the CTA after the thread's first batch
+// of W_r lines has been requested into the L1 and before any x is read: a
+// kernel launched as a programmatic dependent passes its dependency wait
+// here, since W_r is not written by the launch it waits for, and the first
+// weight round trip then overlaps the end of that launch.
+template <typename XT, int EPC, int U = 4, typename Mid = NoStep>
 __device__ __forceinline__ void router_tile(const XT* __restrict__ x, const float* __restrict__ w, int T, int H,
-                                            int N, int j0, int t0, float* __restrict__ logits, float (*part)[4]) {
+                                            int N, int j0, int t0, float* __restrict__ logits, float (*part)[4],
+                                            Mid mid = Mid()) {
     using XR = XRaw<XT>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int j = j0 + (warp >> 2);
     const int hq = ((H >> 2) + 127) / 128 * 128;
     const int hbeg = min((warp & 3) * hq, H), hend = min(hbeg + hq, H);
+    if (j < N) {
+        const float* wr = w + static_cast<size_t>(j) * H;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int h = hbeg + lane * 4 + 128 * u;
+            if (h < hend) prefetch_l1(wr + h);
+        }
+    }
+    mid();
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (j < N) {
         const uint64_t pol = l2_evict_last_policy();
