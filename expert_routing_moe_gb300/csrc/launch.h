@@ -80,8 +80,8 @@ inline int ffn_decode_nt(int T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
 // region at the start of the workspace; the activations follow
 inline size_t ffn_decode_ctr_bytes() { return 2304; }
 long long ffn_decode_act_rows(int T, int N);
-// phase-1 units per expert the decode kernel runs for this shape (I/128, or
-// I/64 when it takes half units)
+// phase-1 units per expert the decode kernel runs for this shape: I/64 half
+// slices (64 gate and 64 up rows each)
 int ffn_decode_units_per_expert(int T, int I, int N, int k);
 // the most experts whose phase-1 units all fit one wave of the SMs
 int ffn_decode_one_wave_experts(int T, int I, int N, int k);
