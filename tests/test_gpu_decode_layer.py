@@ -83,6 +83,16 @@ def test_decode_layer_matches_separate_calls(g, T, sere):
     _compare(g, L, sere, oracle_check=T in (3, 17, 64))
 
 
+@pytest.mark.parametrize("T,sere", [(40, False), (40, True), (64, True)])
+def test_decode_layer_max_experts_and_ranks(g, T, sere):
+    """The library's limits in the one-call decode layer: N = 256 experts
+    (an eight-word early bitmap; the 256 x 256 similarity is read from
+    global memory, past the shared-memory staging limit) and k = 16 (1024
+    dispatch rows at 64 tokens), against the separate calls."""
+    L = syn.qwen_layer(T, H=256, N=256, k=16, I=128, token_stream_offset=T)
+    _compare(g, L, sere)
+
+
 def test_decode_layer_full_size_against_oracle(g):
     for sere in (False, True):
         L = syn.decode(32)
