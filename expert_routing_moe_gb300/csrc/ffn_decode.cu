@@ -394,7 +394,6 @@ __global__ void __launch_bounds__(DcCfg<NT>::THREADS, 1)
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
             if (!ok || fin) break;
             int nxt = 0;
-            if (lane == 0) nxt = atomicAdd(work_head, 1) + static_cast<int>(gridDim.x);
             if (lane == 0) {
                 Unit d;
                 decode(cur, d);
@@ -418,7 +417,14 @@ __global__ void __launch_bounds__(DcCfg<NT>::THREADS, 1)
                     fence_proxy_async_global();
                 }
                 const int nk = d.p1 ? KT1 / 2 : KT2 / s_cnt[5];
+                // the next unit is reserved two stages before this one's last: late
+                // enough that a CTA near the end of the queue holds as little work
+                // that an idle SM could have taken, early enough to hide the
+                // counter's round trip (a loop that stops early reserves nothing,
+                // and the CTA then stops too)
+                const int kres = nk > 2 ? nk - 2 : 0;
                 for (int kt = 0; kt < nk && ok; ++kt) {
+                    if (kt == kres) nxt = atomicAdd(work_head, 1) + static_cast<int>(gridDim.x);
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
                         break;
