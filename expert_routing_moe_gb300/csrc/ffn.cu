@@ -403,9 +403,11 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
             }
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
             if (!ok || done) break;
-            // the next unit's id arrives while this unit's copies are issued
+            // the next unit is reserved two stages before this one's last: late
+            // enough that a CTA near the end of the queue holds little work an
+            // idle SM could have taken, early enough to hide the counter's round
+            // trip (a loop that stops early reserves nothing; the CTA stops too)
             int nxt = 0;
-            if (lane == 0) nxt = atomicAdd(work_head, 1);
             const bool p1 = cur < n1;
             int item, sub, part;   // sub: I-slice or H-tile
             decode(cur, item, sub, part);
@@ -442,7 +444,9 @@ __global__ void __launch_bounds__(StCfg<NT>::THREADS, 1)
                 const int n_g4 = (nrows + 3) / 4;
                 const int n16 = (min(NT, max(16, (nrows + 15) & ~15))) / 16;
                 const int nk = p1 ? KT1 : KT2P;
+                const int kres = nk > 2 ? nk - 2 : 0;
                 for (int kt = 0; kt < nk && ok; ++kt) {
+                    if (kt == kres) nxt = atomicAdd(work_head, 1);
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -835,8 +839,7 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1)
             }
             ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
             if (!ok || done) break;
-            int nxt = 0;
-            if (lane == 0) nxt = atomicAdd(work_head, 1);
+            int nxt = 0;   // reserved two stages before this unit's last (as in ffn_stream_kernel)
             const bool p1 = cur < n1;
             const int v = p1 ? cur : cur - n1;
             const int item = p1 ? v / S : v / MT;
@@ -862,7 +865,9 @@ __global__ void __launch_bounds__(PfCfg::THREADS, 1)
                     fence_proxy_async_global();
                 }
                 const int nk = p1 ? KT1 : KT2;
+                const int kres = nk > 2 ? nk - 2 : 0;
                 for (int kt = 0; kt < nk && ok; ++kt) {
+                    if (kt == kres) nxt = atomicAdd(work_head, 1);
                     if (!mbar_wait(bar(B_EMPTY + stage), phase ^ 1u, abort_flag, st, kSiteProducerEmpty)) {
                         ok = false;
                         break;
