@@ -155,11 +155,14 @@ moe_status_t moe_route_dispatch(const void* x, int x_dtype, const float* w_route
  * One decode MoE layer in one call: moe_route_dispatch, then the grouped
  * SwiGLU FFN with the weighted combine fused in (y = sum_j G(x)_j E_j(x),
  * "MACS" sec. 3.1 Eq. (1); with `sere`, the "SERE" article's batch reroute,
- * sec. 4.1-4.2).  The FFN starts streaming the weights of the experts that
- * are certain to be active -- SERE's primary union P (sec. 4.1: primaries
- * are never rerouted), or without SERE the union of the ranked experts --
- * as soon as ranking ends, while the routing launch still reroutes and
- * permutes; the other experts and the down projections wait for the final
+ * sec. 4.1-4.2).  As soon as ranking ends, while the routing launch still
+ * reroutes and permutes, the FFN starts streaming the weights of a published
+ * set of experts: without SERE the union of the ranked experts; with SERE
+ * its primary union P (sec. 4.1: primaries are never rerouted), or the whole
+ * union before the reroute when that union's phase-1 units fit one wave of
+ * the SMs, or two waves while P's would fill at most a third of one and the
+ * other experts' more than one (an expert that then moves costs only its
+ * phase 1).  The other experts and the down projections wait for the final
  * routing.  Results equal moe_route_dispatch followed by moe_ffn_grouped
  * with MOE_FFN_FUSE_COMBINE (up to the fp32 summation order of y).
  *
