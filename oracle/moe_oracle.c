@@ -45,7 +45,9 @@
  *   orc_similarity     pinned: a duplicated expert -> 1, a negated down
  *                      projection -> -1, a positively scaled one -> 1,
  *                      experts writing disjoint coordinates -> 0, symmetry,
- *                      unit diagonal, |sim| <= 1.
+ *                      unit diagonal, |sim| <= 1; closed forms for the
+ *                      SwiGLU orientation (-1), the stacked-token cosine
+ *                      (1/sqrt 2) and the sign of silu(c) + silu(-c).
  *   orc_token_weights  pinned: entropy against scipy's entropy of softmax,
  *                      closed forms (uniform z -> ln D, one raised entry,
  *                      shift invariance), two-token z-score -> sigmoid(+-delta),

@@ -53,3 +53,54 @@ def test_random_experts_are_bounded_and_not_degenerate():
     off = s[~np.eye(5, dtype=bool)]
     assert np.all(np.abs(off) < 0.99)
     assert np.array_equal(s, s.T)
+
+
+def test_swiglu_orientation_closed_form():
+    """With one intermediate row, an expert's output on token t is
+    s_t * w_d with s_t = silu(g_t) * u_t.  Expert 0 gates on x[0] and takes
+    u from x[1]; expert 1 uses x[0] for both; both share w_d.  On the tokens
+    (c, -c) and (-c, c), with s = sigmoid(c): expert 0 gives
+    s_t = -c^2 (s, 1 - s) and expert 1 gives c^2 (s, 1 - s), so the similarity
+    is exactly -1 for every c.  Gate and up swapped would give
+    -2 s (1 - s) / (s^2 + (1 - s)^2); dropping u would give +1."""
+    for c in (0.7, 1.9, 3.2):
+        x = np.array([[c, -c], [-c, c]], np.float32)
+        wg = np.array([[[1.0, 0.0]], [[1.0, 0.0]]], np.float32)   # [N][I][H]
+        wu = np.array([[[0.0, 1.0]], [[1.0, 0.0]]], np.float32)
+        wd = np.array([[[1.0], [0.5]], [[1.0], [0.5]]], np.float32)   # [N][H][I]
+        s = oracle.similarity(x, wg, wu, wd)
+        assert abs(s[0, 1] + 1.0) < 1e-12, (c, s[0, 1])
+
+
+def test_similarity_is_frobenius_over_the_stacked_tokens():
+    """The similarity is the cosine of the experts' outputs stacked over all
+    calibration tokens (a Frobenius inner product), not an average of
+    per-token cosines.  Tokens (c, 0) and (0, c); expert 0 has gate = up =
+    (1, 0), so its second output is 0; expert 1 has gate = up = (1, 1), so
+    both its outputs equal the first one of expert 0; both share w_d.  The
+    stacked cosine is exactly 1 / sqrt(2) for every c; per-token cosines
+    would average to 1/2 or 1."""
+    for c in (0.8, 2.5):
+        x = np.array([[c, 0.0], [0.0, c]], np.float32)
+        wg = np.array([[[1.0, 0.0]], [[1.0, 1.0]]], np.float32)
+        wu = wg.copy()
+        wd = np.array([[[2.0], [-1.0]], [[2.0], [-1.0]]], np.float32)
+        s = oracle.similarity(x, wg, wu, wd)
+        assert abs(s[0, 1] - 1.0 / np.sqrt(2.0)) < 1e-12, (c, s[0, 1])
+
+
+def test_silu_shape_through_a_sign():
+    """silu(c) + silu(-c) = c * tanh(c / 2) > 0 for c > 0 (with sigmoid(-g) in
+    place of sigmoid(g) the sum would be -c * tanh(c / 2)).  Expert 0 reads g
+    from x[0] and u = x[2] = 1 on the tokens (c, 0, 1) and (-c, 0, 1), so its
+    outputs are (silu(c), silu(-c)) along w_d; expert 1 has the constant gate
+    and up x[2] = 1, so its outputs are (silu(1), silu(1)) along the same w_d,
+    with silu(1) > 0.  Their similarity therefore has the sign of silu(c) +
+    silu(-c): positive."""
+    for c in (0.5, 2.0, 4.0):
+        x = np.array([[c, 0.0, 1.0], [-c, 0.0, 1.0]], np.float32)
+        wg = np.array([[[1.0, 0.0, 0.0]], [[0.0, 0.0, 1.0]]], np.float32)
+        wu = np.array([[[0.0, 0.0, 1.0]], [[0.0, 0.0, 1.0]]], np.float32)
+        wd = np.array([[[1.0], [1.0], [0.0]], [[1.0], [1.0], [0.0]]], np.float32)
+        s = oracle.similarity(x, wg, wu, wd)
+        assert 0.0 < s[0, 1] < 1.0, (c, s[0, 1])
