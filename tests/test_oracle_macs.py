@@ -81,3 +81,45 @@ def test_bf16_input_uses_exact_values():
     e_bf, _, _ = oracle.token_weights(L.x_bf16, L.is_visual.astype(np.uint8), x_dtype=oracle.DT_BF16)
     e_f, _, _ = oracle.token_weights(L.x, L.is_visual.astype(np.uint8))
     assert np.allclose(e_bf, e_f, atol=1e-12)
+
+
+def test_three_visual_tokens_two_alike_closed_form():
+    """Visual entropies (h, h, g): the population statistics give mu = (2h + g)/3
+    and sigma = |h - g| sqrt(2)/3, so Htilde = s/sqrt(2) for the pair and
+    -s sqrt(2) for the odd one (s = sign(h - g)), whatever h and g are.  A sample
+    (n - 1) variance would give 1/sqrt(3) instead, and statistics taken over the
+    text tokens too would move both values."""
+    D, delta = 96, 1.3
+    z = np.zeros((5, D), np.float32)
+    z[1, 3] = 5.0                   # the odd visual token: lower entropy (g < h)
+    z[3, :7] = 9.0                  # a text token far from the others
+    vis = np.array([1, 1, 0, 0, 1], np.uint8)   # token 2 is a plain text token
+    ent, w, _ = oracle.token_weights(z, vis, delta=delta, eps=0.0)
+    h, g = ent[0], ent[1]
+    assert g < h and ent[4] == h
+    sgm = lambda v: 1.0 / (1.0 + np.exp(-v))
+    assert abs(w[0] - sgm(-delta / np.sqrt(2))) < 1e-12
+    assert abs(w[4] - sgm(-delta / np.sqrt(2))) < 1e-12
+    assert abs(w[1] - sgm(delta * np.sqrt(2))) < 1e-12
+    assert w[2] == 1.0 and w[3] == 1.0
+
+
+def test_visual_weights_ignore_the_text_tokens():
+    """Eq. (5) standardises over the visual tokens only: changing the text
+    tokens' features, or adding more text tokens, leaves every visual weight as
+    it was; R_v alone moves, through the text tokens' weight of 1 each."""
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((30, 80)) * rng.uniform(0.2, 4.0, size=(30, 1))).astype(np.float32)
+    vis = (rng.random(30) < 0.5).astype(np.uint8)
+    vis[:2] = 1
+    _, w1, rv1 = oracle.token_weights(x, vis, delta=1.5)
+    x2 = x.copy()
+    x2[vis == 0] = (rng.standard_normal(((vis == 0).sum(), 80)) * 6.0).astype(np.float32)
+    _, w2, rv2 = oracle.token_weights(x2, vis, delta=1.5)
+    assert np.array_equal(w1, w2) and rv1 == rv2
+    x3 = np.concatenate([x, rng.standard_normal((7, 80)).astype(np.float32)])
+    vis3 = np.concatenate([vis, np.zeros(7, np.uint8)])
+    _, w3, rv3 = oracle.token_weights(x3, vis3, delta=1.5)
+    assert np.array_equal(w3[:30], w1) and np.all(w3[30:] == 1.0)
+    wv = w1[vis == 1].sum()
+    assert abs(rv3 - wv / (wv + (vis == 0).sum() + 7)) < 1e-14
