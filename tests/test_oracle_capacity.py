@@ -37,6 +37,37 @@ def test_fixed_point_weight_and_capacity_value():
         assert C // Q == math.floor(g * T * k / N)
 
 
+
+def test_fixed_point_values_are_exact_floors():
+    """The fixed-point weight is w * 2^24 rounded to nearest (ties to even), and
+    both capacities are exact floors in those units: C = floor(gamma S k / N) and
+    C_j = floor(gamma S k / N * (1 + m_j (R_v - 1/2))), the unfloored static
+    value scaled before the floor.  Checked at arbitrary sums S against exact
+    rationals, away from integers by more than the double evaluation's error
+    (S up to 2^37: 8192 tokens of weight 1)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(24)
+    ws = np.concatenate([rng.random(2000).astype(np.float32),
+                         np.float32([2.0 ** -25, 3 * 2.0 ** -25, 5 * 2.0 ** -26, 2.0 ** -24])])
+    for w in ws:
+        assert oracle.fixed_weight(float(w)) == round(Fraction(float(w)) * Q)   # round(): ties to even
+    checked = 0
+    while checked < 400:
+        S = int(rng.integers(1, 1 << 37))
+        k, N = int(rng.integers(1, 17)), int(rng.integers(2, 257))
+        g = float(np.float32(rng.uniform(0.25, 2.0)))
+        r_v = float(np.float32(rng.random()))
+        m = int(rng.integers(-1, 2))
+        c = Fraction(S) * k * Fraction(g) / N
+        ce = c * (1 + m * (Fraction(r_v) - Fraction(1, 2)))
+        margin = max(Fraction(1, 1000), c * Fraction(1, 1 << 48))   # a few double roundings of c
+        if min(abs(c - round(c)), abs(ce - round(ce))) < margin:
+            continue
+        assert oracle.capacity_value(S, k, g, N) == math.floor(c)
+        assert oracle.capacity_expert(S, k, g, N, m, r_v) == math.floor(ce)
+        checked += 1
+
+
 def _random_case(rng, T, N, k, R, gate_levels=None):
     logits = rng.standard_normal((T, N)).astype(np.float32)
     ids, gates = oracle.route(logits, R)
