@@ -8,22 +8,27 @@
 // w = sigmoid(-delta * Htilde); text tokens weigh 1.  The effective visual
 // ratio R_v = sum_vis w / sum_all w.
 //
-// Kernel 1: one warp per token, H = ln Z - (sum e_d (z_d - m)) / Z with
-// m = max z and e_d = exp(z_d - m) (CUDA's fast exponential intrinsic: its
-// error is far below the entropy's fp32 summation error), fixed lane order and
-// xor butterfly.  A row of up to 2048 features is read once into registers
-// (bf16 rows stay packed, 32 registers a lane) and both passes run from
-// there.  Each CTA leaves the count, sum and sum of squares of its visual
-// tokens' entropies as 64-bit fixed-point integers (2^-32 and 2^-24 units).
+// Kernel 1: one warp per token.  With m = max z and the exponent taken in
+// base 2, u_d = (z_d - m) log2(e) formed by one FMA and e_d = 2^u_d (the
+// hardware's approximate exponential: its error is far below the entropy's
+// fp32 summation error), H = ln Z - ln 2 * (sum e_d u_d) / Z, in a fixed lane
+// order with an xor butterfly.  A row of up to 2048 features is read once
+// into registers (bf16 rows stay packed, 32 registers a lane; their maximum
+// is taken on the packed pairs) and both passes run from there.  A
+// non-finite feature always makes H NaN (NaN propagates, +inf gives
+// inf - inf, -inf gives 0 * -inf), so H itself is the finiteness test.
+// Each CTA leaves the count, sum and sum of squares of its visual tokens'
+// entropies as 64-bit fixed-point integers (2^-32 and 2^-24 units).
 // Kernel 2: one thread per token over ceil(T / 256) CTAs.  Every CTA adds up
 // the kernel-1 partials itself; integer sums do not depend on their order,
-// so every CTA holds the same statistics, converted to mean and 1/(sigma +
-// eps) in double by one thread.  Each thread evaluates its token's sigmoid in
-// fp32; the CTA's (visual, total) weight sums are again fixed-point integers
-// (2^-32 units), which the last CTA to finish (a ticket that kernel 1
-// clears) adds up for R_v.  So the results are reproducible bit for bit,
-// and double precision -- slow on this part -- is used for a few scalar
-// operations only.
+// so every CTA holds the same statistics.  n^2 times the variance is formed
+// exactly from them in 128-bit integers (n sum h^2 - (sum h)^2, no
+// cancellation), then mean and 1/(sigma + eps) in fp32 by one thread: double
+// precision is slow on this part and sits on the critical path here.  Each
+// thread evaluates its token's sigmoid in fp32; the CTA's (visual, total)
+// weight sums are again fixed-point integers (2^-32 units), which the last
+// CTA to finish (a ticket that kernel 1 clears) adds up for R_v.  So the
+// results are reproducible bit for bit.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -69,33 +74,58 @@ constexpr int kEntRegChunks = 8;
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-// Max, then sum of e and e * (z - m), over one lane's chunks of a row.
+constexpr float kL2E = 0x1.715476p+0f;   // log2(e), nearest fp32
+constexpr float kLn2 = 0x1.62e430p-1f;   // ln(2), nearest fp32
+
+// 2^u, the approximate hardware exponential (subnormal results flushed to 0;
+// 2^-inf = 0, NaN stays NaN).
+__device__ __forceinline__ float ex2_approx(float u) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(u));
+    return y;
+}
+
+// Elementwise maximum of two packed bf16 pairs.
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+    __nv_bfloat162 x, y;
+    memcpy(&x, &a, 4);
+    memcpy(&y, &b, 4);
+    const __nv_bfloat162 r = __hmax2(x, y);
+    uint32_t o;
+    memcpy(&o, &r, 4);
+    return o;
+}
+
+// The terms of one feature: e = 2^u with u = z log2(e) - ml, ml = m log2(e).
+__device__ __forceinline__ void ent_term(float z, float ml, float& Z, float& S1) {
+    const float u = fmaf(z, kL2E, -ml);
+    const float e = ex2_approx(u);
+    Z += e;
+    S1 = fmaf(e, u, S1);
+}
+
+// Max, then Z = sum e and S1 = sum e * u (base-2 exponents), over one lane's
+// chunks of a row.
 template <typename XT, bool CACHED>
-__device__ __forceinline__ void entropy_lane_sums(const XT* row, int H, int lane, float& m, float& Z, float& S1,
-                                                  bool& finite) {
-    m = -INFINITY;
-    finite = true;
+__device__ __forceinline__ void entropy_lane_sums(const XT* row, int H, int lane, float& m, float& Z, float& S1) {
     if constexpr (CACHED && sizeof(XT) == 2) {
-        // bf16 row kept packed: 8 x 16 bytes per lane, unpacked in each pass
+        // bf16 row kept packed: 8 x 16 bytes per lane, unpacked in the second pass
         uint4 q[kEntRegChunks];
 #pragma unroll
         for (int c = 0; c < kEntRegChunks; ++c) {
             const int h = lane * 8 + c * 256;
             q[c] = (h < H) ? *reinterpret_cast<const uint4*>(row + h) : make_uint4(0u, 0u, 0u, 0u);
         }
+        uint32_t mx = 0xff80ff80u;   // (-inf, -inf)
 #pragma unroll
         for (int c = 0; c < kEntRegChunks; ++c) {
             if (lane * 8 + c * 256 < H) {
-                const uint32_t u[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float a = bf_lo(u[j]), b = bf_hi(u[j]);
-                    finite &= isfinite(a) && isfinite(b);
-                    m = fmaxf(m, fmaxf(a, b));
-                }
+                mx = bf2_max(mx, bf2_max(bf2_max(q[c].x, q[c].y), bf2_max(q[c].z, q[c].w)));
             }
         }
+        m = fmaxf(bf_lo(mx), bf_hi(mx));
         for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+        const float ml = m * kL2E;
         Z = 0.f;
         S1 = 0.f;
 #pragma unroll
@@ -104,12 +134,8 @@ __device__ __forceinline__ void entropy_lane_sums(const XT* row, int H, int lane
                 const uint32_t u[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float d0 = bf_lo(u[j]) - m, d1 = bf_hi(u[j]) - m;
-                    const float e0 = __expf(d0), e1 = __expf(d1);
-                    Z += e0;
-                    S1 = fmaf(e0, d0, S1);
-                    Z += e1;
-                    S1 = fmaf(e1, d1, S1);
+                    ent_term(bf_lo(u[j]), ml, Z, S1);
+                    ent_term(bf_hi(u[j]), ml, Z, S1);
                 }
             }
         }
@@ -125,56 +151,52 @@ __device__ __forceinline__ void entropy_lane_sums(const XT* row, int H, int lane
                 for (int j = 0; j < 8; ++j) v[c][j] = -INFINITY;
             }
         }
+        m = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kEntRegChunks; ++c) {
             if (lane * 8 + c * 256 < H) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    finite &= isfinite(v[c][j]);
-                    m = fmaxf(m, v[c][j]);
-                }
+                for (int j = 0; j < 8; ++j) m = fmaxf(m, v[c][j]);
             }
         }
         for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+        const float ml = m * kL2E;
         Z = 0.f;
         S1 = 0.f;
 #pragma unroll
         for (int c = 0; c < kEntRegChunks; ++c) {
             if (lane * 8 + c * 256 < H) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float d = v[c][j] - m;
-                    const float e = __expf(d);
-                    Z += e;
-                    S1 = fmaf(e, d, S1);
-                }
+                for (int j = 0; j < 8; ++j) ent_term(v[c][j], ml, Z, S1);
             }
         }
     } else {
+        m = -INFINITY;
         for (int h = lane * 8; h < H; h += 256) {
             float v[8];
             load8(row + h, v);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                finite &= isfinite(v[j]);
-                m = fmaxf(m, v[j]);
-            }
+            for (int j = 0; j < 8; ++j) m = fmaxf(m, v[j]);
         }
         for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+        const float ml = m * kL2E;
         Z = 0.f;
         S1 = 0.f;
         for (int h = lane * 8; h < H; h += 256) {
             float v[8];
             load8(row + h, v);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float d = v[j] - m;
-                const float e = __expf(d);
-                Z += e;
-                S1 = fmaf(e, d, S1);
-            }
+            for (int j = 0; j < 8; ++j) ent_term(v[j], ml, Z, S1);
         }
     }
+}
+
+// An unsigned 128-bit integer to the nearest fp32 or a neighbour (two
+// conversions and one fused rounding: a few ulp).
+__device__ __forceinline__ float u128_to_float(unsigned __int128 v) {
+    const float hi = static_cast<float>(static_cast<unsigned long long>(v >> 64));
+    const float lo = static_cast<float>(static_cast<unsigned long long>(v));
+    return fmaf(hi, 18446744073709551616.0f, lo);   // hi * 2^64 + lo
 }
 
 // Sums of the weights of one CTA of kernel 2 (visual, all), 2^-32 units.
@@ -224,18 +246,16 @@ __global__ void __launch_bounds__(256) token_entropy_kernel(const XT* __restrict
     if (t < T) {   // warp-uniform
         const XT* row = x + static_cast<size_t>(t) * H;
         float m, Z, S1;
-        bool finite;
-        entropy_lane_sums<XT, CACHED>(row, H, lane, m, Z, S1, finite);
+        entropy_lane_sums<XT, CACHED>(row, H, lane, m, Z, S1);
         for (int off = 16; off >= 1; off >>= 1) {
             Z += __shfl_xor_sync(kFull, Z, off);
             S1 += __shfl_xor_sync(kFull, S1, off);
         }
-        const bool all_finite = __all_sync(kFull, finite);
         if (lane == 0) {
-            const float hv = logf(Z) - S1 / Z;
+            const float hv = logf(Z) - kLn2 * (S1 / Z);
             entropy[t] = hv;
             s_h[warp] = hv;
-            if (!all_finite) report(st, MOE_DEV_NONFINITE, t);
+            if (!isfinite(hv)) report(st, MOE_DEV_NONFINITE, t);
         }
     }
     __syncthreads();
@@ -277,17 +297,20 @@ __global__ void __launch_bounds__(256) token_weights_kernel(const float* __restr
         st3[2] += p.s2;
     }
     block_sum_i64<3>(st3, red);
-    // population statistics by one thread: a double division or square root
-    // is tens of fp64 operations, and fp64 throughput per SM is small.  The
-    // one-pass variance is exact to far below the fp32 entropies' rounding:
-    // the sums are exact integers and double keeps 53 bits of each quotient.
+    // population statistics by one thread, without double precision (slow on
+    // this part): n^2 * var * 2^64 = n * S2 * 2^40 - S1^2 exactly in 128-bit
+    // integers (entropies in 2^-32 units, squares in 2^-24), then fp32.
     if (threadIdx.x == 0) {
-        const double nv = static_cast<double>(st3[0]);
-        const double mu = nv > 0.0 ? static_cast<double>(st3[1]) / (nv * 4294967296.0) : 0.0;
-        const double m2 = nv > 0.0 ? static_cast<double>(st3[2]) / (nv * 16777216.0) : 0.0;
-        const double sigma = sqrt(fmax(m2 - mu * mu, 0.0));
-        s_inv = static_cast<float>(1.0 / (sigma + static_cast<double>(eps)));
-        s_mu = static_cast<float>(mu);
+        const long long n = st3[0];
+        float mu = 0.f, sigma = 0.f;
+        if (n > 0) {
+            const float nq = static_cast<float>(n) * 4294967296.0f;   // n * 2^32, exact for n <= 2^24
+            mu = static_cast<float>(st3[1]) / nq;
+            const __int128 num = (static_cast<__int128>(n) * st3[2] << 40) - static_cast<__int128>(st3[1]) * st3[1];
+            sigma = num > 0 ? sqrtf(u128_to_float(static_cast<unsigned __int128>(num))) / nq : 0.f;
+        }
+        s_mu = mu;
+        s_inv = 1.0f / (sigma + eps);
     }
     __syncthreads();
     const float inv = s_inv, muf = s_mu;
@@ -319,7 +342,7 @@ __global__ void __launch_bounds__(256) token_weights_kernel(const float* __restr
     }
     block_sum_i64<2>(tot, red);
     if (threadIdx.x == 0) {
-        *r_v = static_cast<float>(tot[1] > 0 ? static_cast<double>(tot[0]) / static_cast<double>(tot[1]) : 0.0);
+        *r_v = tot[1] > 0 ? static_cast<float>(tot[0]) / static_cast<float>(tot[1]) : 0.f;
         *ticket = 0;
     }
 }

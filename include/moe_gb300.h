@@ -384,15 +384,18 @@ moe_status_t moe_similarity_calibrate(const void* x, int n, const void* w_gate, 
  *              per 8 tokens + 16 per 256 tokens + 16), 256-byte aligned; no
  *              initial contents needed
  * Entropies and weights are computed in fp32 (one warp per token for the
- * entropy); the statistics (count, sum and sum of squares of the visual
- * entropies, population variance) and the two weight sums of R_v are added
+ * entropy, exponentials in base 2); the statistics (count, sum and sum of
+ * squares of the visual entropies) and the two weight sums of R_v are added
  * up as 64-bit fixed-point integers (entropy in 2^-32, its square in 2^-24,
  * weights in 2^-32 units), so results do not depend on summation order and
- * are reproducible bit for bit; mean, variance and R_v are then formed in
- * double.  T is at most 2^24 (MOE_ERR_UNSUPPORTED beyond), which keeps those
+ * are reproducible bit for bit; the population variance is formed from them
+ * exactly in 128-bit integers, then mean, standard deviation and R_v in
+ * fp32.  T is at most 2^24 (MOE_ERR_UNSUPPORTED beyond), which keeps those
  * sums in range.  Two calls must not share a workspace concurrently (it
  * holds a completion counter).
- * A non-finite feature sets MOE_DEV_NONFINITE (detail = token) in st.
+ * A token whose entropy comes out non-finite sets MOE_DEV_NONFINITE (detail =
+ * token) in st: any non-finite feature does so, and so can a row with
+ * features of magnitude 2^126 or more (its base-2 exponents overflow fp32).
  */
 moe_status_t moe_token_weights(const void* x, int x_dtype, int T, int H, const uint8_t* is_visual, float delta,
                                float eps, float* entropy, float* token_w, float* r_v, void* workspace,

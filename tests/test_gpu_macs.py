@@ -14,6 +14,7 @@ import torch
 import oracle
 import expert_routing_moe_gb300 as moe
 from expert_routing_moe_gb300 import synthetic as syn
+from expert_routing_moe_gb300 import _abi as abi
 
 pytestmark = pytest.mark.gpu
 
@@ -201,3 +202,39 @@ def test_token_weights_one_workspace_across_sizes(g):
             outs.append((g.host(ent), g.host(w), float(rv.item())))
         assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
         assert outs[0][2] == outs[1][2]
+
+
+@pytest.mark.parametrize("dtype,H", [("bf16", 2048), ("f32", 512), ("bf16", 4096)])
+@pytest.mark.parametrize("bad", ["nan", "+inf", "-inf"])
+def test_token_weights_report_a_nonfinite_feature(g, dtype, H, bad):
+    """One non-finite feature makes its token's entropy non-finite, which sets
+    MOE_DEV_NONFINITE with that token as detail; the other tokens' entropies
+    are those of the clean batch, bit for bit."""
+    rng = np.random.default_rng(11)
+    T, t_bad, h_bad = 64, 37, H - 3
+    x = (rng.standard_normal((T, H)) * 2.0).astype(np.float32)
+    vis = (rng.random(T) < 0.7).astype(np.uint8)
+    if dtype == "bf16":
+        xb = syn.f32_to_bf16_bits(x)
+        clean = g.dev(xb, torch.bfloat16)
+        xb = xb.copy()
+        xb[t_bad, h_bad] = {"nan": 0x7FC0, "+inf": 0x7F80, "-inf": 0xFF80}[bad]
+        dirty = g.dev(xb, torch.bfloat16)
+    else:
+        clean = g.dev(x)
+        x = x.copy()
+        x[t_bad, h_bad] = {"nan": np.nan, "+inf": np.inf, "-inf": -np.inf}[bad]
+        dirty = g.dev(x)
+    ent_c, _, _ = _gpu_weights(g, clean, vis)
+    ent = torch.empty(T, dtype=torch.float32, device=g.DEV)
+    w = torch.empty(T, dtype=torch.float32, device=g.DEV)
+    rv = torch.empty(1, dtype=torch.float32, device=g.DEV)
+    st = g.status_tensor()
+    moe.moe_token_weights(dirty, g.dev(vis), ent, w, rv, 1.0, 1e-6, st)
+    torch.cuda.synchronize()
+    code, detail = (int(v) for v in st.tolist())
+    assert code == abi.MOE_DEV_NONFINITE and detail == t_bad
+    ent = g.host(ent)
+    assert not np.isfinite(ent[t_bad])
+    keep = np.arange(T) != t_bad
+    assert np.array_equal(ent[keep], ent_c[keep])
