@@ -204,14 +204,16 @@ def test_token_weights_one_workspace_across_sizes(g):
         assert outs[0][2] == outs[1][2]
 
 
-@pytest.mark.parametrize("dtype,H", [("bf16", 2048), ("f32", 512), ("bf16", 4096)])
+@pytest.mark.parametrize("dtype,H,T", [("bf16", 2048, 64), ("f32", 512, 64), ("bf16", 4096, 64),
+                                       ("bf16", 2048, 5000)])
 @pytest.mark.parametrize("bad", ["nan", "+inf", "-inf"])
-def test_token_weights_report_a_nonfinite_feature(g, dtype, H, bad):
+def test_token_weights_report_a_nonfinite_feature(g, dtype, H, T, bad):
     """One non-finite feature makes its token's entropy non-finite, which sets
     MOE_DEV_NONFINITE with that token as detail; the other tokens' entropies
-    are those of the clean batch, bit for bit."""
+    are those of the clean batch, bit for bit (at 5000 rows the per-token grid
+    runs in more than one wave)."""
     rng = np.random.default_rng(11)
-    T, t_bad, h_bad = 64, 37, H - 3
+    t_bad, h_bad = 37, H - 3
     x = (rng.standard_normal((T, H)) * 2.0).astype(np.float32)
     vis = (rng.random(T) < 0.7).astype(np.uint8)
     if dtype == "bf16":
@@ -238,3 +240,4 @@ def test_token_weights_report_a_nonfinite_feature(g, dtype, H, bad):
     assert not np.isfinite(ent[t_bad])
     keep = np.arange(T) != t_bad
     assert np.array_equal(ent[keep], ent_c[keep])
+
