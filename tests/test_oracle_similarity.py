@@ -104,3 +104,35 @@ def test_silu_shape_through_a_sign():
         wd = np.array([[[1.0], [1.0], [0.0]], [[1.0], [1.0], [0.0]]], np.float32)
         s = oracle.similarity(x, wg, wu, wd)
         assert 0.0 < s[0, 1] < 1.0, (c, s[0, 1])
+
+
+def test_silent_expert_with_a_shared_down_projection():
+    """An expert whose gate and up projections are zero outputs exactly zero,
+    so its similarity with every other expert is 0, even when its down
+    projection equals another expert's (I = 3, so each expert's gate/up rows are
+    a block of its own)."""
+    rng = np.random.default_rng(12)
+    n, H, I, N = 5, 6, 3, 3
+    x = rng.standard_normal((n, H)).astype(np.float32)
+    wg = rng.standard_normal((N, I, H)).astype(np.float32)
+    wu = rng.standard_normal((N, I, H)).astype(np.float32)
+    wd = rng.standard_normal((N, H, I)).astype(np.float32)
+    wg[1] = 0.0
+    wu[1] = 0.0
+    wd[1] = wd[0]
+    s = oracle.similarity(x, wg, wu, wd)
+    assert s[0, 1] == 0.0 and s[1, 0] == 0.0 and s[1, 2] == 0.0
+    assert abs(s[0, 2]) < 1.0
+
+
+def test_smallest_sizes():
+    """One token, one feature, one intermediate unit: a single expert with a
+    nonzero output has similarity 1 with itself; two such experts with outputs
+    of opposite sign have -1."""
+    x = np.array([[2.0]], np.float32)
+    one = np.ones((1, 1, 1), np.float32)
+    assert oracle.similarity(x, one, one, one).tolist() == [[1.0]]
+    wd = np.array([[[1.0]], [[-3.0]]], np.float32)
+    two = np.ones((2, 1, 1), np.float32)
+    s = oracle.similarity(x, two, two, wd)
+    assert s[0, 1] == -1.0 and s[0, 0] == 1.0 and s[1, 1] == 1.0
